@@ -1,0 +1,202 @@
+/*
+ * spec_verify.h -- C ABI of the target-side verify step of chain speculative
+ * decoding (a draft of k tokens is checked by one wide target pass).
+ *
+ * The step has three parts, one entry point each:
+ *
+ *   spec_verify_attention  paged GQA attention of the k+1 verify rows of every
+ *                          sequence over a block-paged bf16 KV cache
+ *                          (lmdeploy PR #5019, summary: "paged CuTe
+ *                          verification attention"; onnxruntime-genai PR #2457,
+ *                          fast-commit notes: the "wide batched verify").
+ *   spec_accept            greedy prefix match or speculative (rejection)
+ *                          sampling over vocab-sized logits, giving the number
+ *                          of accepted drafts and the correction/bonus token
+ *                          (lmdeploy PR #5019, summary: "speculative sampling";
+ *                          lmdeploy PR #3945, review of reject_sampler.py;
+ *                          onnxruntime-genai PR #2457: greedy speculation is
+ *                          token-identical to greedy decoding).
+ *   spec_commit_state      copies, for every row, the recurrent-state checkpoint
+ *                          of the accepted prefix into the live gated-delta-net
+ *                          state (onnxruntime-genai PR #2457, notes on per-token
+ *                          state checkpoints and CommitPrefix; lmdeploy PR #5019,
+ *                          fix 2: CommitAcceptedRecurrentStateKernel).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor argument is a DEVICE pointer owned by the caller. The library
+ *    never allocates, frees or synchronises; each call only enqueues kernels on
+ *    `stream` (a cudaStream_t; NULL = legacy default stream) and returns.
+ *  - Return value: SPEC_OK, or a negative SPEC_ERR_* code. Arguments the host
+ *    can check (null pointers, sizes, unsupported shapes, a workspace that is
+ *    too small) are checked before anything is launched; on error nothing is
+ *    enqueued. SPEC_ERR_LAUNCH reports a failed kernel launch.
+ *  - `dev_err` (optional, may be NULL) is a device int32 that kernels OR
+ *    SPEC_DEVERR_* bits into when they meet data they cannot use (for example
+ *    a block id outside the cache). The offending unit is skipped: its outputs
+ *    are written as documented per call and the rest of the batch is computed
+ *    normally. No kernel traps, asserts or aborts. The caller clears the word.
+ *  - All index tensors are int32, row-major, densely packed.
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, without requiring the CUDA headers. */
+typedef struct CUstream_st* spec_stream_t;
+
+/* Status codes. */
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARG (-1)   /* null pointer, negative size, bad enum   */
+#define SPEC_ERR_UNSUPPORTED (-2)   /* a shape this build has no kernel for    */
+#define SPEC_ERR_LAUNCH (-3)        /* cudaLaunch* failed (see cudaGetLastError) */
+#define SPEC_ERR_WORKSPACE (-4)     /* workspace missing or smaller than asked  */
+
+/* Bits OR-ed into *dev_err by the kernels. */
+#define SPEC_DEVERR_BLOCK_ID 1     /* block_table entry outside [0, num_blocks)  */
+#define SPEC_DEVERR_TOKEN 2        /* draft token outside [0, V)                 */
+#define SPEC_DEVERR_ACCEPT_LEN 4   /* accept_len outside [0, S-1]                */
+#define SPEC_DEVERR_CTX_LEN 8      /* ctx_len < k+1 or > max_blocks_per_seq * bs */
+#define SPEC_DEVERR_TEMPERATURE 16 /* sampling row with temperature not > 0      */
+#define SPEC_DEVERR_TIMEOUT 32     /* an asynchronous copy did not arrive        */
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* spec_status_string(int status);
+
+/* ------------------------------------------------------------------------ */
+/* 1. Paged GQA verification attention                                        */
+/* ------------------------------------------------------------------------ */
+
+/* Shapes of one attention call. */
+typedef struct spec_attn_desc {
+  int32_t batch;              /* B: sequences                                  */
+  int32_t num_q_heads;        /* Hq                                            */
+  int32_t num_kv_heads;       /* Hkv; Hq % Hkv == 0, G = Hq / Hkv              */
+  int32_t head_dim;           /* D in {64, 128, 256}                           */
+  int32_t block_size;         /* bs: tokens per KV block, in {16, 32, 64, 128} */
+  int32_t max_blocks_per_seq; /* row stride of block_table                     */
+  int64_t num_blocks;         /* physical blocks in k_cache / v_cache          */
+} spec_attn_desc;
+
+/*
+ * Bytes of device workspace spec_verify_attention needs for `d`: room for the
+ * split-KV partial results (normalised partial outputs and their log-sum-exp)
+ * of the largest split plan the kernel can choose, so the caller may size it
+ * once from the shapes alone. Returns 0 for an invalid descriptor.
+ */
+size_t spec_verify_attention_workspace(const spec_attn_desc* d, int32_t k_draft);
+
+/*
+ * out[b, i, h, :] = softmax_t( q[b,i,h,:] . K[b,t,g,:] / sqrt(D) ) . V[b,t,g,:]
+ * for every sequence b, verify row i in [0, k_draft], query head h, with
+ * g = h / G (contiguous GQA groups) and t over the causal window
+ * t <= ctx_lens[b] - (k_draft+1) + i: row 0 is the last committed token and
+ * row i also sees the first i draft tokens of its own chain.
+ *
+ *  q           [B, k_draft+1, Hq, D] bf16
+ *  k_cache     [num_blocks, bs, Hkv, D] bf16. Token t of sequence b is stored
+ *  v_cache     in physical block block_table[b, t / bs], slot t % bs. The KV of
+ *              the k_draft+1 verify tokens is already in the cache.
+ *  block_table [B, max_blocks_per_seq] int32
+ *  ctx_lens    [B] int32, tokens in the cache per sequence, verify tokens
+ *              included; must lie in [k_draft+1, max_blocks_per_seq * bs].
+ *  out         [B, k_draft+1, Hq, D] fp32
+ *  workspace   >= spec_verify_attention_workspace(d, k_draft) bytes, 256-byte
+ *              aligned, contents need not be initialised and are scratch after
+ *              the call. Two calls in flight at once need two workspaces.
+ *
+ * Long contexts are split across CTAs (split-KV) and the partial results are
+ * merged by their log-sum-exp; the split plan is chosen on the device from
+ * ctx_lens, so no host synchronisation is needed.
+ * Device errors: a sequence with an out-of-range ctx_len (SPEC_DEVERR_CTX_LEN)
+ * or block id (SPEC_DEVERR_BLOCK_ID) gets out rows of zeros.
+ * Supported: D in {64,128,256}; bs in {16,32,64,128}; (k_draft+1)*G <= 64.
+ */
+int spec_verify_attention(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, const int32_t* ctx_lens,
+                          int32_t k_draft, float* out, const spec_attn_desc* d,
+                          void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                          spec_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* 2. Acceptance: greedy prefix match or speculative sampling                  */
+/* ------------------------------------------------------------------------ */
+
+#define SPEC_MODE_GREEDY 0
+#define SPEC_MODE_SAMPLE 1
+
+/*
+ * For each row b (k = number of drafts, R = k+1 target positions):
+ *
+ *  Greedy rows (mode[b] == SPEC_MODE_GREEDY): a_j = argmax_v target_logits[b,j,v]
+ *  (lowest index on ties). accept_len[b] = m = first j < k with
+ *  draft_tokens[b,j] != a_j, else k. Emitted: d_0..d_{m-1}, a_m.
+ *
+ *  Sampling rows (mode[b] == SPEC_MODE_SAMPLE), T = temperature[b] > 0:
+ *  p_j = softmax(target_logits[b,j,:] / T), q_j = draft_probs[b,j,:].
+ *  Draft j is accepted iff u_j * q_j(d_j) < p_j(d_j), u_j uniform in (0,1);
+ *  m = first rejected j, else k. The last emitted token is drawn from
+ *  w = max(0, p_m - q_m) (from p_m itself if that is all zero) when m < k, and
+ *  from p_k when m == k; the draw is an exponential race,
+ *  argmax_x w(x) / E_x with E_x = -ln U_x, which samples x with probability
+ *  w(x) / sum(w) without normalising w.
+ *
+ *  Random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed by
+ *  (philox_seed low word, philox_seed high word). u_j uses word 0 of counter
+ *  (0, j, b, 0); U_x of the race at position m uses word (x mod 4) of counter
+ *  (x / 4, m, b, 1). A word w maps to ((w >> 9) + 0.5) * 2^-23.
+ *
+ *  target_logits [B, k+1, V] fp32
+ *  draft_tokens  [B, k] int32
+ *  draft_probs   [B, k, V] fp32, each row a distribution; may be NULL only if
+ *                every row is greedy
+ *  mode          [B] int32 (SPEC_MODE_*); temperature [B] fp32 (ignored for
+ *                greedy rows)
+ *  out_tokens    [B, k+1] int32: d_0..d_{m-1}, final token, then -1 padding
+ *  accept_len    [B] int32: m in [0, k]
+ *
+ * Rows are read only up to the first rejection (early exit), so the bytes read
+ * depend on the outcome.
+ * Device errors: a row with a draft token outside [0, V) (SPEC_DEVERR_TOKEN)
+ * or a sampling row with temperature not > 0 (SPEC_DEVERR_TEMPERATURE) gets
+ * out_tokens all -1 and accept_len -1.
+ */
+int spec_accept(const float* target_logits, const int32_t* draft_tokens,
+                const float* draft_probs, uint64_t philox_seed, const int32_t* mode,
+                const float* temperature, int32_t* out_tokens, int32_t* accept_len,
+                int32_t batch, int32_t k_draft, int32_t vocab, int32_t* dev_err,
+                spec_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* 3. Recurrent-state commit                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * live_state[l, b, :] = snapshots[l, b, accept_len[b], :] for every layer l
+ * and row b. Snapshot slot s holds the state after the verify step consumed
+ * its input s (input 0 is the last committed token), so slot accept_len[b] is
+ * the state of the accepted prefix.
+ *
+ *  snapshots  [L, B, S, state_elems] fp32
+ *  accept_len [B] int32 (as written by spec_accept)
+ *  live_state [L, B, state_elems] fp32
+ *
+ * The copy is bit-exact. A row whose accept_len lies outside [0, S-1] keeps
+ * its live state unchanged and sets SPEC_DEVERR_ACCEPT_LEN.
+ */
+int spec_commit_state(const float* snapshots, const int32_t* accept_len,
+                      float* live_state, int32_t num_layers, int32_t batch,
+                      int32_t num_slots, int64_t state_elems, int32_t* dev_err,
+                      spec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H_ */

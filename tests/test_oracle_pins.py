@@ -1,0 +1,424 @@
+"""Pins of the CPU oracle to facts outside itself (CPU only).
+
+Each test ties one oracle function to something it does not compute: published
+known-answer vectors, closed forms, library routines (numpy argmax, scipy's
+logistic function and chi-square test), invariances of the definition, or the
+output layout printed on the pages. A plausible slip in the oracle (a dropped
+scale, a wrong slot or block index, a transposed head mapping, a sign error in
+the residual, a wrong Philox counter) fails at least one of them.
+"""
+
+import os
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (nearest even) and return the bit patterns."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------
+# Philox and the uniform map
+# --------------------------------------------------------------------------
+
+def test_philox_known_answer_vectors(oracle_mod):
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "philox4x32_10_kat.txt"))
+            if l.strip() and not l.startswith("#")]
+    assert len(rows) == 3
+    for r in rows:
+        vals = [int(v, 16) for v in r]
+        out = oracle_mod.philox4x32_10(vals[0:4], vals[4:6])
+        assert [int(v) for v in out] == vals[6:10]
+
+
+def test_uniform_map_endpoints(oracle_mod):
+    assert oracle_mod.uniform(0) == 2.0 ** -24
+    assert oracle_mod.uniform(0xFFFFFFFF) == 1.0 - 2.0 ** -24
+    assert oracle_mod.uniform(1 << 31) == 0.5 + 2.0 ** -24
+    # the low 9 bits are dropped
+    assert oracle_mod.uniform(0x1FF) == oracle_mod.uniform(0)
+
+
+# --------------------------------------------------------------------------
+# Attention
+# --------------------------------------------------------------------------
+
+def _paged(rng, ctx, Hkv, D, bs, *, contiguous_k=None, contiguous_v=None, spare=2, perm=True):
+    """Lay contiguous per-sequence K/V [B][ctx_b, Hkv, D] out in a shuffled paged cache."""
+    B = len(ctx)
+    nblk = [-(-c // bs) for c in ctx]
+    nb = sum(nblk) + spare
+    order = rng.permutation(nb) if perm else np.arange(nb)
+    kc = np.zeros((nb, bs, Hkv, D), np.uint16)
+    vc = np.zeros((nb, bs, Hkv, D), np.uint16)
+    table = np.full((B, max(nblk)), -1, np.int32)
+    pos = 0
+    for b in range(B):
+        for n in range(nblk[b]):
+            phys = order[pos]
+            pos += 1
+            table[b, n] = phys
+            lo, hi = n * bs, min(ctx[b], (n + 1) * bs)
+            kc[phys, : hi - lo] = contiguous_k[b][lo:hi]
+            vc[phys, : hi - lo] = contiguous_v[b][lo:hi]
+    return kc, vc, table
+
+
+def _random_case(rng, ctx, R, Hq, Hkv, D):
+    q = bf16_bits(rng.standard_normal((len(ctx), R, Hq, D)).astype(np.float32))
+    ks = [bf16_bits(rng.standard_normal((c, Hkv, D)).astype(np.float32)) for c in ctx]
+    vs = [bf16_bits(rng.standard_normal((c, Hkv, D)).astype(np.float32)) for c in ctx]
+    return q, ks, vs
+
+
+def test_attention_block_layout_invariance(oracle_mod):
+    """The result depends on the tokens, not on block size or physical placement."""
+    rng = np.random.default_rng(1)
+    ctx, R, Hq, Hkv, D = [5, 23, 40], 4, 6, 2, 16
+    q, ks, vs = _random_case(rng, ctx, R, Hq, Hkv, D)
+    ref = None
+    for bs, perm in [(1, False), (4, True), (16, True), (64, False)]:
+        kc, vc, table = _paged(rng, ctx, Hkv, D, bs, contiguous_k=ks, contiguous_v=vs, perm=perm)
+        out = oracle_mod.verify_attention(q, kc, vc, table, np.array(ctx, np.int32))
+        if ref is None:
+            ref = out
+        else:
+            assert np.array_equal(out, ref)
+
+
+def test_attention_single_visible_key_returns_its_value(oracle_mod):
+    """ctx = k+1: row 0 sees only token 0, so its output is v_0 exactly."""
+    rng = np.random.default_rng(2)
+    ctx, R, Hq, Hkv, D = [4, 4], 4, 4, 2, 32
+    q, ks, vs = _random_case(rng, ctx, R, Hq, Hkv, D)
+    kc, vc, table = _paged(rng, ctx, Hkv, D, 2, contiguous_k=ks, contiguous_v=vs)
+    out = oracle_mod.verify_attention(q, kc, vc, table, np.array(ctx, np.int32))
+    G = Hq // Hkv
+    for b in range(2):
+        for h in range(Hq):
+            assert np.array_equal(out[b, 0, h], bits_to_f64(vs[b][0, h // G]))
+
+
+def test_attention_two_keys_closed_form(oracle_mod):
+    """Row 1 with ctx = k+1 sees tokens 0 and 1: o = sigmoid(s0-s1) v0 + sigmoid(s1-s0) v1."""
+    rng = np.random.default_rng(3)
+    ctx, R, Hq, Hkv, D = [4], 4, 2, 1, 64
+    q, ks, vs = _random_case(rng, ctx, R, Hq, Hkv, D)
+    kc, vc, table = _paged(rng, ctx, Hkv, D, 4, contiguous_k=ks, contiguous_v=vs)
+    out = oracle_mod.verify_attention(q, kc, vc, table, np.array(ctx, np.int32))
+    k0, k1 = bits_to_f64(ks[0][0, 0]), bits_to_f64(ks[0][1, 0])
+    v0, v1 = bits_to_f64(vs[0][0, 0]), bits_to_f64(vs[0][1, 0])
+    for h in range(Hq):
+        qq = bits_to_f64(q[0, 1, h])
+        s0, s1 = qq @ k0 / 8.0, qq @ k1 / 8.0  # 1/sqrt(64)
+        want = special.expit(s0 - s1) * v0 + special.expit(s1 - s0) * v1
+        np.testing.assert_allclose(out[0, 1, h], want, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_zero_query_gives_mean_of_visible_values(oracle_mod):
+    rng = np.random.default_rng(4)
+    ctx, R, Hq, Hkv, D = [9, 31], 4, 4, 2, 8
+    q, ks, vs = _random_case(rng, ctx, R, Hq, Hkv, D)
+    q[:] = 0
+    kc, vc, table = _paged(rng, ctx, Hkv, D, 4, contiguous_k=ks, contiguous_v=vs)
+    out = oracle_mod.verify_attention(q, kc, vc, table, np.array(ctx, np.int32))
+    G = Hq // Hkv
+    for b, c in enumerate(ctx):
+        for i in range(R):
+            n_vis = c - R + i + 1
+            for h in range(Hq):
+                want = bits_to_f64(vs[b][:n_vis, h // G]).mean(axis=0)
+                np.testing.assert_allclose(out[b, i, h], want, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_causal_window(oracle_mod):
+    """Row i sees tokens t <= ctx - R + i and nothing later."""
+    rng = np.random.default_rng(5)
+    ctx, R, Hq, Hkv, D = [12], 4, 2, 1, 16
+    q, ks, vs = _random_case(rng, ctx, R, Hq, Hkv, D)
+    kc, vc, table = _paged(rng, ctx, Hkv, D, 4, contiguous_k=ks, contiguous_v=vs)
+    base = oracle_mod.verify_attention(q, kc, vc, table, np.array(ctx, np.int32))
+    P = ctx[0] - R
+    for t in range(P, ctx[0]):  # perturb token t (its key and value)
+        ks2 = [ks[0].copy()]
+        vs2 = [vs[0].copy()]
+        ks2[0][t] = bf16_bits(rng.standard_normal((Hkv, D)).astype(np.float32))
+        vs2[0][t] = bf16_bits(rng.standard_normal((Hkv, D)).astype(np.float32))
+        kc2, vc2, table2 = _paged(rng, ctx, Hkv, D, 4, contiguous_k=ks2, contiguous_v=vs2)
+        out = oracle_mod.verify_attention(q, kc2, vc2, table2, np.array(ctx, np.int32))
+        for i in range(R):
+            if t <= P + i:
+                assert not np.array_equal(out[0, i], base[0, i])
+            else:
+                assert np.array_equal(out[0, i], base[0, i])
+
+
+def test_attention_gqa_groups_are_contiguous(oracle_mod):
+    """With V constant per kv head, query head h returns the constant of kv head h // G."""
+    rng = np.random.default_rng(6)
+    ctx, R, Hq, Hkv, D = [20, 7], 4, 8, 4, 8
+    q, ks, vs = _random_case(rng, ctx, R, Hq, Hkv, D)
+    consts = np.array([1.0, -2.0, 0.5, 3.0], np.float32)
+    for b in range(len(ctx)):
+        vs[b][:] = bf16_bits(np.broadcast_to(consts[None, :, None], (ctx[b], Hkv, D)).copy())
+    kc, vc, table = _paged(rng, ctx, Hkv, D, 8, contiguous_k=ks, contiguous_v=vs)
+    out = oracle_mod.verify_attention(q, kc, vc, table, np.array(ctx, np.int32))
+    G = Hq // Hkv
+    for h in range(Hq):
+        np.testing.assert_allclose(out[:, :, h, :], consts[h // G], rtol=1e-12)
+
+
+def test_attention_subset_matches_full(oracle_mod):
+    rng = np.random.default_rng(7)
+    ctx, R, Hq, Hkv, D = [6, 17, 33, 9], 4, 4, 2, 16
+    q, ks, vs = _random_case(rng, ctx, R, Hq, Hkv, D)
+    kc, vc, table = _paged(rng, ctx, Hkv, D, 4, contiguous_k=ks, contiguous_v=vs)
+    full = oracle_mod.verify_attention(q, kc, vc, table, np.array(ctx, np.int32))
+    sub = oracle_mod.verify_attention(q, kc, vc, table, np.array(ctx, np.int32), seqs=[3, 1])
+    assert np.array_equal(sub[0], full[3]) and np.array_equal(sub[1], full[1])
+
+
+def test_attention_rejects_bad_block_and_ctx(oracle_mod):
+    rng = np.random.default_rng(8)
+    ctx, R, Hq, Hkv, D = [8, 8], 4, 2, 1, 8
+    q, ks, vs = _random_case(rng, ctx, R, Hq, Hkv, D)
+    kc, vc, table = _paged(rng, ctx, Hkv, D, 4, contiguous_k=ks, contiguous_v=vs)
+    bad = table.copy()
+    bad[1, 1] = kc.shape[0]
+    out = oracle_mod.verify_attention(q, kc, vc, bad, np.array(ctx, np.int32), check=False)
+    with pytest.raises(oracle_mod.OracleError) as e:
+        oracle_mod.verify_attention(q, kc, vc, bad, np.array(ctx, np.int32))
+    assert e.value.code == -5
+    assert np.all(out[1] == 0) and np.any(out[0] != 0)
+    with pytest.raises(oracle_mod.OracleError) as e:
+        oracle_mod.verify_attention(q, kc, vc, table, np.array([3, 8], np.int32))
+    assert e.value.code == -6
+
+
+# --------------------------------------------------------------------------
+# Greedy acceptance
+# --------------------------------------------------------------------------
+
+def test_greedy_equals_sequential_greedy_decoding(oracle_mod):
+    """Speculative greedy output = the target's own greedy tokens, cut after the first miss."""
+    rng = np.random.default_rng(10)
+    B, k, V = 64, 5, 50
+    L = rng.standard_normal((B, k + 1, V)).astype(np.float32)
+    seq_greedy = np.argmax(L, axis=-1)  # sequential greedy decoding of the same logits
+    m_true = rng.integers(0, k + 1, B)
+    d = seq_greedy[:, :k].copy()
+    for b in range(B):
+        if m_true[b] < k:
+            d[b, m_true[b]] = (seq_greedy[b, m_true[b]] + 1 + rng.integers(0, V - 1)) % V
+    tok, alen, _, _, rc = oracle_mod.accept(L, d, None, 0, np.zeros(B, np.int32), np.ones(B, np.float32))
+    assert rc == 0
+    assert np.array_equal(alen, m_true)
+    for b in range(B):
+        m = m_true[b]
+        assert np.array_equal(tok[b, : m + 1], seq_greedy[b, : m + 1])
+        assert np.all(tok[b, m + 1:] == -1)
+
+
+def test_greedy_reject_sampler_fixture(oracle_mod):
+    rows = [l for l in open(os.path.join(GOLDEN, "reject_sampler_fixture.txt"))
+            if l.startswith("row")]
+    drafts, argmaxes, expected = [], [], []
+    for r in rows:
+        a, b, c = r[3:].split("|")
+        drafts.append([int(x) for x in a.split()])
+        argmaxes.append([int(x) for x in b.split()])
+        expected.append([int(x) for x in c.split()])
+    B, k, V = 3, 2, 4
+    L = np.zeros((B, k + 1, V), np.float32)
+    for b in range(B):
+        for j in range(k + 1):
+            L[b, j, argmaxes[b][j]] = 5.0
+    tok, alen, _, _, _ = oracle_mod.accept(L, np.array(drafts, np.int32), None, 0,
+                                           np.zeros(B, np.int32), np.ones(B, np.float32))
+    assert tok.tolist() == expected
+    assert alen.tolist() == [2, 0, 0]
+
+
+def test_greedy_ties_go_to_lowest_index(oracle_mod):
+    L = np.zeros((1, 2, 6), np.float32)
+    L[0, 0, [2, 4]] = 1.0
+    L[0, 1, [1, 5]] = 3.0
+    tok, alen, _, _, _ = oracle_mod.accept(L, np.array([[2]], np.int32), None, 0,
+                                           np.zeros(1, np.int32), np.ones(1, np.float32))
+    assert alen[0] == 1 and tok[0].tolist() == [2, 1]
+    tok, alen, _, _, _ = oracle_mod.accept(L, np.array([[4]], np.int32), None, 0,
+                                           np.zeros(1, np.int32), np.ones(1, np.float32))
+    assert alen[0] == 0 and tok[0].tolist() == [2, -1]
+
+
+# --------------------------------------------------------------------------
+# Speculative sampling
+# --------------------------------------------------------------------------
+
+def _softmax(x):
+    e = np.exp(x - x.max(-1, keepdims=True))
+    return e / e.sum(-1, keepdims=True)
+
+
+def _chi2_ok(samples, probs, n_min=5):
+    counts = np.bincount(samples, minlength=len(probs)).astype(np.float64)
+    exp = probs * counts.sum()
+    keep = exp >= n_min
+    obs = np.append(counts[keep], counts[~keep].sum())
+    ex = np.append(exp[keep], exp[~keep].sum())
+    if ex[-1] == 0:
+        obs, ex = obs[:-1], ex[:-1]
+    return stats.chisquare(obs, ex).pvalue
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_sampling_first_token_follows_target(oracle_mod, T):
+    """Speculative sampling emits a first token distributed as p_0 = softmax(l_0/T)."""
+    rng = np.random.default_rng(11)
+    B, k, V = 200_000, 2, 8
+    l0 = rng.normal(0, 1.5, (k + 1, V)).astype(np.float32)
+    dl = (l0[:k] + rng.normal(0, 1.0, (k, V))).astype(np.float32)
+    q = _softmax(dl.astype(np.float64) / T).astype(np.float32)
+    L = np.broadcast_to(l0, (B, k + 1, V))
+    Q = np.broadcast_to(q, (B, k, V))
+    d = np.stack([rng.choice(V, B, p=q[j] / q[j].sum()) for j in range(k)], 1).astype(np.int32)
+    tok, alen, margin, gap, rc = oracle_mod.accept(L, d, Q, 1234, np.ones(B, np.int32),
+                                                   np.full(B, T, np.float32))
+    assert rc == 0
+    p0 = _softmax(l0[0].astype(np.float64) / T)
+    assert _chi2_ok(tok[:, 0], p0) > 1e-3
+    # given d_0 accepted, the second token follows p_1
+    sel = alen >= 1
+    p1 = _softmax(l0[1].astype(np.float64) / T)
+    assert _chi2_ok(tok[sel, 1], p1) > 1e-3
+    # and the plain acceptance rate equals sum_x min(p, q)
+    acc_rate = np.mean(alen >= 1)
+    want = np.minimum(p0, q[0].astype(np.float64)).sum()
+    assert abs(acc_rate - want) < 5 * np.sqrt(want * (1 - want) / B)
+    # an unrelated statistic must fail the same test (the check has power)
+    assert _chi2_ok(tok[:, 0], q[0].astype(np.float64) / q[0].sum()) < 1e-3
+
+
+def test_sampling_bonus_token_follows_last_target_row(oracle_mod):
+    """With q = p every draft is accepted and the bonus token follows p_k."""
+    rng = np.random.default_rng(12)
+    B, k, V = 100_000, 2, 16
+    L = np.zeros((B, k + 1, V), np.float32)  # p_j uniform: 1/16 exactly
+    lk = rng.normal(0, 1.0, V).astype(np.float32)
+    L[:, k] = lk
+    Q = np.full((B, k, V), 1.0 / 16, np.float32)
+    d = rng.integers(0, V, (B, k)).astype(np.int32)
+    tok, alen, _, _, _ = oracle_mod.accept(L, d, Q, 99, np.ones(B, np.int32), np.ones(B, np.float32))
+    assert np.all(alen == k)
+    assert np.array_equal(tok[:, :k], d)
+    assert _chi2_ok(tok[:, k], _softmax(lk.astype(np.float64))) > 1e-3
+
+
+def test_sampling_zero_target_probability_always_rejects(oracle_mod):
+    B, k, V = 1000, 3, 10
+    L = np.zeros((B, k + 1, V), np.float32)
+    L[:, 0, 3] = -1e30  # p_0(3) = 0
+    Q = np.full((B, k, V), 0.1, np.float32)
+    d = np.full((B, k), 3, np.int32)
+    tok, alen, _, _, _ = oracle_mod.accept(L, d, Q, 5, np.ones(B, np.int32), np.ones(B, np.float32))
+    assert np.all(alen == 0)
+    assert np.all(tok[:, 0] != 3) and np.all(tok[:, 1:] == -1)
+
+
+def test_sampling_residual_support(oracle_mod):
+    """p = (1/2, 1/2, 0, ...), q = (1/4, 3/4, 0, ...): a rejected draft 1 resamples token 0."""
+    B, k, V = 20_000, 1, 4
+    L = np.full((B, k + 1, V), -1e30, np.float32)
+    L[:, 0, 0] = 0.0
+    L[:, 0, 1] = 0.0
+    L[:, 1, :] = 0.0
+    Q = np.zeros((B, k, V), np.float32)
+    Q[:, 0, 0], Q[:, 0, 1] = 0.25, 0.75
+    d = np.ones((B, k), np.int32)
+    tok, alen, _, _, _ = oracle_mod.accept(L, d, Q, 7, np.ones(B, np.int32), np.ones(B, np.float32))
+    rej = alen == 0
+    assert np.all(tok[rej, 0] == 0)
+    # P(accept) = p/q = 2/3
+    assert abs(np.mean(~rej) - 2 / 3) < 0.02
+
+
+def test_sampling_uniform_uses_documented_counter(oracle_mod):
+    """u_j is word 0 of Philox counter (0, j, b, 0) under key (seed lo, seed hi)."""
+    B, k, V = 64, 2, 4
+    seed = 0x0123456789ABCDEF
+    L = np.zeros((B, k + 1, V), np.float32)
+    L[:, 0, :] = np.log(np.array([0.5, 0.2, 0.2, 0.1], np.float32))
+    Q = np.zeros((B, k, V), np.float32)
+    Q[:, :, 0] = 1.0  # one-hot q: accept draft 0 iff u_0 < p_0(0) = 0.5
+    d = np.zeros((B, k), np.int32)
+    tok, alen, _, _, _ = oracle_mod.accept(L, d, Q, seed, np.ones(B, np.int32), np.ones(B, np.float32))
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for b in range(B):
+        u0 = oracle_mod.uniform(oracle_mod.philox4x32_10([0, 0, b, 0], key)[0])
+        assert (alen[b] >= 1) == (u0 < 0.5)
+
+
+def test_sampling_is_deterministic_per_seed(oracle_mod):
+    rng = np.random.default_rng(13)
+    B, k, V = 256, 3, 64
+    L = rng.normal(0, 2, (B, k + 1, V)).astype(np.float32)
+    Q = _softmax(L[:, :k] + rng.normal(0, 1, (B, k, V))).astype(np.float32)
+    d = rng.integers(0, V, (B, k)).astype(np.int32)
+    args = (L, d, Q)
+    a = oracle_mod.accept(*args, 42, np.ones(B, np.int32), np.ones(B, np.float32))
+    b = oracle_mod.accept(*args, 42, np.ones(B, np.int32), np.ones(B, np.float32))
+    c = oracle_mod.accept(*args, 43, np.ones(B, np.int32), np.ones(B, np.float32))
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert not np.array_equal(a[0], c[0])
+
+
+def test_accept_invalid_rows(oracle_mod):
+    B, k, V = 3, 2, 5
+    L = np.zeros((B, k + 1, V), np.float32)
+    Q = np.full((B, k, V), 0.2, np.float32)
+    d = np.array([[0, 1], [5, 0], [1, 1]], np.int32)
+    temp = np.array([1.0, 1.0, 0.0], np.float32)
+    tok, alen, _, _, rc = oracle_mod.accept(L, d, Q, 1, np.array([1, 1, 1], np.int32), temp, check=False)
+    assert rc != 0
+    assert alen[0] >= 0 and alen[1] == -1 and alen[2] == -1
+    assert np.all(tok[1] == -1) and np.all(tok[2] == -1)
+
+
+# --------------------------------------------------------------------------
+# State commit
+# --------------------------------------------------------------------------
+
+def test_commit_picks_accepted_slot(oracle_mod):
+    rng = np.random.default_rng(20)
+    L, B, S, E = 3, 5, 4, 12
+    snaps = rng.standard_normal((L, B, S, E)).astype(np.float32)
+    alen = np.array([0, 3, 1, 2, 3], np.int32)  # 3 = k: the last snapshot
+    live = np.zeros((L, B, E), np.float32)
+    assert oracle_mod.commit_state(snaps, alen, live) == 0
+    for l in range(L):
+        for b in range(B):
+            assert np.array_equal(live[l, b], snaps[l, b, alen[b]])
+    assert np.array_equal(live[:, 1], snaps[:, 1, S - 1])
+    assert np.array_equal(live[:, 0], snaps[:, 0, 0])
+
+
+def test_commit_skips_invalid_rows(oracle_mod):
+    rng = np.random.default_rng(21)
+    L, B, S, E = 2, 3, 4, 8
+    snaps = rng.standard_normal((L, B, S, E)).astype(np.float32)
+    live = np.full((L, B, E), 7.0, np.float32)
+    rc = oracle_mod.commit_state(snaps, np.array([1, 4, -1], np.int32), live, check=False)
+    assert rc == -7
+    assert np.array_equal(live[:, 0], snaps[:, 0, 1])
+    assert np.all(live[:, 1:] == 7.0)
