@@ -1,0 +1,436 @@
+"""Benchmark of the speculative-decoding verify step on GB300.
+
+One step = one pass of the whole verify path over one batch of synthetic
+inputs already resident in HBM: paged verify attention (one attention layer),
+acceptance (rejection sampling at the workload's temperature, or greedy), and,
+for workloads with gated-delta-net layers, the recurrent-state commit.
+
+Metric: verified tokens/s = sum_b (accept_len_b + 1) / step time.
+
+Prints one JSON line (rank 0). `--impl reference` times the CPU oracle instead
+(on the host cores, a bounded sample of the same workload, scaled to the same
+metric).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from speculative_decoding_verification_paged_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verified tokens/s per verify step (1 GB300); verify-attn & accept HBM GB/s vs peak"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "llama8b_eagle3"
+L2_FLUSH_BYTES = 512 << 20
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+ATTN_SOURCE = os.path.join(ROOT, "speculative_decoding_verification_paged_gb300", "csrc", "attention.cu")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default=DEFAULT_WORKLOAD, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--mode", default=None, choices=[None, "sample", "greedy", "mixed"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; each rank verifies its own batch)
+# --------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# algorithmic bytes
+# --------------------------------------------------------------------------
+def attention_bytes(w, ctx_lens):
+    ctx = [int(c) for c in ctx_lens]
+    kv = sum(ctx) * w.num_kv_heads * w.head_dim * 2 * 2
+    qo = w.batch * w.rows * w.num_q_heads * w.head_dim * (2 + 4)
+    table = sum(-(-c // w.block_size) for c in ctx) * 4 + w.batch * 4
+    return kv + qo + table
+
+
+def accept_bytes(w, modes, accept_len):
+    V, k = w.vocab, w.k_draft
+    total = 0
+    for md, m in zip(modes, accept_len):
+        m = int(m)
+        if m < 0:
+            continue
+        total += (m + 1) * 4 * V
+        if md == 1:
+            total += (4 * V if m < k else 0) + 32 * m
+    total += w.batch * (k * 4 + 4 + 4 + (k + 1) * 4 + 4)  # drafts, mode, temperature, out_tokens, accept_len
+    return total
+
+
+def commit_bytes(w):
+    return 2 * w.gdn_layers * w.batch * w.state_elems * 4 if w.gdn_layers else 0
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per attention call from an ncu capture, if taken on the current source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    src = hashlib.sha256(open(ATTN_SOURCE, "rb").read()).hexdigest()
+    entry = rec.get(workload)
+    if not entry or entry.get("attention_source_sha256") != src:
+        return None
+    return entry.get("dram_bytes_per_call")
+
+
+# --------------------------------------------------------------------------
+# native arm
+# --------------------------------------------------------------------------
+def run_native(args, world, rank, local):
+    import speculative_decoding_verification_paged_gb300 as sv
+
+    sv.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = wl.WORKLOADS[args.config]
+    mode = args.mode or w.mode
+    a = wl.make_attention_inputs(w, device=dev, seed=w.seed + 1000 * rank)
+    acc_in = wl.make_accept_inputs(w, device=dev, seed=w.seed + 1000 * rank, mode=mode)
+    g = wl.make_gdn_inputs(w, device=dev, seed=w.seed + 1000 * rank) if w.gdn_layers else None
+    B, R = w.batch, w.rows
+    out = torch.empty((B, R, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+    ws = torch.empty(sv.spec_verify_attention_workspace(a["q"], a["k_cache"], a["block_table"], w.k_draft),
+                     dtype=torch.uint8, device=dev)
+    toks = torch.empty((B, R), dtype=torch.int32, device=dev)
+    alen = torch.empty((B,), dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sv.spec_verify_attention(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["ctx_lens"], w.k_draft, out,
+                                 workspace=ws, dev_err=err)
+        ev[1].record(stream)
+        sv.spec_accept(acc_in["target_logits"], acc_in["draft_tokens"], acc_in["draft_probs"],
+                       acc_in["philox_seed"], acc_in["mode"], acc_in["temperature"], toks, alen, dev_err=err)
+        ev[2].record(stream)
+        if g is not None:
+            sv.spec_commit_state(g["snapshots"], alen, g["live_state"], dev_err=err)
+
+    launches_per_step = 3 + 1 + (1 if g is not None else 0)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        ev[0].record(stream)
+        step()
+        ev[3].record(stream)
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())}")
+
+    per_step, t_attn, t_acc, t_cmt = [], [], [], []
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start
+    for _ in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        ev[0].record(stream)
+        step()
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        per_step.append(ev[0].elapsed_time(ev[3]))
+        t_attn.append(ev[0].elapsed_time(ev[1]))
+        t_acc.append(ev[1].elapsed_time(ev[2]))
+        t_cmt.append(ev[2].elapsed_time(ev[3]))
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+
+    ms = statistics.mean(per_step)
+    alen_h = alen.cpu().numpy()
+    tokens = float(np.sum(alen_h + 1))
+    ms_max = reduce_max(ms, world)
+    tokens_all = reduce_sum(tokens, world)
+    value = tokens_all / (ms_max / 1e3)
+
+    peak, peak_kind = measured_peaks()
+    ctx = a["ctx_lens"].cpu().numpy()
+    ab = attention_bytes(w, ctx)
+    cb = accept_bytes(w, acc_in["mode"].cpu().numpy(), alen_h)
+    mb = commit_bytes(w)
+    ta, tc, tm = statistics.mean(t_attn), statistics.mean(t_acc), statistics.mean(t_cmt)
+    kernels = {
+        "attention": {"ms": ta, "bytes": ab, "GBps": ab / ta / 1e6, "frac": ab / ta / 1e6 / peak},
+        "accept": {"ms": tc, "bytes": cb, "GBps": cb / tc / 1e6, "frac": cb / tc / 1e6 / peak,
+                   "full_read_bytes": w.batch * 4 * w.vocab * (R + w.k_draft)},
+    }
+    if g is not None:
+        kernels["commit"] = {"ms": tm, "bytes": mb, "GBps": mb / tm / 1e6, "frac": mb / tm / 1e6 / peak}
+    dominant = max(kernels, key=lambda k: kernels[k]["ms"])
+    dk = kernels[dominant]
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["GBps"], "peak": peak, "unit": "GB/s",
+                "frac": dk["frac"], "peak_source": peak_kind,
+                "traffic": recorded_traffic(args.config) if dominant == "attention" else None}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(sv, w, a, acc_in, g, out, ws, toks, alen, err, dev, args, flush)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch_per_gpu": w.batch, "k_draft": w.k_draft, "mode": mode,
+                   "ctx": list(w.ctx_range) if w.ctx_range else sorted(set(w.ctx_lens)),
+                   "block_size": w.block_size, "heads": [w.num_q_heads, w.num_kv_heads], "head_dim": w.head_dim,
+                   "vocab": w.vocab, "gdn_layers": w.gdn_layers, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between timed steps (512 MiB write)"},
+        "verified_tokens_per_step": tokens_all, "mean_accept_len": float(np.mean(alen_h)),
+        "kernels": kernels, "roofline": roofline, "clocks": clk, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    return result
+
+
+def run_e2e(sv, w, a, acc_in, g, out, ws, toks, alen, err, dev, args, flush):
+    """Same metric through the public API with the step's inputs in pinned host memory."""
+    names = ["q", "k_cache", "v_cache", "block_table", "ctx_lens"]
+    host = {n: a[n].cpu().pin_memory() for n in names}
+    for n in ["target_logits", "draft_tokens", "draft_probs", "mode", "temperature"]:
+        host[n] = acc_in[n].cpu().pin_memory()
+    devbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    toks_h = torch.empty(toks.shape, dtype=toks.dtype).pin_memory()
+    alen_h = torch.empty(alen.shape, dtype=alen.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * 4 + toks_h.numel() * 4 + alen_h.numel() * 4
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def step():
+        for n, t in host.items():
+            devbuf[n].copy_(t, non_blocking=True)
+        sv.spec_verify_attention(devbuf["q"], devbuf["k_cache"], devbuf["v_cache"], devbuf["block_table"],
+                                 devbuf["ctx_lens"], w.k_draft, out, workspace=ws, dev_err=err)
+        sv.spec_accept(devbuf["target_logits"], devbuf["draft_tokens"], devbuf["draft_probs"],
+                       acc_in["philox_seed"], devbuf["mode"], devbuf["temperature"], toks, alen, dev_err=err)
+        if g is not None:
+            sv.spec_commit_state(g["snapshots"], alen, g["live_state"], dev_err=err)
+        out_h.copy_(out, non_blocking=True)
+        toks_h.copy_(toks, non_blocking=True)
+        alen_h.copy_(alen, non_blocking=True)
+
+    n = max(3, min(args.steps, 10))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(n):
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.mean(times)
+    tokens = float((alen_h.numpy() + 1).sum())
+    return {"value": tokens / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n}
+
+
+# --------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# --------------------------------------------------------------------------
+def oracle_step_estimate(w, mode, budget_s, seed_offset=0):
+    """Time the oracle on a bounded sample of one step; return (s per full step, tokens, sample text, threads)."""
+    import oracle
+    oracle.build()
+    a = wl.make_attention_inputs(w, device="cpu", seed=w.seed + seed_offset)
+    acc_in = wl.make_accept_inputs(w, device="cpu", seed=w.seed + seed_offset, mode=mode)
+    q = a["q"].view(torch.int16).numpy().view(np.uint16)
+    kc = a["k_cache"].view(torch.int16).numpy().view(np.uint16)
+    vc = a["v_cache"].view(torch.int16).numpy().view(np.uint16)
+    table, ctx = a["block_table"].numpy(), a["ctx_lens"].numpy()
+    threads = oracle.max_threads()
+    # attention: whole sequences until the budget is spent, scaled by context length
+    t0 = time.perf_counter()
+    done_ctx, done = 0, 0
+    order = list(range(w.batch))
+    while done < len(order) and time.perf_counter() - t0 < budget_s * 0.7:
+        b = order[done]
+        oracle.verify_attention(q, kc, vc, table, ctx, seqs=np.array([b], np.int32))
+        done_ctx += int(ctx[b])
+        done += 1
+    t_attn_sample = time.perf_counter() - t0
+    t_attn = t_attn_sample * float(ctx.sum()) / max(done_ctx, 1)
+    t1 = time.perf_counter()
+    tok, alen, _, _, _ = oracle.accept(acc_in["target_logits"].numpy(), acc_in["draft_tokens"].numpy(),
+                                       acc_in["draft_probs"].numpy(), acc_in["philox_seed"],
+                                       acc_in["mode"].numpy(), acc_in["temperature"].numpy())
+    t_acc = time.perf_counter() - t1
+    t_cmt = 0.0
+    if w.gdn_layers:
+        g = wl.make_gdn_inputs(w.replace(gdn_layers=1), device="cpu", seed=w.seed + seed_offset)
+        live = g["live_state"].numpy()
+        t2 = time.perf_counter()
+        oracle.commit_state(g["snapshots"].numpy(), alen, live)
+        t_cmt = (time.perf_counter() - t2) * w.gdn_layers
+    tokens = float(np.sum(alen + 1))
+    sample = (f"attention over {done}/{w.batch} sequences ({done_ctx} of {int(ctx.sum())} context tokens, "
+              f"scaled by tokens) + acceptance of all {w.batch} rows"
+              + (f" + commit of 1/{w.gdn_layers} layers (scaled)" if w.gdn_layers else ""))
+    return t_attn + t_acc + t_cmt, tokens, sample, threads
+
+
+def run_reference(args, world, rank):
+    w = wl.WORKLOADS[args.config]
+    mode = args.mode or w.mode
+    per_step_budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    times, tokens, sample, threads = [], 0.0, "", 1
+    for i in range(args.warmup + args.steps):
+        s, tokens, sample, threads = oracle_step_estimate(w, mode, per_step_budget)
+        if i >= args.warmup:
+            times.append(s)
+    ms = statistics.mean(times) * 1e3
+    value = tokens / (ms / 1e3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "batch_per_gpu": w.batch, "k_draft": w.k_draft, "mode": mode,
+                   "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return
+    result = run_native(args, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            w = wl.WORKLOADS[args.config]
+            s, tokens, sample, threads = oracle_step_estimate(w, args.mode or w.mode, args.cpu_seconds)
+            result["cpu_baseline"] = {"value": tokens / s, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                      "sample": sample}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

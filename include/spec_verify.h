@@ -65,6 +65,7 @@ typedef struct CUstream_st* spec_stream_t;
 #define SPEC_DEVERR_CTX_LEN 8      /* ctx_len < k+1 or > max_blocks_per_seq * bs */
 #define SPEC_DEVERR_TEMPERATURE 16 /* sampling row with temperature not > 0      */
 #define SPEC_DEVERR_TIMEOUT 32     /* an asynchronous copy did not arrive        */
+#define SPEC_DEVERR_MODE 64        /* mode not 0/1, or sampling row without probs */
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* spec_status_string(int status);
@@ -163,9 +164,11 @@ int spec_verify_attention(const void* q, const void* k_cache, const void* v_cach
  *
  * Rows are read only up to the first rejection (early exit), so the bytes read
  * depend on the outcome.
- * Device errors: a row with a draft token outside [0, V) (SPEC_DEVERR_TOKEN)
- * or a sampling row with temperature not > 0 (SPEC_DEVERR_TEMPERATURE) gets
- * out_tokens all -1 and accept_len -1.
+ * Device errors: a row with a draft token outside [0, V) (SPEC_DEVERR_TOKEN),
+ * a sampling row with temperature not > 0 (SPEC_DEVERR_TEMPERATURE), or a mode
+ * other than 0/1 or a sampling row with draft_probs == NULL (SPEC_DEVERR_MODE)
+ * gets out_tokens all -1 and accept_len -1.
+ * Supported: k_draft <= 31; vocab <= 16 * 49152.
  */
 int spec_accept(const float* target_logits, const int32_t* draft_tokens,
                 const float* draft_probs, uint64_t philox_seed, const int32_t* mode,

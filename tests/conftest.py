@@ -17,3 +17,15 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def sv():
+    """The CUDA library binding, built for sm_103a; skips where no GPU is present."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_paged_gb300 as svmod
+    svmod.build()
+    svmod.load_library()
+    return svmod

@@ -1,0 +1,158 @@
+"""Acceptance on the GPU against the oracle (parity gate) and against the
+distributional facts of speculative sampling.
+
+Greedy tokens and accept lengths must match bit-exactly. Sampled rows must
+match bit-exactly except rows the oracle marks as near ties (|u - p/q| < 1e-5,
+or race keys within 1e-5 relative), which are counted and must stay below
+1e-4 of the decisions.
+"""
+
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+
+from helpers import MAX_EXCUSED_RATE, compare_accept
+from speculative_decoding_verification_paged_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def run_accept(sv, inp, modes, *, probs="given"):
+    B, R, V = inp["target_logits"].shape
+    toks = torch.full((B, R), -7, dtype=torch.int32, device=DEV)
+    alen = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q = inp["draft_probs"] if probs == "given" else None
+    sv.spec_accept(inp["target_logits"], inp["draft_tokens"], q, inp["philox_seed"], modes, inp["temperature"],
+                   toks, alen, dev_err=err)
+    torch.cuda.synchronize()
+    return toks.cpu().numpy(), alen.cpu().numpy(), int(err.item())
+
+
+def oracle_accept(oracle_mod, inp, modes, probs="given"):
+    return oracle_mod.accept(inp["target_logits"].cpu().numpy(), inp["draft_tokens"].cpu().numpy(),
+                             inp["draft_probs"].cpu().numpy() if probs == "given" else None,
+                             inp["philox_seed"], modes.cpu().numpy(), inp["temperature"].cpu().numpy())
+
+
+CASES = [
+    ("tiny", "sample"), ("tiny", "greedy"), ("llama8b_eagle3", "sample"), ("llama8b_eagle3", "greedy"),
+    ("serving128", "mixed"), ("hybrid_gdn", "sample"), ("hybrid_gdn", "greedy"), ("longctx", "sample"),
+]
+
+
+@pytest.mark.parametrize("name,mode", CASES, ids=[f"{a}-{b}" for a, b in CASES])
+def test_accept_parity_named_workloads(sv, oracle_mod, name, mode):
+    w = wl.WORKLOADS[name]
+    inp = wl.make_accept_inputs(w, device=DEV, mode=mode)
+    tok, alen, err = run_accept(sv, inp, inp["mode"])
+    assert err == 0
+    rt, ra, margin, gap, rc = oracle_accept(oracle_mod, inp, inp["mode"])
+    assert rc == 0
+    bad, excused = compare_accept(tok, alen, rt, ra, margin, gap)
+    assert bad == 0, f"{bad} rows differ from the oracle"
+    assert np.all((alen >= 0) & (alen <= w.k_draft))
+    for b in range(w.batch):
+        assert np.all(tok[b, alen[b] + 1:] == -1) and tok[b, alen[b]] >= 0
+
+
+def test_accept_greedy_without_draft_probs(sv, oracle_mod):
+    w = wl.WORKLOADS["tiny"].replace(batch=64)
+    inp = wl.make_accept_inputs(w, device=DEV, mode="greedy")
+    tok, alen, err = run_accept(sv, inp, inp["mode"], probs=None)
+    rt, ra, _, _, _ = oracle_accept(oracle_mod, inp, inp["mode"], probs=None)
+    assert err == 0 and np.array_equal(tok, rt) and np.array_equal(alen, ra)
+
+
+def test_accept_greedy_is_sequential_greedy(sv):
+    """Emitted tokens = argmax of each target row, cut after the first draft miss."""
+    B, k, V = 512, 5, 4000
+    g = torch.Generator(device=DEV).manual_seed(3)
+    L = torch.randn((B, k + 1, V), generator=g, device=DEV) * 3
+    am = L.argmax(-1).to(torch.int32)
+    m_true = torch.randint(0, k + 1, (B,), generator=g, device=DEV)
+    d = am[:, :k].clone()
+    rows = torch.arange(B, device=DEV)
+    miss = m_true < k
+    d[rows[miss], m_true[miss]] = (d[rows[miss], m_true[miss]] + 1) % V
+    inp = {"target_logits": L, "draft_tokens": d.contiguous(), "draft_probs": None, "philox_seed": 0,
+           "temperature": torch.ones(B, device=DEV)}
+    tok, alen, err = run_accept(sv, inp, torch.zeros(B, dtype=torch.int32, device=DEV), probs=None)
+    assert err == 0
+    assert np.array_equal(alen, m_true.cpu().numpy())
+    amc = am.cpu().numpy()
+    for b in range(B):
+        assert np.array_equal(tok[b, : alen[b] + 1], amc[b, : alen[b] + 1])
+
+
+def test_accept_near_tie_rate_over_many_decisions(sv, oracle_mod):
+    B, k, V = 20000, 3, 96
+    w = wl.Workload(name="many", batch=B, ctx_lens=(4,) * B, vocab=V, k_draft=k, logit_sigma=2.0, noise_sigma=1.0,
+                    mode="mixed", temperature=(0.5, 1.2), seed=11)
+    inp = wl.make_accept_inputs(w, device=DEV)
+    tok, alen, err = run_accept(sv, inp, inp["mode"])
+    rt, ra, margin, gap, _ = oracle_accept(oracle_mod, inp, inp["mode"])
+    bad, excused = compare_accept(tok, alen, rt, ra, margin, gap)
+    decisions = int(np.sum(np.where(ra >= 0, np.minimum(ra + 1, k), 0)))
+    assert err == 0 and bad == 0
+    assert excused / decisions < MAX_EXCUSED_RATE, (excused, decisions)
+
+
+def test_accept_vocab_not_multiple_of_four(sv, oracle_mod):
+    w = wl.WORKLOADS["tiny"].replace(vocab=1001, batch=32, mode="mixed")
+    inp = wl.make_accept_inputs(w, device=DEV)
+    tok, alen, err = run_accept(sv, inp, inp["mode"])
+    rt, ra, margin, gap, _ = oracle_accept(oracle_mod, inp, inp["mode"])
+    assert err == 0 and compare_accept(tok, alen, rt, ra, margin, gap)[0] == 0
+
+
+def test_accept_large_vocab_uses_full_cluster(sv, oracle_mod):
+    w = wl.WORKLOADS["hybrid_gdn"].replace(vocab=700001, batch=4, mode="mixed")
+    inp = wl.make_accept_inputs(w, device=DEV)
+    tok, alen, err = run_accept(sv, inp, inp["mode"])
+    rt, ra, margin, gap, _ = oracle_accept(oracle_mod, inp, inp["mode"])
+    assert err == 0 and compare_accept(tok, alen, rt, ra, margin, gap)[0] == 0
+
+
+def _chi2(samples, probs):
+    counts = np.bincount(samples, minlength=len(probs)).astype(np.float64)
+    return stats.chisquare(counts, probs * counts.sum()).pvalue
+
+
+def test_accept_sampling_distribution_chi_square(sv):
+    """Over 10^6 rows the first emitted token follows p_0, the second (given d_0 kept) p_1."""
+    B, k, V, T = 1_000_000, 2, 8, 1.0
+    rng = np.random.default_rng(5)
+    l = rng.normal(0, 1.5, (k + 1, V)).astype(np.float32)
+    q = np.exp(l[:k] + rng.normal(0, 1, (k, V)))
+    q = (q / q.sum(-1, keepdims=True)).astype(np.float32)
+    L = torch.tensor(l, device=DEV).expand(B, k + 1, V).contiguous()
+    Q = torch.tensor(q, device=DEV).expand(B, k, V).contiguous()
+    g = torch.Generator(device=DEV).manual_seed(7)
+    d = torch.multinomial(Q.view(B * k, V), 1, generator=g).view(B, k).to(torch.int32)
+    inp = {"target_logits": L, "draft_tokens": d, "draft_probs": Q, "philox_seed": 2024,
+           "temperature": torch.full((B,), T, device=DEV)}
+    tok, alen, err = run_accept(sv, inp, torch.ones(B, dtype=torch.int32, device=DEV))
+    assert err == 0
+    p = np.exp(l.astype(np.float64) / T)
+    p /= p.sum(-1, keepdims=True)
+    assert _chi2(tok[:, 0], p[0]) > 1e-3
+    sel = alen >= 1
+    assert _chi2(tok[sel, 1], p[1]) > 1e-3
+    assert _chi2(tok[:, 0], q[0].astype(np.float64) / q[0].sum()) < 1e-3  # the test has power
+
+
+def test_accept_invalid_rows_flagged(sv):
+    B, k, V = 4, 3, 100
+    L = torch.zeros((B, k + 1, V), device=DEV)
+    Q = torch.full((B, k, V), 1.0 / V, device=DEV)
+    d = torch.tensor([[1, 2, 3], [1, 200, 3], [1, 2, 3], [4, 5, 6]], dtype=torch.int32, device=DEV)
+    modes = torch.tensor([1, 1, 1, 2], dtype=torch.int32, device=DEV)
+    temp = torch.tensor([1.0, 1.0, 0.0, 1.0], device=DEV)
+    inp = {"target_logits": L, "draft_tokens": d, "draft_probs": Q, "philox_seed": 1, "temperature": temp}
+    tok, alen, err = run_accept(sv, inp, modes)
+    assert alen[0] == k and np.all(alen[1:] == -1) and np.all(tok[1:] == -1)
+    assert err & sv.DEVERR["token"] and err & sv.DEVERR["temperature"] and err & sv.DEVERR["mode"]

@@ -1,0 +1,119 @@
+"""Verify attention on the GPU against the double-precision oracle (parity gate).
+
+Small cases are checked in full; the named workloads at their full sizes are
+checked on sampled sequences (the oracle recomputes those sequences one by one
+from the same device inputs). Tolerances: max-abs <= 1e-2 and relative L2 <=
+2e-3 per case.
+"""
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import ATTN_MAX_ABS, ATTN_REL_L2, attention_errors, oracle_attention_for
+from speculative_decoding_verification_paged_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+# (name, B, ctx_lens, bs, Hq, Hkv, D, k): every (head_dim, m-tile count) instantiation,
+# ragged contexts spanning several 64-key tiles and splits, block sizes 16..128.
+SMALL = [
+    ("d64_mt1_bs16", 5, (4, 63, 64, 65, 700), 16, 8, 2, 64, 3),
+    ("d64_mt2_bs32", 3, (9, 333, 1030), 32, 8, 2, 64, 7),
+    ("d64_mt4_bs64", 2, (8, 1500), 64, 16, 2, 64, 7),
+    ("d128_mt1_bs64", 4, (100, 2048, 4, 129), 64, 32, 8, 128, 3),
+    ("d128_mt2_bs16", 3, (640, 77, 1999), 16, 12, 2, 128, 3),
+    ("d128_mt4_bs128", 3, (129, 2000, 9), 128, 16, 2, 128, 7),
+    ("d256_mt1_bs64", 3, (1000, 5, 300), 64, 4, 2, 256, 3),
+    ("d256_mt2_bs64", 3, (300, 1000, 77), 64, 12, 2, 256, 3),
+    ("d256_mt4_bs32", 2, (257, 900), 32, 16, 2, 256, 7),
+]
+
+
+def run_attention(sv, a, w, **kw):
+    out = torch.full((w.batch, w.rows, w.num_q_heads, w.head_dim), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sv.spec_verify_attention(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["ctx_lens"], w.k_draft, out,
+                             dev_err=err, **kw)
+    torch.cuda.synchronize()
+    return out, int(err.item())
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_attention_small_cases_full_parity(sv, oracle_mod, case):
+    name, B, ctx, bs, Hq, Hkv, D, k = case
+    w = wl.Workload(name=name, batch=B, ctx_lens=ctx, block_size=bs, num_q_heads=Hq, num_kv_heads=Hkv,
+                    head_dim=D, k_draft=k, seed=zlib.crc32(name.encode()) % 1000)
+    a = wl.make_attention_inputs(w, device=DEV)
+    out, err = run_attention(sv, a, w)
+    assert err == 0
+    ref = oracle_attention_for(oracle_mod, a)
+    mx, rel = attention_errors(out.cpu().numpy(), ref)
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+
+
+def test_attention_tiny_workload(sv, oracle_mod):
+    w = wl.WORKLOADS["tiny"]
+    a = wl.make_attention_inputs(w, device=DEV)
+    out, err = run_attention(sv, a, w)
+    assert err == 0
+    mx, rel = attention_errors(out.cpu().numpy(), oracle_attention_for(oracle_mod, a))
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+
+
+@pytest.mark.parametrize("name", ["llama8b_eagle3", "serving128", "hybrid_gdn", "longctx"])
+def test_attention_full_size_sampled_sequences(sv, oracle_mod, name):
+    w = wl.WORKLOADS[name]
+    a = wl.make_attention_inputs(w, device=DEV)
+    out, err = run_attention(sv, a, w)
+    assert err == 0
+    assert torch.isfinite(out).all()
+    ctx = a["ctx_lens"].cpu().numpy()
+    picks = sorted({0, w.batch - 1, int(np.argmax(ctx)), int(np.argmin(ctx))})
+    if name == "longctx":
+        picks = sorted({int(np.argmax(ctx)), int(np.argmin(ctx))})
+    ref = oracle_attention_for(oracle_mod, a, seqs=np.array(picks, np.int32))
+    mx, rel = attention_errors(out[picks].cpu().numpy(), ref)
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+
+
+def test_attention_is_deterministic_and_reuses_workspace(sv):
+    w = wl.WORKLOADS["llama8b_eagle3"].replace(batch=8, ctx_lens=(2048,) * 8)
+    a = wl.make_attention_inputs(w, device=DEV)
+    ws = torch.empty(sv.spec_verify_attention_workspace(a["q"], a["k_cache"], a["block_table"], w.k_draft),
+                     dtype=torch.uint8, device=DEV)
+    o1, _ = run_attention(sv, a, w, workspace=ws)
+    o2, _ = run_attention(sv, a, w, workspace=ws)
+    assert torch.equal(o1, o2)
+
+
+def test_attention_bad_block_and_bad_ctx_give_zero_rows(sv, oracle_mod):
+    w = wl.Workload(name="bad", batch=4, ctx_lens=(300, 300, 300, 300), block_size=16, num_q_heads=8,
+                    num_kv_heads=2, head_dim=128, k_draft=3, seed=5)
+    a = wl.make_attention_inputs(w, device=DEV)
+    a["block_table"][1, 3] = a["num_blocks"] + 5          # out-of-range block id
+    a["ctx_lens"][2] = 2                                   # ctx < k+1
+    out, err = run_attention(sv, a, w)
+    assert err & sv.DEVERR["block_id"] and err & sv.DEVERR["ctx_len"]
+    assert torch.all(out[1] == 0) and torch.all(out[2] == 0)
+    ref = oracle_attention_for(oracle_mod, a, seqs=np.array([0, 3], np.int32))
+    mx, rel = attention_errors(out[[0, 3]].cpu().numpy(), ref)
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2
+
+
+def test_attention_minimal_context_row0_is_v0(sv):
+    """ctx = k+1: row 0 sees one key, so its output is that key's value."""
+    w = wl.Workload(name="min", batch=3, ctx_lens=(4, 4, 4), block_size=16, num_q_heads=8, num_kv_heads=2,
+                    head_dim=64, k_draft=3, seed=9)
+    a = wl.make_attention_inputs(w, device=DEV)
+    out, err = run_attention(sv, a, w)
+    assert err == 0
+    for b in range(3):
+        phys = int(a["block_table"][b, 0])
+        v0 = a["v_cache"][phys, 0].float()  # [Hkv, D]
+        for h in range(8):
+            assert torch.allclose(out[b, 0, h], v0[h // 4], atol=1e-6, rtol=0)

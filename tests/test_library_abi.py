@@ -1,0 +1,94 @@
+"""The C-ABI library builds, loads and exports every entry point of spec_verify.h (CPU only).
+
+Also checks the host-side argument validation, which returns before any CUDA
+call and so needs no GPU.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import speculative_decoding_verification_paged_gb300 as sv
+    sv.build()
+    return sv.load_library()
+
+
+def declared_functions():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(spec_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("spec_verify_attention", "spec_accept", "spec_commit_state"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    import speculative_decoding_verification_paged_gb300 as sv
+    assert sv.status_string(0) == "ok"
+    assert sv.status_string(-4) == "workspace missing or too small"
+
+
+def _desc(**kw):
+    import speculative_decoding_verification_paged_gb300 as sv
+    base = dict(batch=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=64, max_blocks_per_seq=4,
+                num_blocks=8)
+    base.update(kw)
+    return sv._AttnDesc(**base)
+
+
+def test_attention_host_validation(lib):
+    fake = ctypes.c_void_p(256)
+    d = _desc()
+    ws = lib.spec_verify_attention_workspace(ctypes.byref(d), 3)
+    assert ws > 0
+    # workspace grows with batch and head count
+    assert lib.spec_verify_attention_workspace(ctypes.byref(_desc(batch=64)), 3) > ws
+    # invalid descriptor
+    assert lib.spec_verify_attention_workspace(None, 3) == 0
+    assert lib.spec_verify_attention_workspace(ctypes.byref(_desc(num_q_heads=7)), 3) == 0
+    call = lambda dd, kd=3, wsb=ws, q=fake, w=fake: lib.spec_verify_attention(
+        q, fake, fake, fake, fake, kd, fake, ctypes.byref(dd), w, wsb, None, None)
+    assert call(_desc(), q=None) == -1
+    assert call(_desc(num_q_heads=7)) == -1
+    assert call(_desc(), kd=0) == -1
+    assert call(_desc(head_dim=96)) == -2
+    assert call(_desc(block_size=48)) == -2
+    assert call(_desc(num_q_heads=36, num_kv_heads=2)) == -2  # (k+1)*G = 72 > 64 rows
+    assert call(_desc(), wsb=ws - 1) == -4
+    assert call(_desc(), w=None) == -4
+    assert call(_desc(batch=0)) == 0
+
+
+def test_accept_and_commit_host_validation(lib):
+    fake = ctypes.c_void_p(256)
+    acc = lambda B=2, k=3, V=100, logits=fake: lib.spec_accept(logits, fake, fake, 1, fake, fake, fake, fake,
+                                                               B, k, V, None, None)
+    assert acc(k=0) == -1
+    assert acc(V=0) == -1
+    assert acc(logits=None) == -1
+    assert acc(k=32) == -2
+    assert acc(B=0) == 0
+    com = lambda L=2, B=2, S=4, E=16, snaps=fake: lib.spec_commit_state(snaps, fake, fake, L, B, S, E, None, None)
+    assert com(S=0) == -1
+    assert com(snaps=None) == -1
+    assert com(L=0) == 0
+    assert com(L=1000, B=1000) == -2
