@@ -205,54 +205,90 @@ def run_native(args, world, rank, local):
     g = wl.make_gdn_inputs(w, device=dev, seed=w.seed + 1000 * rank) if w.gdn_layers else None
     B, R = w.batch, w.rows
     out = torch.empty((B, R, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
-    ws = torch.empty(sv.spec_verify_attention_workspace(a["q"], a["k_cache"], a["block_table"], w.k_draft),
-                     dtype=torch.uint8, device=dev)
+    ws = sv.new_attention_workspace(
+        sv.spec_verify_attention_workspace(a["q"], a["k_cache"], a["block_table"], w.k_draft), dev)
     toks = torch.empty((B, R), dtype=torch.int32, device=dev)
     alen = torch.empty((B,), dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_read = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def attention():
         sv.spec_verify_attention(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["ctx_lens"], w.k_draft, out,
                                  workspace=ws, dev_err=err)
-        ev[1].record(stream)
+
+    def accept():
         sv.spec_accept(acc_in["target_logits"], acc_in["draft_tokens"], acc_in["draft_probs"],
                        acc_in["philox_seed"], acc_in["mode"], acc_in["temperature"], toks, alen, dev_err=err)
-        ev[2].record(stream)
+
+    def commit():
         if g is not None:
             sv.spec_commit_state(g["snapshots"], alen, g["live_state"], dev_err=err)
 
-    launches_per_step = 3 + 1 + (1 if g is not None else 0)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    def step():
+        attention()
+        accept()
+        commit()
+
+    launches_per_step = 1 + 1 + (1 if g is not None else 0)
     for _ in range(args.warmup):
-        flush.zero_()
-        ev[0].record(stream)
         step()
-        ev[3].record(stream)
     torch.cuda.synchronize()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
 
-    per_step, t_attn, t_acc, t_cmt = [], [], [], []
+    # The step (and each call alone) is captured once into a CUDA graph and
+    # replayed, so the device timeline carries no host launch gaps.
+    graphs = {}
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for name, fn in (("step", step), ("attention", attention), ("accept", accept), ("commit", commit)):
+            if name == "commit" and g is None:
+                continue
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                fn()
+            graphs[name] = graph
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def l2_flush():
+        # write a buffer larger than L2, then read another one so the dirty lines
+        # are written back here and not inside the next timed region
+        flush.zero_()
+        flush_read.sum()
+
+    def timed(graph, n):
+        times = []
+        for _ in range(n):
+            l2_flush()  # between timed replays, outside the events
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return times
+
+    for _ in range(2):
+        graphs["step"].replay()
     clocks = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)  # let the sampler start
-    for _ in range(args.steps):
-        flush.zero_()  # L2 flush between timed steps (outside the events)
-        ev[0].record(stream)
-        step()
-        ev[3].record(stream)
-        torch.cuda.synchronize()
-        per_step.append(ev[0].elapsed_time(ev[3]))
-        t_attn.append(ev[0].elapsed_time(ev[1]))
-        t_acc.append(ev[1].elapsed_time(ev[2]))
-        t_cmt.append(ev[2].elapsed_time(ev[3]))
+    per_step = timed(graphs["step"], args.steps)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
+    t_attn = timed(graphs["attention"], args.steps)
+    t_acc = timed(graphs["accept"], args.steps)
+    t_cmt = timed(graphs["commit"], args.steps) if "commit" in graphs else [0.0]
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())}")
 
     ms = statistics.mean(per_step)
     alen_h = alen.cpu().numpy()
@@ -292,7 +328,8 @@ def run_native(args, world, rank, local):
                    "ctx": list(w.ctx_range) if w.ctx_range else sorted(set(w.ctx_lens)),
                    "block_size": w.block_size, "heads": [w.num_q_heads, w.num_kv_heads], "head_dim": w.head_dim,
                    "vocab": w.vocab, "gdn_layers": w.gdn_layers, "parallelism": f"replicas x{world}",
-                   "l2": "flushed between timed steps (512 MiB write)"},
+                   "l2": "flushed between timed steps (512 MiB write, then 512 MiB read)",
+                   "timing": "CUDA-graph replay of the step, CUDA events on the launching stream"},
         "verified_tokens_per_step": tokens_all, "mean_accept_len": float(np.mean(alen_h)),
         "kernels": kernels, "roofline": roofline, "clocks": clk, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
@@ -414,11 +451,14 @@ def run_reference(args, world, rank):
 
 def main():
     args = parse()
-    world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
+        # the oracle runs on rank 0's host cores only; other ranks exit without work
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
         if rank == 0:
             print(json.dumps(run_reference(args, world, rank)), flush=True)
         return
+    world, rank, local = dist_setup(args.gpus)
     result = run_native(args, world, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:

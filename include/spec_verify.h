@@ -109,12 +109,15 @@ size_t spec_verify_attention_workspace(const spec_attn_desc* d, int32_t k_draft)
  *              included; must lie in [k_draft+1, max_blocks_per_seq * bs].
  *  out         [B, k_draft+1, Hq, D] fp32
  *  workspace   >= spec_verify_attention_workspace(d, k_draft) bytes, 256-byte
- *              aligned, contents need not be initialised and are scratch after
- *              the call. Two calls in flight at once need two workspaces.
+ *              aligned, ZERO-FILLED before its first use (it holds per-unit
+ *              arrival counters that every call returns to zero; the rest is
+ *              scratch). Reuse it for later calls on the same stream; two calls
+ *              in flight at once need two workspaces.
  *
- * Long contexts are split across CTAs (split-KV) and the partial results are
- * merged by their log-sum-exp; the split plan is chosen on the device from
- * ctx_lens, so no host synchronisation is needed.
+ * The key tiles of all (sequence, kv head) units are split evenly over the
+ * CTAs (split-KV); a unit held by several CTAs is merged by its log-sum-exp
+ * inside the same launch. The split is chosen on the device from ctx_lens, so
+ * no host synchronisation is needed.
  * Device errors: a sequence with an out-of-range ctx_len (SPEC_DEVERR_CTX_LEN)
  * or block id (SPEC_DEVERR_BLOCK_ID) gets out rows of zeros.
  * Supported: D in {64,128,256}; bs in {16,32,64,128}; (k_draft+1)*G <= 64.

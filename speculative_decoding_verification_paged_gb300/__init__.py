@@ -25,7 +25,7 @@ from . import buildlib as _build_mod
 
 __all__ = [
     "SpecError", "build", "library_path", "load_library", "spec_verify_attention",
-    "spec_verify_attention_workspace", "spec_accept", "spec_commit_state", "status_string",
+    "spec_verify_attention_workspace", "new_attention_workspace", "spec_accept", "spec_commit_state", "status_string",
     "DEVERR", "MODE_GREEDY", "MODE_SAMPLE",
 ]
 
@@ -139,6 +139,11 @@ def spec_verify_attention_workspace(q: torch.Tensor, k_cache: torch.Tensor, bloc
     return int(load_library().spec_verify_attention_workspace(ctypes.byref(d), int(k_draft)))
 
 
+def new_attention_workspace(nbytes: int, device) -> torch.Tensor:
+    """A workspace for spec_verify_attention: zero-filled once, reusable by later calls on one stream."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
 def spec_verify_attention(q, k_cache, v_cache, block_table, ctx_lens, k_draft: int, out,
                           workspace: Optional[torch.Tensor] = None, dev_err: Optional[torch.Tensor] = None,
                           stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
@@ -158,7 +163,7 @@ def spec_verify_attention(q, k_cache, v_cache, block_table, ctx_lens, k_draft: i
     d = _attn_desc(q, k_cache, block_table)
     need = int(lib.spec_verify_attention_workspace(ctypes.byref(d), int(k_draft)))
     if workspace is None:
-        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        workspace = new_attention_workspace(need, q.device)
     _need(workspace, "workspace", torch.uint8, 1)
     rc = lib.spec_verify_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens),
                                    int(k_draft), _ptr(out), ctypes.byref(d), _ptr(workspace),

@@ -32,7 +32,7 @@ namespace acc {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 16;
-constexpr int kSliceTarget = 16384;  // logits per CTA (64 KB of shared memory)
+constexpr int kSliceTarget = 8192;   // logits per CTA (32 KB of shared memory)
 constexpr int kMaxSlice = 48 * 1024;
 constexpr int kMaxK = 31;
 
@@ -65,8 +65,8 @@ struct Shared {
   float wf[kWarps];
   float wg[kWarps];
   int32_t wi[kWarps];
-  int32_t bcast_i[4];
-  float bcast_f[4];
+  float l_draft[kMaxK];  // target logit of each draft token, read once at start
+  float q_draft[kMaxK];  // draft probability of each draft token
   uint64_t bar;
 };
 
@@ -115,6 +115,24 @@ __device__ __forceinline__ float block_sum(Shared& sh, float v) {
   return v;
 }
 
+// Slice values x in [0, n) are read as float4 groups when the slice is 16-byte
+// aligned (always when bulk copies are used); `fn(x, v)` sees every element once.
+template <typename F>
+__device__ __forceinline__ void for_slice(const float* buf, int n, bool vec, F fn) {
+  if (vec) {
+    const float4* b4 = reinterpret_cast<const float4*>(buf);
+    for (int g = threadIdx.x; g * 4 < n; g += kThreads) {
+      const float4 v = b4[g];
+      fn(4 * g, v.x);
+      fn(4 * g + 1, v.y);
+      fn(4 * g + 2, v.z);
+      fn(4 * g + 3, v.w);
+    }
+  } else {
+    for (int x = threadIdx.x; x < n; x += kThreads) fn(x, buf[x]);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
   extern __shared__ __align__(128) float buf[];
   __shared__ Shared sh;
@@ -152,22 +170,34 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
   const float c2 = (1.0f / T) * 1.4426950408889634f;  // logit -> log2 units of p
   const uint32_t sh_pos = smem_u32(&sh.pos[0]);
   const uint32_t sh_race = smem_u32(&sh.race[0]);
+  bool bulk = p.bulk != 0;
+  const bool vec = bulk;  // 16-byte aligned slices
 
+  auto row_ptr = [&](int j) { return p.logits + ((int64_t)b * R + j) * V + x0; };
   if (tid == 0) {
     mbar_init(&sh.bar, 1);
     fence_mbar_init();
   }
+  // the values every decision needs are read once, up front, off the critical path
+  if (!greedy && tid < k) {
+    sh.l_draft[tid] = __ldg(p.logits + ((int64_t)b * R + tid) * V + d[tid]);
+    sh.q_draft[tid] = __ldg(p.probs + ((int64_t)b * k + tid) * V + d[tid]);
+  }
   __syncthreads();
   uint32_t phase = 0;
-  bool bulk = p.bulk != 0;
   bool pending = false;  // a bulk copy was issued and not yet observed complete
 
-  auto row_ptr = [&](int j) { return p.logits + ((int64_t)b * R + j) * V + x0; };
   auto issue_row = [&](int j) {
     if (bulk) {
       if (tid == 0) {
         mbar_arrive_expect_tx(&sh.bar, (uint32_t)n * 4u);
         bulk_g2s(smem_u32(buf), row_ptr(j), (uint32_t)n * 4u, &sh.bar);
+        // the next position is likely needed: start pulling it into L2 now
+        // (same 16-byte alignment rule as the bulk copy)
+        if (p.prefetch && j < k) {
+          bulk_prefetch_l2(row_ptr(j + 1), (uint32_t)n * 4u);
+          if (!greedy) bulk_prefetch_l2(p.probs + ((int64_t)b * k + j) * V + x0, (uint32_t)n * 4u);
+        }
       }
       pending = true;
     } else {
@@ -187,36 +217,66 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
     }
     __syncthreads();
   };
+  // (best value, lowest index) over the ranks' published partials. Lane r of every
+  // warp reads rank r's partial (the DSMEM loads overlap) and the warp reduces
+  // them with shuffles in a fixed tree, so every CTA gets a bit-identical result.
+  const int lane = tid & 31;
+  auto cluster_best = [&](uint32_t local, float& bv, int& bi, float* sum) {
+    float v = -INFINITY, acc = 0.f;
+    int i = INT32_MAX;
+    if (lane < csize) {
+      const uint32_t a = map_to_rank(local, (uint32_t)lane);
+      v = ld_cluster_f32(a);
+      i = ld_cluster_s32(a + 8);
+      acc = ld_cluster_f32(a + 4);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+      acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+    }
+    bv = v;
+    bi = i;
+    if (sum) *sum = acc;
+  };
+  // Softmax statistics of the whole row from the ranks' (slice max, slice sum) pairs.
+  auto cluster_stats = [&](uint32_t local, float& M, float& Z) {
+    float mr = -INFINITY, zr = 0.f;
+    if (lane < csize) {
+      const uint32_t a = map_to_rank(local, (uint32_t)lane);
+      mr = ld_cluster_f32(a);
+      zr = ld_cluster_f32(a + 4);
+    }
+    float mm = mr;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+    float zz = lane < csize ? zr * fast_exp2((mr - mm) * c2) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+    M = mm;
+    Z = zz;
+  };
 
   int m = k;
   int token = -1;
   issue_row(0);
   for (int j = 0; j <= k; ++j) {
     wait_row();
-    // L2 prefetch needs the same 16-byte alignment as the bulk copies
-    if (p.prefetch && bulk && tid == 0 && j < k) {
-      bulk_prefetch_l2(row_ptr(j + 1), (uint32_t)n * 4u);
-      if (!greedy) bulk_prefetch_l2(p.probs + ((int64_t)b * k + j) * V + x0, (uint32_t)n * 4u);
-    }
     if (greedy) {
       // ---- argmax of the slice, then of the cluster (ranks are in vocab order)
       float v = -INFINITY;
       int idx = INT32_MAX;
-      for (int x = tid; x < n; x += kThreads) {
-        const float l = buf[x];
+      for_slice(buf, n, vec, [&](int x, float l) {
         if (l > v) { v = l; idx = x0 + x; }
-      }
+      });
       block_argmax(sh, v, idx);
       if (tid == 0) sh.pos[j] = Part{v, 0.f, idx, 0};
       cluster_sync_all();
-      float bv = -INFINITY;
-      int bi = INT32_MAX;
-      for (int r = 0; r < csize; ++r) {
-        const uint32_t a = map_to_rank(sh_pos + j * sizeof(Part), (uint32_t)r);
-        const float ov = ld_cluster_f32(a);
-        const int oi = ld_cluster_s32(a + 8);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
+      float bv;
+      int bi;
+      cluster_best(sh_pos + j * sizeof(Part), bv, bi, nullptr);
       if (j < k && d[j] == bi) {
         issue_row(j + 1);
         continue;
@@ -237,8 +297,8 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
         for (int e = 0; e < 4; ++e) {
           const int x = g4 * 4 + e;
           if (x < n) {
-            const float E = -logf(word_to_uniform(w.v[e]));
-            const float key = buf[x] * c2 - log2f(E);
+            const float E = -__logf(word_to_uniform(w.v[e]));
+            const float key = buf[x] * c2 - __log2f(E);
             if (key > best) { best = key; bidx = x0 + x; }
           }
         }
@@ -246,37 +306,26 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       block_argmax(sh, best, bidx);
       if (tid == 0) sh.race[0] = Part{best, 0.f, bidx, 0};
       cluster_sync_all();
-      float bv = -INFINITY;
-      int bi = INT32_MAX;
-      for (int r = 0; r < csize; ++r) {
-        const uint32_t a = map_to_rank(sh_race, (uint32_t)r);
-        const float ov = ld_cluster_f32(a);
-        const int oi = ld_cluster_s32(a + 8);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
+      float bv;
+      int bi;
+      cluster_best(sh_race, bv, bi, nullptr);
       m = k;
       token = bi;
       break;
     }
     // ---- sampling statistics of p_j = softmax(l / T): slice max, then sum of exp
     float mx = -INFINITY;
-    for (int x = tid; x < n; x += kThreads) mx = fmaxf(mx, buf[x]);
+    for_slice(buf, n, vec, [&](int, float l) { mx = fmaxf(mx, l); });
     mx = block_max(sh, mx);
     float z = 0.f;
-    for (int x = tid; x < n; x += kThreads) z += exp2f((buf[x] - mx) * c2);
+    for_slice(buf, n, vec, [&](int, float l) { z += fast_exp2((l - mx) * c2); });
     z = block_sum(sh, z);
     if (tid == 0) sh.pos[j] = Part{mx, z, 0, 0};
     cluster_sync_all();
-    float M = -INFINITY;
-    for (int r = 0; r < csize; ++r) M = fmaxf(M, ld_cluster_f32(map_to_rank(sh_pos + j * sizeof(Part), (uint32_t)r)));
-    float Z = 0.f;
-    for (int r = 0; r < csize; ++r) {
-      const uint32_t a = map_to_rank(sh_pos + j * sizeof(Part), (uint32_t)r);
-      Z += ld_cluster_f32(a + 4) * exp2f((ld_cluster_f32(a) - M) * c2);
-    }
-    const int dj = d[j];
-    const float pd = exp2f((p.logits[((int64_t)b * R + j) * V + dj] - M) * c2) / Z;
-    const float qd = p.probs[((int64_t)b * k + j) * V + dj];
+    float M, Z;
+    cluster_stats(sh_pos + j * sizeof(Part), M, Z);
+    const float pd = fast_exp2((sh.l_draft[j] - M) * c2) / Z;
+    const float qd = sh.q_draft[j];
     const Philox4 wu = philox4x32_10(0u, (uint32_t)j, (uint32_t)b, 0u, p.seed_lo, p.seed_hi);
     const float u = word_to_uniform(wu.v[0]);
     if (u * qd < pd) {
@@ -293,7 +342,7 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       for (int g4 = tid; g4 * 4 < n; g4 += kThreads) {
         const int gx = x0 + g4 * 4;
         float qv[4];
-        if (p.bulk && g4 * 4 + 3 < n) {
+        if (vec && g4 * 4 + 3 < n) {
           const float4 q4 = __ldg(reinterpret_cast<const float4*>(qrow + g4 * 4));
           qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
         } else {
@@ -305,12 +354,14 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
         for (int e = 0; e < 4; ++e) {
           const int x = g4 * 4 + e;
           if (x < n) {
-            const float px = exp2f((buf[x] - M) * c2) * invZ;
+            const float px = fast_exp2((buf[x] - M) * c2) * invZ;
             const float wt = pass == 0 ? fmaxf(px - qv[e], 0.f) : px;
             wsum += wt;
-            const float E = -logf(word_to_uniform(w.v[e]));
-            const float key = wt / E;
-            if (key > best) { best = key; bidx = x0 + x; }
+            if (wt > 0.f) {
+              const float E = -__logf(word_to_uniform(w.v[e]));
+              const float key = __fdividef(wt, E);
+              if (key > best) { best = key; bidx = x0 + x; }
+            }
           }
         }
       }
@@ -318,15 +369,9 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       wsum = block_sum(sh, wsum);
       if (tid == 0) sh.race[pass] = Part{best, wsum, bidx, 0};
       cluster_sync_all();
-      float bv = -1.f, total = 0.f;
-      int bi = INT32_MAX;
-      for (int r = 0; r < csize; ++r) {
-        const uint32_t a = map_to_rank(sh_race + pass * sizeof(Part), (uint32_t)r);
-        const float ov = ld_cluster_f32(a);
-        total += ld_cluster_f32(a + 4);
-        const int oi = ld_cluster_s32(a + 8);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
+      float bv, total;
+      int bi;
+      cluster_best(sh_race + pass * sizeof(Part), bv, bi, &total);
       token = bi;
       if (total > 0.f) break;  // identical in every CTA: the same partials, the same order
     }
@@ -400,15 +445,29 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
   auto kern = acc::accept_kernel;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  // Function attributes and the cluster-size probe depend only on (device, slice):
+  // remember the last answer so steady-state calls make no extra runtime queries.
+  static int cached_dev = -1, cached_vocab = -1, cached_csize = 0, cached_slice = 0;
+  static size_t cached_smem = 0;
+  const bool cached = dev == cached_dev && vocab == cached_vocab;
+  if (cached) {
+    p.csize = cached_csize;
+    p.slice = cached_slice;
+  }
   // Clusters larger than 8 CTAs are not guaranteed to fit a GPC; if the device
   // cannot hold one, use 8 CTAs with larger slices.
   for (int attempt = 0; attempt < 2; ++attempt) {
     const size_t smem = (size_t)p.slice * sizeof(float);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return SPEC_ERR_LAUNCH;
-    if (p.csize > 8 &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-      return SPEC_ERR_LAUNCH;
+    if (!cached || smem > cached_smem) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return SPEC_ERR_LAUNCH;
+      if (p.csize > 8 &&
+          cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return SPEC_ERR_LAUNCH;
+      cached_smem = smem > cached_smem ? smem : cached_smem;
+    }
     cfg.gridDim = dim3((unsigned)(batch * p.csize), 1, 1);
     cfg.blockDim = dim3(acc::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
@@ -419,13 +478,19 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.csize <= 8) break;
+    if (cached || p.csize <= 8) break;
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0) break;
     (void)cudaGetLastError();
     p.csize = 8;
     p.slice = (((vocab + 7) / 8) + 3) & ~3;
     if (p.slice > acc::kMaxSlice) return SPEC_ERR_UNSUPPORTED;
+  }
+  if (!cached) {
+    cached_dev = dev;
+    cached_vocab = vocab;
+    cached_csize = p.csize;
+    cached_slice = p.slice;
   }
   if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return SPEC_ERR_LAUNCH;
   return SPEC_OK;

@@ -12,50 +12,49 @@
 //  * All (k+1)*G query rows that share one kv head are packed into the M
 //    dimension of the tensor-core tile, so each K/V byte is read from HBM once
 //    per kv head. M = 16, 32 or 64 rows (1, 2 or 4 m16 tiles).
-//  * Work item = (sequence, key chunk, kv head). A tiny plan kernel sizes the
-//    key chunk from the actual context lengths (device side, no host sync) so
-//    the items cover the GPU several times over; persistent CTAs pull items
-//    from an atomic counter. Partial results of a split sequence are merged
-//    by their log-sum-exp in a third kernel.
-//  * Paged K/V tiles are staged into swizzled shared memory with 16-byte
-//    cp.async copies (3-stage ring), each key looked up through the block
-//    table; the block id is range-checked before any byte is read.
-//  * QK^T and PV run on mma.sync m16n8k16 (bf16 in, fp32 accumulate). P is
-//    split into a bf16 high part and a bf16 remainder and both are multiplied
-//    with V, so PV keeps ~16 mantissa bits of P; softmax statistics and the
-//    output stay fp32.
+//  * One launch, stream-K split: the key tiles of all (sequence, kv head)
+//    units are laid end to end and every persistent CTA takes an equal,
+//    contiguous range of that tile stream, so the load is balanced for any mix
+//    of context lengths. A unit that spans several CTAs is merged by its
+//    log-sum-exp: every CTA that holds a piece writes a normalised partial,
+//    and the last one to finish (an atomic counter per unit, which it resets)
+//    combines them. The range split is computed inside the kernel from
+//    ctx_lens, so no host synchronisation and no extra launch is needed.
+//  * A producer warp stages paged K/V tiles (and each unit's query rows) into
+//    128-byte-swizzled shared memory with tiled TMA copies (one 3-D box per
+//    KV block piece and 64-wide slice of the head dimension), completing on
+//    per-stage mbarriers; the ring runs across unit boundaries and the four
+//    consumer warps release each stage through a second mbarrier. Block ids
+//    are range-checked before they are used; a bad or unallocated block is
+//    read as zeros through an out-of-range box coordinate.
+//  * QK^T and PV run on mma.sync m16n8k16 (bf16 in, fp32 accumulate), several
+//    independent accumulator chains per warp. P is split into a bf16 high part
+//    and a bf16 remainder and both are multiplied with V, so PV keeps ~16
+//    mantissa bits of P; softmax statistics and the output stay fp32.
 #include <math.h>
+
+#include <cuda.h>
 
 #include "common.cuh"
 
 namespace specv {
 namespace attn {
 
-constexpr int kThreads = 128;
-constexpr int kWarps = kThreads / 32;
-constexpr int kStages = 3;
-constexpr int kTargetItems = 1216;
+constexpr int kConsumers = 128;               // 4 consumer warps
+constexpr int kWarps = kConsumers / 32;
+constexpr int kThreads = kConsumers + 32;     // + 1 producer warp
+constexpr int kMaxGrid = 1024;                // persistent CTAs; each owns two partial slots
 constexpr int kMaxBatch = 4096;
-constexpr int kHeaderBytes = 256;
-
-struct WsHeader {
-  int32_t chunk_tiles;
-  int32_t total_splits;
-  int32_t next_item;
-  int32_t pad;
-};
+constexpr int kSmemBudget = 200 * 1024;       // ring + query buffers
+constexpr int kBarConsumers = 1;              // named barrier id of the consumer warps
 
 struct Params {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k_cache;
-  const __nv_bfloat16* v_cache;
   const int32_t* block_table;
   const int32_t* ctx_lens;
   float* out;
-  WsHeader* hdr;
-  const int32_t* prefix;
-  float* lse;    // [max_items][n_rows], log2 units
-  float* opart;  // [max_items][n_rows][D]
+  int32_t* counters;  // [B * Hkv] arrival counters, zero between calls
+  float* lse;         // [2 * kMaxGrid][n_rows], log2 units
+  float* opart;       // [2 * kMaxGrid][n_rows][D]
   int32_t* dev_err;
   int64_t num_blocks;
   int batch, rows_per_seq, num_q_heads, num_kv_heads, gqa, n_rows;
@@ -68,439 +67,596 @@ __host__ __device__ constexpr int tile_keys(int D, int MT) { return (D >= 256 &&
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// ---------------------------------------------------------------------------
-// Plan: chunk size and per-sequence split prefix, from the actual ctx_lens.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ ctx_lens, int batch,
-                                                    int rows_per_seq, int64_t max_ctx, int tk,
-                                                    int num_kv_heads, WsHeader* hdr, int32_t* prefix,
-                                                    int32_t* dev_err) {
-  __shared__ int64_t warp_tiles[32];
-  __shared__ int32_t warp_splits[32];
-  __shared__ int32_t s_chunk;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (batch + blockDim.x - 1) / blockDim.x;
-  const int b0 = tid * per;
-  int64_t my_tiles = 0;
-  for (int i = 0; i < per; ++i) {
-    const int b = b0 + i;
-    if (b < batch) {
-      const int c = ctx_lens[b];
-      const bool ok = c >= rows_per_seq && (int64_t)c <= max_ctx;
-      if (!ok) raise_error(dev_err, SPEC_DEVERR_CTX_LEN);
-      my_tiles += ok ? (c + tk - 1) / tk : 0;
-    }
-  }
-  int64_t t = my_tiles;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-  if (lane == 0) warp_tiles[warp] = t;
-  __syncthreads();
-  if (tid == 0) {
-    int64_t total = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += warp_tiles[w];
-    const int64_t units = total * num_kv_heads;
-    int64_t chunk = (units + kTargetItems - 1) / kTargetItems;
-    s_chunk = (int)(chunk < 1 ? 1 : chunk);
-  }
-  __syncthreads();
-  const int chunk = s_chunk;
-  int32_t my_splits = 0;
-  for (int i = 0; i < per; ++i) {
-    const int b = b0 + i;
-    if (b < batch) {
-      const int c = ctx_lens[b];
-      const bool ok = c >= rows_per_seq && (int64_t)c <= max_ctx;
-      const int nt = ok ? (c + tk - 1) / tk : 0;
-      my_splits += (nt + chunk - 1) / chunk;
-    }
-  }
-  // exclusive scan of my_splits across the block
-  int32_t incl = my_splits;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) warp_splits[warp] = incl;
-  __syncthreads();
-  if (tid == 0) {
-    int32_t run = 0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-      const int32_t v = warp_splits[w];
-      warp_splits[w] = run;
-      run += v;
-    }
-    hdr->chunk_tiles = chunk;
-    hdr->total_splits = run;
-    hdr->next_item = 0;
-    prefix[batch] = run;
-  }
-  __syncthreads();
-  int32_t run = warp_splits[warp] + incl - my_splits;
-  for (int i = 0; i < per; ++i) {
-    const int b = b0 + i;
-    if (b < batch) {
-      prefix[b] = run;
-      const int c = ctx_lens[b];
-      const bool ok = c >= rows_per_seq && (int64_t)c <= max_ctx;
-      const int nt = ok ? (c + tk - 1) / tk : 0;
-      run += (nt + chunk - 1) / chunk;
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Main kernel.
-// ---------------------------------------------------------------------------
 template <int D, int MT>
 struct Cfg {
-  static constexpr int TK = tile_keys(D, MT);           // keys per pipeline stage
-  static constexpr int WN = kWarps / MT;            // warps splitting the keys of a tile
-  static constexpr int KW = TK / WN;                // keys per warp per tile
-  static constexpr int ROWS = 16 * MT;              // packed query rows (padded)
-  static constexpr int CPK = D / 8;                 // 16-byte chunks per key row
-  static constexpr int TILE_BYTES = TK * D * 2;     // one K (or V) tile
+  static constexpr int TK = tile_keys(D, MT);     // keys per pipeline stage
+  static constexpr int WN = kWarps / MT;          // warps splitting the keys of a tile
+  static constexpr int KW = TK / WN;              // keys per warp per tile
+  static constexpr int NT = KW / 8;               // 8-key n-tiles per warp
+  static constexpr int KSPLIT = NT >= 4 ? 1 : 2;  // independent QK^T chains per n-tile
+  static constexpr int ROWS = 16 * MT;            // packed query rows (padded)
+  static constexpr int SUBS = D / 64;             // 128-byte-wide column slices
+  static constexpr int TILE_BYTES = TK * D * 2;   // one K (or V) tile
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int RING_BYTES = kStages * STAGE_BYTES;
   static constexpr int Q_BYTES = ROWS * D * 2;
-  static constexpr int MERGE_BYTES = 64 * D * 4 + 2 * 64 * 4;  // O, m, l of every warp
-  static constexpr int SCRATCH_BYTES = RING_BYTES > MERGE_BYTES ? RING_BYTES : MERGE_BYTES;
-  static constexpr bool Q_IN_REGS = D <= 128;
+  static constexpr int S = (3 * (STAGE_BYTES + Q_BYTES) <= kSmemBudget) ? 3 : 2;  // pipeline depth
+  static constexpr int RING_BYTES = S * STAGE_BYTES;
+  static constexpr int SCRATCH_BYTES = (WN - 1) * MT * 16 * D * 4;  // cross-warp merge
+  // Two CTAs per SM when their shared memory fits (228 KB per SM, 1 KB reserved per CTA);
+  // then registers are capped so ten warps fit the SM's four register-file partitions,
+  // and the query fragments are re-read from shared memory instead of held in registers.
+  static constexpr int SMEM_EST = 1024 + RING_BYTES + S * Q_BYTES + 2048;
+  static constexpr int MIN_BLOCKS = 2 * (SMEM_EST + 1024) <= 228 * 1024 ? 2 : 1;
+  static constexpr bool Q_IN_REGS = MIN_BLOCKS == 1 && D <= 128;
   static_assert(KW % 16 == 0, "each warp needs whole 16-key steps");
   static_assert(WN * MT == kWarps, "warp layout");
+  static_assert(SCRATCH_BYTES <= STAGE_BYTES, "merge scratch reuses one ring stage");
 };
 
 template <int D, int MT>
 size_t smem_bytes(int batch) {
   using C = Cfg<D, MT>;
-  return align256(C::SCRATCH_BYTES) + align256(C::Q_BYTES) + align256((size_t)(batch + 1) * 4) + 256;
+  return 1024 /* alignment slack */ + (size_t)C::RING_BYTES + (size_t)C::S * C::Q_BYTES + 2 * C::S * 8 +
+         2 * 64 * 4 + 16 + align256((size_t)(batch + 2) * 4) + align256((size_t)batch * 4) + 64;
 }
 
-// Byte offset of 16-byte chunk `ch` of row `row` in a swizzled [rows][D] bf16 tile.
-template <int D>
-__device__ __forceinline__ uint32_t swz(int row, int ch) {
-  return (uint32_t)(row * (D * 2) + ((ch ^ (row & 7)) << 4));
+// Byte offset of 16-byte chunk `ch` (along D) of row `row` in a tile of `rows`
+// rows stored as D/64 slices of [rows][64] bf16 with the 128-byte TMA swizzle.
+__device__ __forceinline__ uint32_t swz(int row, int ch, int rows) {
+  return (uint32_t)((ch >> 3) * rows * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4));
+}
+
+// Position in the stream of key tiles: unit (b, g) and tile index inside it.
+struct Cursor {
+  int b, g, tile, ntiles, seq;
+};
+
+__device__ __forceinline__ void cursor_advance(Cursor& c, const int32_t* s_prefix, int B, int Hkv) {
+  if (++c.tile < c.ntiles) return;
+  c.tile = 0;
+  ++c.seq;
+  if (++c.g < Hkv) return;
+  c.g = 0;
+  do {
+    ++c.b;
+  } while (c.b < B && s_prefix[c.b + 1] == s_prefix[c.b]);
+  c.ntiles = c.b < B ? s_prefix[c.b + 1] - s_prefix[c.b] : 0;
+}
+
+__device__ __forceinline__ Cursor cursor_at(int64_t f, const int32_t* s_prefix, int B, int Hkv) {
+  int lo = 0, hi = B;  // largest b with s_prefix[b] * Hkv <= f
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)s_prefix[mid] * Hkv <= f) lo = mid; else hi = mid;
+  }
+  while (lo < B && s_prefix[lo + 1] == s_prefix[lo]) ++lo;  // skip empty sequences
+  Cursor c;
+  c.b = lo;
+  c.ntiles = s_prefix[lo + 1] - s_prefix[lo];
+  const int64_t r = f - (int64_t)s_prefix[lo] * Hkv;
+  c.g = (int)(r / c.ntiles);
+  c.tile = (int)(r - (int64_t)c.g * c.ntiles);
+  c.seq = 0;
+  return c;
+}
+
+// What the finaliser of a unit needs once the unit's last tile in range is done.
+struct Fin {
+  int b, g, seq;
+  int complete;   // the whole unit lies in this CTA's range: write the output directly
+  int slot;       // partial slot of this CTA's piece
+  int64_t u0;     // first tile of the unit in the tile stream
+  int c0, nseg;   // first CTA holding a piece of the unit, number of pieces
+};
+
+// Partial slot of the piece of unit [u0, ...) held by CTA c: slot 0 for a CTA's
+// first unit, slot 1 for its last one (a CTA's middle units are always whole).
+__device__ __forceinline__ int piece_slot(int c, int c0, int64_t u0, int64_t W) {
+  return 2 * c + ((c == c0 && u0 > (int64_t)c * W) ? 1 : 0);
 }
 
 template <int D, int MT>
-__global__ void __launch_bounds__(kThreads) verify_attention_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, Cfg<D, MT>::MIN_BLOCKS) verify_attention_kernel(const Params p,
+                                                                    const __grid_constant__ CUtensorMap tm_q,
+                                                                    const __grid_constant__ CUtensorMap tm_k,
+                                                                    const __grid_constant__ CUtensorMap tm_v) {
   using C = Cfg<D, MT>;
-  constexpr int TK = C::TK, WN = C::WN, KW = C::KW, CPK = C::CPK;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int TK = C::TK, WN = C::WN, KW = C::KW, NT = C::NT, KSPLIT = C::KSPLIT, S = C::S;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* qs = smem + align256(C::SCRATCH_BYTES);
-  int32_t* s_prefix = reinterpret_cast<int32_t*>(qs + align256(C::Q_BYTES));
-  int32_t* s_misc = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(s_prefix) +
-                                               align256((size_t)(p.batch + 1) * 4));
-  float* m_o = reinterpret_cast<float*>(ring);            // [64][D] after the ring is drained
-  float* m_m = m_o + 64 * D;                              // [64]
-  float* m_l = m_m + 64;                                  // [64]
+  uint8_t* qbuf = ring + C::RING_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(qbuf + S * C::Q_BYTES);
+  uint64_t* empty = full + S;
+  float* s_m = reinterpret_cast<float*>(empty + S);  // [64] cross-warp max
+  float* s_l = s_m + 64;                              // [64] cross-warp sum
+  int32_t* s_bad = reinterpret_cast<int32_t*>(s_l + 64);  // [S] per unit slot: a block id was bad
+  int32_t* s_prefix = s_bad + 4;                           // [B + 1]
+  int32_t* s_ctx = s_prefix + ((p.batch + 2 + 63) & ~63);   // [B] context lengths
+  int32_t* s_misc = s_ctx + ((p.batch + 63) & ~63);          // [16]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int mt = warp / WN, wn = warp % WN;
   const int B = p.batch, Hkv = p.num_kv_heads, G = p.gqa, R = p.rows_per_seq;
+  const int64_t max_ctx = (int64_t)p.max_blocks << p.block_shift;
 
-  for (int i = tid; i <= B; i += kThreads) s_prefix[i] = p.prefix[i];
-  const int chunk = p.hdr->chunk_tiles;
-  const int n_items = p.hdr->total_splits * Hkv;
-  const uint32_t ring_u32 = smem_u32(ring);
-  const uint32_t q_u32 = smem_u32(qs);
-
-  for (;;) {
-    __syncthreads();  // previous item fully done with shared memory
-    if (tid == 0) s_misc[0] = atomicAdd(&p.hdr->next_item, 1);
+  // ---- 1. split plan: per-sequence tile counts and their exclusive prefix (same in every CTA)
+  {
+    const int per = (B + kThreads - 1) / kThreads;
+    const int b0 = tid * per;
+    int mine = 0;
+    for (int i = 0; i < per; ++i) {
+      const int b = b0 + i;
+      if (b < B) {
+        const int c = p.ctx_lens[b];
+        if (c >= R && (int64_t)c <= max_ctx) mine += (c + TK - 1) / TK;
+      }
+    }
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_misc[warp] = incl;
     __syncthreads();
-    const int item = s_misc[0];
-    if (item >= n_items) break;
-    const int us = item / Hkv, g = item - us * Hkv;
-    int lo = 0, hi = B;  // find b with s_prefix[b] <= us < s_prefix[b+1]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_prefix[mid] <= us) lo = mid; else hi = mid;
+    int run = incl - mine;
+    for (int w = 0; w < warp; ++w) run += s_misc[w];
+    if (tid == kThreads - 1) s_prefix[B] = run + mine;
+    for (int i = 0; i < per; ++i) {
+      const int b = b0 + i;
+      if (b < B) {
+        s_prefix[b] = run;
+        const int c = p.ctx_lens[b];
+        s_ctx[b] = c;
+        if (c >= R && (int64_t)c <= max_ctx) run += (c + TK - 1) / TK;
+      }
     }
-    const int b = lo;
-    const int split = us - s_prefix[b];
-    const int nsplit = s_prefix[b + 1] - s_prefix[b];
-    const int ctx = p.ctx_lens[b];
-    const int ntiles = (ctx + TK - 1) / TK;
-    const int tile_begin = split * chunk;
-    const int tile_end = min(ntiles, tile_begin + chunk);
-    const int n_tiles_item = tile_end - tile_begin;
-    const int prefix_len = ctx - R;  // committed tokens before the verify rows
-    const int32_t* table = p.block_table + (int64_t)b * p.max_blocks;
-    bool bad = false;
-
-    // ---- Q tile: packed row r = i*G + j  <-  q[b, i, g*G + j, :]
-    for (int c = tid; c < C::ROWS * CPK; c += kThreads) {
-      const int r = c / CPK, ch = c - r * CPK;
-      const bool valid = r < p.n_rows;
-      const int i = valid ? r / G : 0, j = valid ? r - i * G : 0;
-      const __nv_bfloat16* src = p.q + (((int64_t)b * R + i) * p.num_q_heads + g * G + j) * D + ch * 8;
-      cp_async_16(q_u32 + swz<D>(r, ch), valid ? (const void*)src : (const void*)p.q, valid ? 16u : 0u);
+    if (tid == 0) {
+      for (int s = 0; s < S; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], kWarps);
+      }
+      fence_mbar_init();
     }
+    __syncthreads();
+  }
+  // unusable sequences (ctx out of range) get zero rows, each from one CTA
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    if (s_prefix[b + 1] != s_prefix[b]) continue;
+    if (tid == 0) raise_error(p.dev_err, SPEC_DEVERR_CTX_LEN);
+    float4* dst = reinterpret_cast<float4*>(p.out + (int64_t)b * R * p.num_q_heads * D);
+    for (int i = tid; i < R * p.num_q_heads * D / 4; i += kThreads) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int64_t T = (int64_t)s_prefix[B] * Hkv;
+  if (T == 0) return;
+  const int64_t W = (T + gridDim.x - 1) / gridDim.x;
+  const int64_t f0 = (int64_t)blockIdx.x * W;
+  const int64_t f1 = min(T, f0 + W);
+  if (f0 >= f1) return;
 
-    auto load_tile = [&](int tile, int stage) {
-      const int t0 = (tile_begin + tile) * TK;
-      const uint32_t kdst = ring_u32 + stage * C::STAGE_BYTES;
-      const uint32_t vdst = kdst + C::TILE_BYTES;
-#pragma unroll 4
-      for (int c = tid; c < TK * CPK; c += kThreads) {
-        const int key = c / CPK, ch = c - key * CPK;
-        const int t = t0 + key;
-        bool valid = t < ctx;
-        int64_t off = 0;
-        if (valid) {
-          const int32_t phys = __ldg(table + (t >> p.block_shift));
+  const uint32_t ring_u32 = smem_u32(ring);
+  const uint32_t q_u32 = smem_u32(qbuf);
+
+  // =====================================================================
+  // Producer warp: one thread issues every TMA copy, S stages ahead.
+  // =====================================================================
+  if (warp == kWarps) {
+    // Lane 0 issues the copies. The warp keeps a window of 32 consecutive
+    // block-table entries of the current sequence in its lanes (one coalesced
+    // load per 32 blocks), so issuing a tile never waits on a table lookup.
+    constexpr int BHmax = TK;
+    const int bs = 1 << p.block_shift;
+    const int BH = bs < TK ? bs : TK;  // rows per KV box
+    const int pieces = TK / BH;
+    Cursor ld = cursor_at(f0, s_prefix, B, Hkv);
+    bool fresh = true;
+    int win_b = -1, win_base = 0, win_val = 0;
+    for (int64_t f = f0; f < f1; ++f) {
+      const int s = (int)((f - f0) % S);
+      const int64_t rnd = (f - f0) / S;
+      const int b = ld.b, g = ld.g;
+      const int ctx = s_ctx[b];
+      const int t0 = ld.tile * TK;
+      const int slot = ld.seq % S;
+      int zc[BHmax / 16 > 0 ? BHmax / 16 : 1];  // box row coordinate per piece (bs >= 16)
+      bool bad = false;
+#pragma unroll
+      for (int pc = 0; pc < BHmax / 16; ++pc) {
+        if (pc >= pieces) break;
+        const int t = t0 + pc * BH;
+        int z = -BH;  // fully out of range: the box reads as zeros
+        if (t < ctx) {
+          const int n = t >> p.block_shift;  // logical block
+          if (b != win_b || n < win_base || n >= win_base + 32) {
+            win_b = b;
+            win_base = n;
+            const int nb = (ctx + bs - 1) >> p.block_shift;
+            win_val = (n + lane < nb) ? __ldg(p.block_table + (int64_t)b * p.max_blocks + n + lane) : 0;
+          }
+          const int32_t phys = __shfl_sync(0xffffffffu, win_val, n - win_base);
           if (phys < 0 || (int64_t)phys >= p.num_blocks) {
             bad = true;
-            valid = false;
           } else {
-            off = (((int64_t)phys << p.block_shift) + (t & ((1 << p.block_shift) - 1))) * Hkv + g;
-            off = off * D + ch * 8;
+            z = (int)(((int64_t)phys << p.block_shift) + (t & (bs - 1)));
           }
         }
-        const uint32_t so = swz<D>(key, ch);
-        cp_async_16(kdst + so, p.k_cache + off, valid ? 16u : 0u);
-        cp_async_16(vdst + so, p.v_cache + off, valid ? 16u : 0u);
+        zc[pc] = z;
       }
-    };
-
+      if (lane == 0) {
+        if (rnd > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((rnd - 1) & 1)))
+          raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+        if (fresh) s_bad[slot] = 0;
+        if (bad) s_bad[slot] = 1;
+        const uint32_t q_bytes = fresh ? (uint32_t)(R * G * D * 2) : 0u;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)C::STAGE_BYTES + q_bytes);
+        if (fresh) {
+          const uint32_t qdst = q_u32 + slot * C::Q_BYTES;
 #pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-      if (s < n_tiles_item) load_tile(s, s);
-      cp_async_commit();
+          for (int sub = 0; sub < C::SUBS; ++sub)
+            tma_load_3d(qdst + sub * C::ROWS * 128, &tm_q, sub * 64, g * G, b * R, &full[s]);
+        }
+        const uint32_t kdst = ring_u32 + s * C::STAGE_BYTES;
+        const uint32_t vdst = kdst + C::TILE_BYTES;
+#pragma unroll
+        for (int pc = 0; pc < BHmax / 16; ++pc) {
+          if (pc >= pieces) break;
+#pragma unroll
+          for (int sub = 0; sub < C::SUBS; ++sub) {
+            const uint32_t off = sub * TK * 128 + pc * BH * 128;
+            tma_load_3d(kdst + off, &tm_k, sub * 64, g, zc[pc], &full[s]);
+            tma_load_3d(vdst + off, &tm_v, sub * 64, g, zc[pc], &full[s]);
+          }
+        }
+      }
+      __syncwarp();
+      const int before = ld.seq;
+      cursor_advance(ld, s_prefix, B, Hkv);
+      fresh = ld.seq != before;
     }
+    return;
+  }
 
-    float o[D / 8][4];
-#pragma unroll
-    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};
-    float l_run[2] = {0.f, 0.f};
-    uint32_t qf[C::Q_IN_REGS ? D / 16 : 1][4];
+  // =====================================================================
+  // Consumer warps.
+  // =====================================================================
+  const int mt = warp / WN, wn = warp % WN;
+  // padded query rows stay zero in every query buffer (TMA writes rows < R*G only)
+  for (int i = tid; i < S * C::SUBS * (C::ROWS - p.n_rows) * 8; i += kConsumers) {
+    const int ch = i % 8, rest = i / 8;
+    const int r = p.n_rows + rest % (C::ROWS - p.n_rows);
+    const int bs_sub = rest / (C::ROWS - p.n_rows);
+    const int buf = bs_sub / C::SUBS, sub = bs_sub % C::SUBS;
+    *reinterpret_cast<uint4*>(qbuf + buf * C::Q_BYTES + sub * C::ROWS * 128 + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+  }
+  named_sync(kBarConsumers, kConsumers);
 
-    // rows owned by this thread inside its m16 tile, and their causal limits
-    const int r0 = mt * 16 + (lane >> 2), r1 = r0 + 8;
-    const int lim0 = prefix_len + (r0 < p.n_rows ? r0 / G : 0);
-    const int lim1 = prefix_len + (r1 < p.n_rows ? r1 / G : 0);
+  Cursor cu = cursor_at(f0, s_prefix, B, Hkv);
+  bool cu_fresh = true;
+  bool from_zero = true;
+  float o[D / 8][4];
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  uint32_t qf[C::Q_IN_REGS ? D / 16 : 1][4];
+  int ctx = 0, prefix_len = 0, lim0 = 0, lim1 = 0;
+  const int row_in = lane >> 2;
+  const int r0 = mt * 16 + row_in, r1 = r0 + 8;
 
-    for (int tile = 0; tile < n_tiles_item; ++tile) {
-      cp_async_wait<kStages - 2>();
-      __syncthreads();
-      if (tile + kStages - 1 < n_tiles_item) load_tile(tile + kStages - 1, (tile + kStages - 1) % kStages);
-      cp_async_commit();
-      if (C::Q_IN_REGS && tile == 0) {
-#pragma unroll
-        for (int ks = 0; ks < (C::Q_IN_REGS ? D / 16 : 1); ++ks) {
-          const int mi = lane >> 3;
-          const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
-          ldmatrix_x4(q_u32 + swz<D>(row, 2 * ks + (mi >> 1)), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-        }
-      }
-      const int stage = tile % kStages;
-      const uint32_t kbase = ring_u32 + stage * C::STAGE_BYTES;
-      const uint32_t vbase = kbase + C::TILE_BYTES;
-      const int t0 = (tile_begin + tile) * TK;
-      const int kw0 = wn * KW;
-
-      // ---- S = Q K^T for this warp's KW keys
-      float s[KW / 8][4];
-#pragma unroll
-      for (int n = 0; n < KW / 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t a[4];
-        if constexpr (C::Q_IN_REGS) {
-          a[0] = qf[ks][0]; a[1] = qf[ks][1]; a[2] = qf[ks][2]; a[3] = qf[ks][3];
-        } else {
-          const int mi = lane >> 3;
-          const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
-          ldmatrix_x4(q_u32 + swz<D>(row, 2 * ks + (mi >> 1)), a[0], a[1], a[2], a[3]);
-        }
-#pragma unroll
-        for (int np = 0; np < KW / 16; ++np) {
-          const int mi = lane >> 3;
-          const int key = kw0 + np * 16 + (mi >> 1) * 8 + (lane & 7);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4(kbase + swz<D>(key, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-          mma_bf16_16816(s[2 * np], a, b0, b1);
-          mma_bf16_16816(s[2 * np + 1], a, b2, b3);
-        }
-      }
-
-      // ---- scale, causal mask, online softmax (log2 domain)
-      const bool needs_mask = t0 + TK - 1 > prefix_len;
-      float tmax[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-      for (int n = 0; n < KW / 8; ++n) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float x = s[n][e] * p.scale_log2;
-          if (needs_mask) {
-            const int t = t0 + kw0 + n * 8 + 2 * (lane & 3) + (e & 1);
-            if (t > (e < 2 ? lim0 : lim1)) x = -INFINITY;
-          }
-          s[n][e] = x;
-          tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
-        }
-      }
-      float alpha[2], m_use[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 1));
-        tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 2));
-        const float m_new = fmaxf(m_run[h], tmax[h]);
-        m_use[h] = m_new == -INFINITY ? 0.f : m_new;
-        alpha[h] = fast_exp2(m_run[h] - m_use[h]);  // exp2(-inf) = 0 on the first visible tile
-        m_run[h] = m_new;
-        l_run[h] *= alpha[h];
-      }
-#pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        o[n][0] *= alpha[0]; o[n][1] *= alpha[0];
-        o[n][2] *= alpha[1]; o[n][3] *= alpha[1];
-      }
-#pragma unroll
-      for (int n = 0; n < KW / 8; ++n) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pv = fast_exp2(s[n][e] - m_use[e >> 1]);
-          s[n][e] = pv;
-          l_run[e >> 1] += pv;
-        }
-      }
-
-      // ---- O += P V, with P = P_hi + P_lo (two bf16 products)
-#pragma unroll
-      for (int kk = 0; kk < KW / 16; ++kk) {
-        uint32_t ah[4], al[4];
-        {
-          const float* p0 = s[2 * kk];
-          const float* p1 = s[2 * kk + 1];
-          const float src[8] = {p0[0], p0[1], p0[2], p0[3], p1[0], p1[1], p1[2], p1[3]};
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(src[2 * r], src[2 * r + 1]);
-            const float2 hf = __bfloat1622float2(h2);
-            ah[r] = *reinterpret_cast<const uint32_t*>(&h2);
-            al[r] = pack_bf16(src[2 * r] - hf.x, src[2 * r + 1] - hf.y);
-          }
-        }
-#pragma unroll
-        for (int dp = 0; dp < D / 16; ++dp) {
-          const int mi = lane >> 3;
-          const int key = kw0 + kk * 16 + (mi & 1) * 8 + (lane & 7);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(vbase + swz<D>(key, 2 * dp + (mi >> 1)), b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * dp], ah, b0, b1);
-          mma_bf16_16816(o[2 * dp], al, b0, b1);
-          mma_bf16_16816(o[2 * dp + 1], ah, b2, b3);
-          mma_bf16_16816(o[2 * dp + 1], al, b2, b3);
-        }
-      }
-    }
-
-    // ---- combine the WN key-split warps and write the item's result
+  // Combine a finished unit: merge the key-split warps, then write the output
+  // (whole unit) or a normalised partial, and let the last piece merge them all.
+  auto finalize = [&](const Fin& F, float* scratch) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
       l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
     }
-    cp_async_wait<0>();
-    bad = __syncthreads_or(bad) != 0;
-    {
-      const int base_row = wn * C::ROWS + mt * 16 + (lane >> 2);
+    named_sync(kBarConsumers, kConsumers);  // every warp is done reading the stage used as scratch
+    if constexpr (WN > 1) {
+      if (wn > 0) {
+        const int base = ((wn - 1) * MT + mt) * 16;
 #pragma unroll
-      for (int n = 0; n < D / 8; ++n) {
-        const int d = n * 8 + 2 * (lane & 3);
-        *reinterpret_cast<float2*>(&m_o[base_row * D + d]) = make_float2(o[n][0], o[n][1]);
-        *reinterpret_cast<float2*>(&m_o[(base_row + 8) * D + d]) = make_float2(o[n][2], o[n][3]);
-      }
-      if ((lane & 3) == 0) {
-        m_m[base_row] = m_run[0];
-        m_l[base_row] = l_run[0];
-        m_m[base_row + 8] = m_run[1];
-        m_l[base_row + 8] = l_run[1];
-      }
-    }
-    __syncthreads();
-    if (bad && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
-    const bool direct = nsplit == 1;
-    for (int idx = tid; idx < p.n_rows * (D / 4); idx += kThreads) {
-      const int r = idx / (D / 4), d4 = idx - r * (D / 4);
-      // r lives in m-tile r/16; the WN warps of that m-tile hold partial sums
-      const int rmt = r >> 4, rin = r & 15;
-      float M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < WN; ++w) M = fmaxf(M, m_m[w * C::ROWS + rmt * 16 + rin]);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      float L = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < WN; ++w) {
-        const int row = w * C::ROWS + rmt * 16 + rin;
-        const float f = fast_exp2(m_m[row] - Mu);
-        L += m_l[row] * f;
-        const float4 v = *reinterpret_cast<const float4*>(&m_o[row * D + d4 * 4]);
-        acc.x += v.x * f; acc.y += v.y * f; acc.z += v.z * f; acc.w += v.w * f;
-      }
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-      if (bad) acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (direct) {
-        const int i = r / G, j = r - i * G;
-        float* dst = p.out + (((int64_t)b * R + i) * p.num_q_heads + g * G + j) * D + d4 * 4;
-        *reinterpret_cast<float4*>(dst) = acc;
-      } else {
-        *reinterpret_cast<float4*>(p.opart + ((int64_t)item * p.n_rows + r) * D + d4 * 4) = acc;
-        if (d4 == 0) {
-          float lse2 = L > 0.f ? M + __log2f(L) : -INFINITY;
-          if (bad) lse2 = __int_as_float(0x7fc00000);  // NaN marks an unusable partial
-          p.lse[(int64_t)item * p.n_rows + r] = lse2;
+        for (int n = 0; n < D / 8; ++n) {
+          const int d = n * 8 + 2 * (lane & 3);
+          *reinterpret_cast<float2*>(&scratch[(base + row_in) * D + d]) = make_float2(o[n][0], o[n][1]);
+          *reinterpret_cast<float2*>(&scratch[(base + row_in + 8) * D + d]) = make_float2(o[n][2], o[n][3]);
+        }
+        if ((lane & 3) == 0) {
+          s_m[base + row_in] = m_run[0];
+          s_l[base + row_in] = l_run[0];
+          s_m[base + row_in + 8] = m_run[1];
+          s_l[base + row_in + 8] = l_run[1];
         }
       }
     }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Merge of split partials by log-sum-exp; zero rows for unusable sequences.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) merge_kernel(const Params p, int D) {
-  const int Hkv = p.num_kv_heads, G = p.gqa, R = p.rows_per_seq;
-  const int b = blockIdx.x / Hkv, g = blockIdx.x - b * Hkv;
-  const int first = p.prefix[b];
-  const int nsplit = p.prefix[b + 1] - first;
-  if (nsplit == 1) return;  // written directly by the main kernel
-  const int d4n = D / 4;
-  for (int idx = threadIdx.x; idx < p.n_rows * d4n; idx += blockDim.x) {
-    const int r = idx / d4n, d4 = idx - r * d4n;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (nsplit > 1) {
-      float M = -INFINITY;
-      bool bad = false;
-      for (int s = 0; s < nsplit; ++s) {
-        const float l = p.lse[((int64_t)(first + s) * Hkv + g) * p.n_rows + r];
-        bad |= l != l;
-        M = fmaxf(M, l);
+    const bool bad = named_sync_or(kBarConsumers, kConsumers, s_bad[F.seq % S] != 0);
+    if (wn == 0) {
+      float M[2] = {m_run[0], m_run[1]};
+      if constexpr (WN > 1) {
+#pragma unroll
+        for (int w = 1; w < WN; ++w) {
+          const int base = ((w - 1) * MT + mt) * 16 + row_in;
+          M[0] = fmaxf(M[0], s_m[base]);
+          M[1] = fmaxf(M[1], s_m[base + 8]);
+        }
       }
-      if (!bad && M != -INFINITY) {
-        float W = 0.f;
-        for (int s = 0; s < nsplit; ++s) {
-          const int64_t it = (int64_t)(first + s) * Hkv + g;
-          const float f = exp2f(p.lse[it * p.n_rows + r] - M);
-          if (f > 0.f) {
-            const float4 v = *reinterpret_cast<const float4*>(p.opart + (it * p.n_rows + r) * D + d4 * 4);
-            acc.x += f * v.x; acc.y += f * v.y; acc.z += f * v.z; acc.w += f * v.w;
+      float Mu[2], L[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        Mu[h] = M[h] == -INFINITY ? 0.f : M[h];
+        const float f = fast_exp2(m_run[h] - Mu[h]);
+        L[h] = l_run[h] * f;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+          o[n][2 * h] *= f;
+          o[n][2 * h + 1] *= f;
+        }
+      }
+      if constexpr (WN > 1) {
+#pragma unroll
+        for (int w = 1; w < WN; ++w) {
+          const int base = ((w - 1) * MT + mt) * 16 + row_in;
+          const float fa = fast_exp2(s_m[base] - Mu[0]);
+          const float fb = fast_exp2(s_m[base + 8] - Mu[1]);
+          L[0] += s_l[base] * fa;
+          L[1] += s_l[base + 8] * fb;
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n) {
+            const int d = n * 8 + 2 * (lane & 3);
+            const float2 va = *reinterpret_cast<const float2*>(&scratch[base * D + d]);
+            const float2 vb = *reinterpret_cast<const float2*>(&scratch[(base + 8) * D + d]);
+            o[n][0] += va.x * fa;
+            o[n][1] += va.y * fa;
+            o[n][2] += vb.x * fb;
+            o[n][3] += vb.y * fb;
           }
-          W += f;
         }
-        const float inv = 1.f / W;
-        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = h == 0 ? r0 : r1;
+        if (r < p.n_rows) {
+          const float inv = (L[h] > 0.f && !bad) ? 1.f / L[h] : 0.f;
+          float* dst;
+          if (F.complete) {
+            const int i = r / G, j = r - i * G;
+            dst = p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
+          } else {
+            dst = p.opart + ((int64_t)F.slot * p.n_rows + r) * D;
+            if ((lane & 3) == 0) {
+              float lse2 = L[h] > 0.f ? M[h] + __log2f(L[h]) : -INFINITY;
+              if (bad) lse2 = __int_as_float(0x7fc00000);  // NaN marks an unusable piece
+              p.lse[(int64_t)F.slot * p.n_rows + r] = lse2;
+            }
+          }
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n) {
+            const int d = n * 8 + 2 * (lane & 3);
+            *reinterpret_cast<float2*>(dst + d) = make_float2(o[n][2 * h] * inv, o[n][2 * h + 1] * inv);
+          }
+        }
       }
     }
-    const int i = r / G, j = r - i * G;
-    *reinterpret_cast<float4*>(p.out + (((int64_t)b * R + i) * p.num_q_heads + g * G + j) * D + d4 * 4) = acc;
+    if (bad && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
+    if (!F.complete) {
+      __threadfence();  // publish this piece before counting it
+      named_sync(kBarConsumers, kConsumers);
+      const int unit = F.b * Hkv + F.g;
+      if (tid == 0) s_misc[8] = (atomicAdd(p.counters + unit, 1) == F.nseg - 1) ? 1 : 0;
+      named_sync(kBarConsumers, kConsumers);
+      if (s_misc[8]) {
+        __threadfence();
+        for (int idx = tid; idx < p.n_rows * (D / 4); idx += kConsumers) {
+          const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+          float Mx = -INFINITY;
+          bool nan = false;
+          for (int s = 0; s < F.nseg; ++s) {
+            const int slot = piece_slot(F.c0 + s, F.c0, F.u0, W);
+            const float l = __ldcg(p.lse + (int64_t)slot * p.n_rows + r);
+            nan |= l != l;
+            Mx = fmaxf(Mx, l);
+          }
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (!nan && Mx != -INFINITY) {
+            float wsum = 0.f;
+            for (int s = 0; s < F.nseg; ++s) {
+              const int slot = piece_slot(F.c0 + s, F.c0, F.u0, W);
+              const float wgt = exp2f(__ldcg(p.lse + (int64_t)slot * p.n_rows + r) - Mx);
+              if (wgt > 0.f) {
+                const float4 v =
+                    __ldcg(reinterpret_cast<const float4*>(p.opart + ((int64_t)slot * p.n_rows + r) * D) + d4);
+                acc.x += wgt * v.x;
+                acc.y += wgt * v.y;
+                acc.z += wgt * v.z;
+                acc.w += wgt * v.w;
+              }
+              wsum += wgt;
+            }
+            const float inv = 1.f / wsum;
+            acc.x *= inv;
+            acc.y *= inv;
+            acc.z *= inv;
+            acc.w *= inv;
+          }
+          const int i = r / G, j = r - i * G;
+          reinterpret_cast<float4*>(p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D)[d4] = acc;
+        }
+        if (tid == 0) p.counters[unit] = 0;  // ready for the next call
+      }
+    }
+    fence_proxy_async_smem();  // scratch writes before the next TMA into this stage
+    named_sync(kBarConsumers, kConsumers);
+  };
+
+  for (int64_t f = f0; f < f1; ++f) {
+    const int stage = (int)((f - f0) % S);
+    const int64_t rnd = (f - f0) / S;
+    if (!mbar_wait_bounded(&full[stage], (uint32_t)(rnd & 1)) && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+    const uint32_t kbase = ring_u32 + stage * C::STAGE_BYTES;
+    const uint32_t vbase = kbase + C::TILE_BYTES;
+    const uint32_t qb = q_u32 + (cu.seq % S) * C::Q_BYTES;
+    const int t0 = cu.tile * TK;
+
+    if (cu_fresh) {
+      from_zero = cu.tile == 0;
+      ctx = s_ctx[cu.b];
+      prefix_len = ctx - R;
+      lim0 = prefix_len + (r0 < p.n_rows ? r0 / G : 0);
+      lim1 = prefix_len + (r1 < p.n_rows ? r1 / G : 0);
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
+      if constexpr (C::Q_IN_REGS) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int mi = lane >> 3;
+          const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
+          ldmatrix_x4(qb + swz(row, 2 * ks + (mi >> 1), C::ROWS), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+        }
+      }
+    }
+    // keys past the context in the last tile may hold stale cache bytes: zero those V rows
+    if (t0 + TK > ctx) {
+      const int valid = ctx - t0;
+      for (int i = tid; i < (TK - valid) * (D / 8); i += kConsumers) {
+        const int row = valid + i / (D / 8), ch = i % (D / 8);
+        *reinterpret_cast<uint4*>(ring + stage * C::STAGE_BYTES + C::TILE_BYTES + swz(row, ch, TK)) =
+            make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      named_sync(kBarConsumers, kConsumers);
+    }
+    const int kw0 = wn * KW;
+
+    // ---- S = Q K^T for this warp's KW keys (KSPLIT independent chains per n-tile)
+    float sacc[KSPLIT][NT][4];
+#pragma unroll
+    for (int c = 0; c < KSPLIT; ++c)
+#pragma unroll
+      for (int n = 0; n < NT; ++n) sacc[c][n][0] = sacc[c][n][1] = sacc[c][n][2] = sacc[c][n][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+      uint32_t a[4];
+      if constexpr (C::Q_IN_REGS) {
+        a[0] = qf[ks][0]; a[1] = qf[ks][1]; a[2] = qf[ks][2]; a[3] = qf[ks][3];
+      } else {
+        const int mi = lane >> 3;
+        const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
+        ldmatrix_x4(qb + swz(row, 2 * ks + (mi >> 1), C::ROWS), a[0], a[1], a[2], a[3]);
+      }
+#pragma unroll
+      for (int np = 0; np < NT / 2; ++np) {
+        const int mi = lane >> 3;
+        const int key = kw0 + np * 16 + (mi >> 1) * 8 + (lane & 7);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(kbase + swz(key, 2 * ks + (mi & 1), TK), b0, b1, b2, b3);
+        mma_bf16_16816(sacc[ks % KSPLIT][2 * np], a, b0, b1);
+        mma_bf16_16816(sacc[ks % KSPLIT][2 * np + 1], a, b2, b3);
+      }
+    }
+    float s[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float v = sacc[0][n][e];
+        if constexpr (KSPLIT > 1) v += sacc[1][n][e];
+        s[n][e] = v;
+      }
+
+    // ---- scale, causal mask, online softmax (log2 domain, lazy rescaling)
+    const bool needs_mask = t0 + TK - 1 > prefix_len;
+    float tmax[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float x = s[n][e] * p.scale_log2;
+        if (needs_mask) {
+          const int t = t0 + kw0 + n * 8 + 2 * (lane & 3) + (e & 1);
+          if (t > (e < 2 ? lim0 : lim1)) x = -INFINITY;
+        }
+        s[n][e] = x;
+        tmax[e >> 1] = fmaxf(tmax[e >> 1], x);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 1));
+      tmax[h] = fmaxf(tmax[h], __shfl_xor_sync(0xffffffffu, tmax[h], 2));
+    }
+    // The running max may lag the true max by up to 8 (log2 units): P <= 256 stays
+    // exact enough in fp32 and in the hi/lo bf16 split, and O is rescaled rarely.
+    const bool grow = tmax[0] > m_run[0] + 8.f || tmax[1] > m_run[1] + 8.f;
+    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float m_new = fmaxf(m_run[h], tmax[h]);
+        const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_run[h] - m_new);
+        m_run[h] = m_new;
+        l_run[h] *= alpha;
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+          o[n][2 * h] *= alpha;
+          o[n][2 * h + 1] *= alpha;
+        }
+      }
+    }
+    const float m_use0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+    const float m_use1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float pv = fast_exp2(s[n][e] - (e < 2 ? m_use0 : m_use1));
+        s[n][e] = pv;
+        l_run[e >> 1] += pv;
+      }
+    }
+
+    // ---- O += P V with P = P_hi + P_lo (two bf16 products)
+#pragma unroll
+    for (int kk = 0; kk < KW / 16; ++kk) {
+      uint32_t ah[4], al[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float* pp = s[2 * kk + (r >> 1)];
+        const float x0 = pp[2 * (r & 1)], x1 = pp[2 * (r & 1) + 1];
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(x0, x1);
+        const float2 hf = __bfloat1622float2(h2);
+        ah[r] = *reinterpret_cast<const uint32_t*>(&h2);
+        al[r] = pack_bf16(x0 - hf.x, x1 - hf.y);
+      }
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        const int mi = lane >> 3;
+        const int key = kw0 + kk * 16 + (mi & 1) * 8 + (lane & 7);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(vbase + swz(key, 2 * dp + (mi >> 1), TK), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dp], ah, b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], ah, b2, b3);
+        mma_bf16_16816(o[2 * dp], al, b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], al, b2, b3);
+      }
+    }
+
+    // ---- end of this unit's tiles in range: finalise (the stage is the scratch)
+    if (f == f1 - 1 || cu.tile == cu.ntiles - 1) {
+      Fin fin;
+      const int64_t u0 = (int64_t)s_prefix[cu.b] * Hkv + (int64_t)cu.g * cu.ntiles;
+      fin.b = cu.b;
+      fin.g = cu.g;
+      fin.seq = cu.seq;
+      fin.complete = from_zero && cu.tile == cu.ntiles - 1;
+      fin.u0 = u0;
+      fin.c0 = (int)(u0 / W);
+      fin.nseg = (int)((u0 + cu.ntiles - 1) / W) - fin.c0 + 1;
+      fin.slot = piece_slot((int)blockIdx.x, fin.c0, u0, W);
+      finalize(fin, reinterpret_cast<float*>(ring + stage * C::STAGE_BYTES));
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    const int before = cu.seq;
+    cursor_advance(cu, s_prefix, B, Hkv);
+    cu_fresh = cu.seq != before;
   }
 }
 
@@ -508,8 +664,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const Params p, int D) {
 // Host side
 // ---------------------------------------------------------------------------
 struct Layout {
-  size_t prefix_off, lse_off, opart_off, total;
-  int64_t max_items;
+  size_t lse_off, opart_off, total;
 };
 
 static bool desc_ok(const spec_attn_desc* d, int k_draft) {
@@ -528,43 +683,85 @@ static bool shape_supported(const spec_attn_desc* d, int k_draft) {
   if (rows > 64) return false;
   if (d->batch > kMaxBatch) return false;
   if ((int64_t)d->max_blocks_per_seq * bs > INT32_MAX / 2) return false;
+  if ((int64_t)d->num_blocks * bs > INT32_MAX) return false;  // TMA row coordinate is 32-bit
+  if ((int64_t)d->batch * (k_draft + 1) > INT32_MAX) return false;
   return true;
 }
 
 static Layout layout_for(const spec_attn_desc* d, int k_draft) {
   Layout L;
   const int64_t n_rows = (int64_t)(k_draft + 1) * (d->num_q_heads / d->num_kv_heads);
-  L.max_items = kTargetItems + (int64_t)d->num_kv_heads * d->batch;
-  L.prefix_off = kHeaderBytes;
-  L.lse_off = L.prefix_off + align256((size_t)(d->batch + 1) * 4);
-  L.opart_off = L.lse_off + align256((size_t)(L.max_items * n_rows * 4));
-  L.total = L.opart_off + align256((size_t)(L.max_items * n_rows * d->head_dim * 4));
+  const int64_t slots = 2 * (int64_t)kMaxGrid;
+  L.lse_off = align256((size_t)d->batch * d->num_kv_heads * 4);
+  L.opart_off = L.lse_off + align256((size_t)(slots * n_rows * 4));
+  L.total = L.opart_off + align256((size_t)(slots * n_rows * d->head_dim * 4));
   return L;
 }
 
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// A bf16 3-D view {x: 64-wide slice of D, y: head, z: token row} with 128-byte swizzle.
+static bool make_map(CUtensorMap* map, const void* base, uint64_t D, uint64_t heads, uint64_t rows,
+                     uint32_t box_heads, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {D, heads, rows};
+  const cuuint64_t strides[2] = {D * 2, heads * D * 2};
+  const cuuint32_t box[3] = {64, box_heads, box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int MT>
-static int launch_main(const Params& p, int batch, cudaStream_t stream) {
+static int launch_main(const Params& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       cudaStream_t stream) {
   auto kern = verify_attention_kernel<D, MT>;
-  const size_t smem = smem_bytes<D, MT>(batch);
+  const size_t smem = smem_bytes<D, MT>(p.batch);
+  static int cached_dev = -1, cached_grid = 0;
+  static size_t cached_smem = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return SPEC_ERR_LAUNCH;
-  int sms = 0, per_sm = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
-    return SPEC_ERR_LAUNCH;
-  if (per_sm < 1) return SPEC_ERR_UNSUPPORTED;
-  kern<<<sms * per_sm, kThreads, smem, stream>>>(p);
+  if (dev != cached_dev || smem != cached_smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SPEC_ERR_LAUNCH;
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+      return SPEC_ERR_LAUNCH;
+    if (per_sm < 1) return SPEC_ERR_UNSUPPORTED;
+    cached_grid = sms * per_sm > kMaxGrid ? kMaxGrid : sms * per_sm;
+    cached_dev = dev;
+    cached_smem = smem;
+  }
+  kern<<<cached_grid, kThreads, smem, stream>>>(p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
 template <int D>
-static int launch_main_d(const Params& p, int mt, int batch, cudaStream_t stream) {
+static int launch_main_d(const Params& p, int mt, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, cudaStream_t stream) {
   switch (mt) {
-    case 1: return launch_main<D, 1>(p, batch, stream);
-    case 2: return launch_main<D, 2>(p, batch, stream);
-    default: return launch_main<D, 4>(p, batch, stream);
+    case 1: return launch_main<D, 1>(p, tq, tk, tv, stream);
+    case 2: return launch_main<D, 2>(p, tq, tk, tv, stream);
+    default: return launch_main<D, 4>(p, tq, tk, tv, stream);
   }
 }
 
@@ -594,47 +791,43 @@ extern "C" int spec_verify_attention(const void* q, const void* k_cache, const v
     return SPEC_ERR_INVALID_ARG;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
+  const int R = k_draft + 1, G = d->num_q_heads / d->num_kv_heads, D = d->head_dim;
+  const int bs = d->block_size;
+  const int mt = R * G <= 16 ? 1 : (R * G <= 32 ? 2 : 4);
+  const int tk = attn::tile_keys(D, mt);
+  CUtensorMap tq, tk_map, tv_map;
+  if (!attn::make_map(&tq, q, D, d->num_q_heads, (uint64_t)d->batch * R, (uint32_t)G, (uint32_t)R) ||
+      !attn::make_map(&tk_map, k_cache, D, d->num_kv_heads, (uint64_t)d->num_blocks * bs, 1,
+                      (uint32_t)(bs < tk ? bs : tk)) ||
+      !attn::make_map(&tv_map, v_cache, D, d->num_kv_heads, (uint64_t)d->num_blocks * bs, 1,
+                      (uint32_t)(bs < tk ? bs : tk)))
+    return SPEC_ERR_LAUNCH;
+
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   attn::Params p;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
-  p.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
   p.block_table = block_table;
   p.ctx_lens = ctx_lens;
   p.out = out;
-  p.hdr = reinterpret_cast<attn::WsHeader*>(ws);
-  p.prefix = reinterpret_cast<const int32_t*>(ws + L.prefix_off);
+  p.counters = reinterpret_cast<int32_t*>(ws);
   p.lse = reinterpret_cast<float*>(ws + L.lse_off);
   p.opart = reinterpret_cast<float*>(ws + L.opart_off);
   p.dev_err = dev_err;
   p.num_blocks = d->num_blocks;
   p.batch = d->batch;
-  p.rows_per_seq = k_draft + 1;
+  p.rows_per_seq = R;
   p.num_q_heads = d->num_q_heads;
   p.num_kv_heads = d->num_kv_heads;
-  p.gqa = d->num_q_heads / d->num_kv_heads;
-  p.n_rows = p.rows_per_seq * p.gqa;
+  p.gqa = G;
+  p.n_rows = R * G;
   int shift = 0;
-  while ((1 << shift) < d->block_size) ++shift;
+  while ((1 << shift) < bs) ++shift;
   p.block_shift = shift;
   p.max_blocks = d->max_blocks_per_seq;
-  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d->head_dim));
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
 
-  const int D = d->head_dim;
-  const int mt = p.n_rows <= 16 ? 1 : (p.n_rows <= 32 ? 2 : 4);
-  const int tk = attn::tile_keys(D, mt);
-  const int64_t max_ctx = (int64_t)d->max_blocks_per_seq * d->block_size;
-
-  attn::plan_kernel<<<1, 1024, 0, stream>>>(ctx_lens, d->batch, p.rows_per_seq, max_ctx, tk, d->num_kv_heads,
-                                            p.hdr, reinterpret_cast<int32_t*>(ws + L.prefix_off), dev_err);
-  if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_LAUNCH;
-  int rc;
   switch (D) {
-    case 64: rc = attn::launch_main_d<64>(p, mt, d->batch, stream); break;
-    case 128: rc = attn::launch_main_d<128>(p, mt, d->batch, stream); break;
-    default: rc = attn::launch_main_d<256>(p, mt, d->batch, stream); break;
+    case 64: return attn::launch_main_d<64>(p, mt, tq, tk_map, tv_map, stream);
+    case 128: return attn::launch_main_d<128>(p, mt, tq, tk_map, tv_map, stream);
+    default: return attn::launch_main_d<256>(p, mt, tq, tk_map, tv_map, stream);
   }
-  if (rc != SPEC_OK) return rc;
-  attn::merge_kernel<<<d->batch * d->num_kv_heads, 256, 0, stream>>>(p, D);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }

@@ -84,8 +84,8 @@ def test_attention_full_size_sampled_sequences(sv, oracle_mod, name):
 def test_attention_is_deterministic_and_reuses_workspace(sv):
     w = wl.WORKLOADS["llama8b_eagle3"].replace(batch=8, ctx_lens=(2048,) * 8)
     a = wl.make_attention_inputs(w, device=DEV)
-    ws = torch.empty(sv.spec_verify_attention_workspace(a["q"], a["k_cache"], a["block_table"], w.k_draft),
-                     dtype=torch.uint8, device=DEV)
+    ws = sv.new_attention_workspace(
+        sv.spec_verify_attention_workspace(a["q"], a["k_cache"], a["block_table"], w.k_draft), DEV)
     o1, _ = run_attention(sv, a, w, workspace=ws)
     o2, _ = run_attention(sv, a, w, workspace=ws)
     assert torch.equal(o1, o2)
