@@ -14,9 +14,8 @@ Readings of the pages that the oracle fixes (the pages leave them open):
 ctx_lens counts the verify tokens; row i sits at absolute position
 ctx - (k+1) + i; GQA groups are contiguous; softmax scale 1/sqrt(D); greedy
 ties go to the lowest index; acceptance compares u*q < p; the residual falls
-back to p when max(0, p-q) is all zero; the correction/bonus token is an
-inverse-CDF draw with one Philox uniform per row, as documented in
-spec_verify.h.
+back to p when max(0, p-q) is all zero; the correction/bonus draw is an
+exponential race keyed by Philox words as documented in spec_verify.h.
 """
 
 from __future__ import annotations
@@ -155,9 +154,8 @@ def accept(target_logits, draft_tokens, draft_probs, seed: int, mode, temperatur
     """Greedy / speculative-sampling acceptance, double precision.
 
     Returns (out_tokens [B,k+1] int32, accept_len [B] int32, accept_margin [B],
-    draw_margin [B], status). accept_margin is the smallest |u - p/q| among the
-    drafts tested; draw_margin the distance of the final inverse-CDF draw from
-    the nearest cumulative boundary, relative to the total weight.
+    race_gap [B], status). accept_margin is the smallest |u - p/q| among the
+    drafts tested; race_gap the relative gap between the two largest race keys.
     """
     lib = _load()
     L = _c(target_logits, np.float32)

@@ -23,8 +23,7 @@
  *    lmdeploy PR #3945 review of spec_decode/reject_sampler.py, whose fixture
  *    pads the emitted tokens with -1), i.e. the rule of Leviathan et al. 2023
  *    and Chen et al. 2023: accept a draft d with probability min(1, p(d)/q(d)),
- *    otherwise draw from max(0, p - q) normalised; the draw is inverse-CDF
- *    sampling with one uniform per row (an exact sampler of w / sum(w)).
+ *    otherwise draw from max(0, p - q) normalised.
  *  - Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
  *    easy as 1, 2, 3", SC'11.
  *  - state commit: the operators publish the recurrent state after every verify
@@ -248,29 +247,30 @@ static void softmax_stats(const float* row, int V, double T, double* mx, double*
 }
 
 /*
- * Inverse-CDF draw from non-negative weights w (length V): the first x whose
- * running sum of w exceeds u * sum(w). *margin receives the distance from
- * u * sum(w) to the nearer of the two running-sum boundaries around x,
- * relative to sum(w) (a draw near a boundary is a near tie).
+ * Exponential race over weights w (length V): argmax_x w(x) / E_x with
+ * E_x = -ln U(word x mod 4 of Philox counter (x/4, m, b, 1)). Ties go to the
+ * lowest index. Returns the winner; *gap receives (best - second) / best.
  */
-static int inverse_cdf(const double* w, int V, double u, double* margin) {
-  double total = 0.0;
-  for (int x = 0; x < V; ++x) total += w[x];
-  const double target = u * total;
-  double run = 0.0;
-  int last_positive = 0;
+static int exponential_race(const double* w, int V, uint64_t seed, int m, int b, double* gap) {
+  int best = -1;
+  double best_key = -1.0, second_key = -1.0;
   for (int x = 0; x < V; ++x) {
-    if (w[x] > 0.0) last_positive = x;
-    const double next = run + w[x];
-    if (next > target) {
-      const double a = target - run, b = next - target;
-      *margin = (a < b ? a : b) / total;
-      return x;
+    uint32_t word = philox_word(seed, (uint32_t)(x / 4), (uint32_t)m, (uint32_t)b, 1u, x % 4);
+    double e = -log(oracle_uniform(word));
+    double key = w[x] / e;
+    if (key > best_key) {
+      second_key = best_key;
+      best_key = key;
+      best = x;
+    } else if (key > second_key) {
+      second_key = key;
     }
-    run = next;
   }
-  *margin = 0.0;
-  return last_positive;
+  if (best_key > 0.0)
+    *gap = (best_key - (second_key > 0.0 ? second_key : 0.0)) / best_key;
+  else
+    *gap = 0.0;
+  return best;
 }
 
 /*
@@ -278,16 +278,15 @@ static int inverse_cdf(const double* w, int V, double u, double* margin) {
  * NULL when every row is greedy); mode [B] (0 greedy, 1 sampling);
  * temperature [B]. Outputs out_tokens [B,k+1], accept_len [B], and for the
  * parity bookkeeping accept_margin [B] = min over the drafts that were tested
- * of |u - p/q| (+inf for greedy rows or when every q was 0) and draw_margin [B]
- * = relative distance of the final draw from a cumulative boundary (+inf for
- * greedy rows).
+ * of |u - p/q| (+inf for greedy rows or when every q was 0) and race_gap [B] =
+ * relative gap between the two largest race keys (+inf for greedy rows).
  * Invalid rows (draft token out of range, sampling temperature not > 0) get
  * out_tokens -1 and accept_len -1; the call then returns an error code but
  * still computes every other row.
  */
 int oracle_accept(const float* target_logits, const int32_t* draft_tokens, const float* draft_probs,
                   uint64_t seed, const int32_t* mode, const float* temperature, int B, int k, int V,
-                  int32_t* out_tokens, int32_t* accept_len, double* accept_margin, double* draw_margin,
+                  int32_t* out_tokens, int32_t* accept_len, double* accept_margin, double* race_gap,
                   int n_threads) {
   if (!target_logits || !draft_tokens || !mode || !temperature || !out_tokens || !accept_len)
     return ORACLE_ERR_ARG;
@@ -364,8 +363,7 @@ int oracle_accept(const float* target_logits, const int32_t* draft_tokens, const
           for (int x = 0; x < V; ++x) w[x] = exp((double)L[(int64_t)k * V + x] / T - mx) / z;
         }
         for (int j = 0; j < m; ++j) tok[j] = d[j];
-        const double u_draw = oracle_uniform(philox_word(seed, 0u, (uint32_t)m, (uint32_t)b, 1u, 0));
-        tok[m] = inverse_cdf(w, V, u_draw, &gap);
+        tok[m] = exponential_race(w, V, seed, m, b, &gap);
         free(w);
       }
     }
@@ -377,7 +375,7 @@ int oracle_accept(const float* target_logits, const int32_t* draft_tokens, const
     }
     accept_len[b] = m;
     if (accept_margin) accept_margin[b] = margin;
-    if (draw_margin) draw_margin[b] = gap;
+    if (race_gap) race_gap[b] = gap;
   }
   return status;
 }

@@ -5,7 +5,7 @@ import torch
 
 ATTN_MAX_ABS = 1e-2      # attention: max-abs error vs the double-precision oracle
 ATTN_REL_L2 = 2e-3       # attention: relative L2 error vs the oracle
-NEAR_TIE = 1e-5          # sampled decisions: |u - p/q| (or the draw's CDF margin) below this are excused
+NEAR_TIE = 1e-5          # sampled decisions: |u - p/q| (or race keys this close, relative) are excused
 MAX_EXCUSED_RATE = 1e-4  # ... and must stay below this share of decisions
 
 
@@ -24,10 +24,10 @@ def oracle_attention_for(oracle, a: dict, seqs=None):
                                    a["block_table"].cpu().numpy(), a["ctx_lens"].cpu().numpy(), seqs=seqs)
 
 
-def compare_accept(tok, alen, ref_tok, ref_alen, margin, draw_margin):
+def compare_accept(tok, alen, ref_tok, ref_alen, margin, race_gap):
     """Rows must match bit-exactly unless the oracle marks them as a near tie.
 
     Returns (n_mismatch_unexcused, n_excused_rows)."""
     same = (np.asarray(tok) == ref_tok).all(1) & (np.asarray(alen) == ref_alen)
-    excused = (margin < NEAR_TIE) | (draw_margin < NEAR_TIE)
+    excused = (margin < NEAR_TIE) | (race_gap < NEAR_TIE)
     return int(np.sum(~same & ~excused)), int(np.sum(excused))

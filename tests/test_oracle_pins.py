@@ -369,26 +369,25 @@ def test_sampling_uniform_uses_documented_counter(oracle_mod):
         assert (alen[b] >= 1) == (u0 < 0.5)
 
 
-def test_final_draw_is_inverse_cdf_of_documented_uniform(oracle_mod):
-    """With every draft accepted (q = p), the bonus token is searchsorted(cumsum(p_k), u * sum)
-    with u from word 0 of Philox counter (0, k, b, 1)."""
+def test_final_draw_is_exponential_race_of_documented_uniforms(oracle_mod):
+    """With every draft accepted (q = p), the bonus token is argmax_x p_k(x) / E_x with
+    E_x = -ln U(word x mod 4 of Philox counter (x/4, k, b, 1))."""
     rng = np.random.default_rng(14)
-    B, k, V = 400, 2, 16
+    B, k, V = 200, 2, 16
     seed = 777
     L = np.zeros((B, k + 1, V), np.float32)
     L[:, k] = rng.normal(0, 1.5, (B, V)).astype(np.float32)
     Q = np.full((B, k, V), 1.0 / 16, np.float32)
     d = rng.integers(0, V, (B, k)).astype(np.int32)
-    tok, alen, _, draw_margin, _ = oracle_mod.accept(L, d, Q, seed, np.ones(B, np.int32), np.ones(B, np.float32))
+    tok, alen, _, gap, _ = oracle_mod.accept(L, d, Q, seed, np.ones(B, np.int32), np.ones(B, np.float32))
     assert np.all(alen == k)
     key = [seed & 0xFFFFFFFF, seed >> 32]
     for b in range(B):
         p = _softmax(L[b, k].astype(np.float64))
-        u = oracle_mod.uniform(oracle_mod.philox4x32_10([0, k, b, 1], key)[0])
-        c = np.cumsum(p)
-        want = int(np.searchsorted(c, u * c[-1], side="right"))
-        if draw_margin[b] > 1e-12:
-            assert tok[b, k] == want
+        words = np.concatenate([oracle_mod.philox4x32_10([x4, k, b, 1], key) for x4 in range(V // 4)])
+        e = -np.log(np.array([oracle_mod.uniform(int(w)) for w in words]))
+        if gap[b] > 1e-12:
+            assert tok[b, k] == int(np.argmax(p / e))
 
 
 def test_sampling_is_deterministic_per_seed(oracle_mod):
