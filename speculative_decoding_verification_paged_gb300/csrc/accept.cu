@@ -20,8 +20,10 @@
 // partial that every CTA of the cluster reads through distributed shared
 // memory, in rank order, so all CTAs reach bit-identical decisions without
 // any global-memory round trip. The correction / bonus token is an
-// exponential race over the slice already in shared memory, with Philox
-// uniforms generated on the fly.
+// exponential race over the slice already in shared memory: Philox uniforms
+// are generated on the fly (one block per 4 logits) and the draft
+// probabilities of the rejected position are loaded in batches, so the race
+// costs one memory latency per batch rather than per element.
 #include <math.h>
 
 #include "common.cuh"
@@ -259,6 +261,72 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
     Z = zz;
   };
 
+  // Exponential race over this row's slice at position `pos`: the token is
+  // argmax_x w(x) / E_x with E_x = -ln U_x, U_x from word (x mod 4) of Philox
+  // counter (x / 4, pos, b, 1). kind 0: w = max(0, p - q) with
+  // p = exp2((l - M) c2) * invZ; kind 1: w = p; kind 2: keys compared in log2
+  // units, l c2 - log2 E_x (no normaliser needed). Returns the winner (same in
+  // every CTA) and, in *total, the sum of the weights over the row (kinds 0, 1).
+  auto race = [&](int kind, float M, float invZ, const float* qrow, int pos, int slot, float* total) -> int {
+    constexpr int kBatch = 8;  // float4 groups whose draft probabilities are loaded together
+    float best = kind == 2 ? -INFINITY : -1.f, wsum = 0.f;
+    int bidx = INT32_MAX;
+    for (int base = tid; base * 4 < n; base += kThreads * kBatch) {
+      float qv[kBatch][4];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int g4 = base + i * kThreads;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qv[i][e] = 0.f;
+        if (kind == 0 && g4 * 4 < n) {
+          if (vec) {
+            const float4 q4 = __ldg(reinterpret_cast<const float4*>(qrow) + g4);
+            qv[i][0] = q4.x; qv[i][1] = q4.y; qv[i][2] = q4.z; qv[i][3] = q4.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qv[i][e] = (g4 * 4 + e < n) ? qrow[g4 * 4 + e] : 0.f;
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int g4 = base + i * kThreads;
+        if (g4 * 4 >= n) break;
+        const Philox4 w = philox4x32_10((uint32_t)((x0 >> 2) + g4), (uint32_t)pos, (uint32_t)b, 1u, p.seed_lo,
+                                        p.seed_hi);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int x = g4 * 4 + e;
+          if (x < n) {
+            // accurate log: the winner's U is often close to 1, where E is small
+            const float E = -logf(word_to_uniform(w.v[e]));
+            if (kind == 2) {
+              const float key = buf[x] * c2 - log2f(E);
+              if (key > best) { best = key; bidx = x0 + x; }
+            } else {
+              const float px = fast_exp2((buf[x] - M) * c2) * invZ;
+              const float wt = kind == 0 ? fmaxf(px - qv[i][e], 0.f) : px;
+              wsum += wt;
+              if (wt > 0.f) {
+                const float key = __fdividef(wt, E);
+                if (key > best) { best = key; bidx = x0 + x; }
+              }
+            }
+          }
+        }
+      }
+    }
+    block_argmax(sh, best, bidx);
+    if (kind != 2) wsum = block_sum(sh, wsum);
+    if (tid == 0) sh.race[slot] = Part{best, wsum, bidx, 0};
+    cluster_sync_all();
+    float bv, tot;
+    int bi;
+    cluster_best(sh_race + slot * sizeof(Part), bv, bi, &tot);
+    if (total) *total = tot;
+    return bi;
+  };
+
   int m = k;
   int token = -1;
   issue_row(0);
@@ -286,31 +354,9 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       break;
     }
     if (j == k) {
-      // ---- every draft accepted: bonus token from p_k by exponential race,
-      // compared in log2 units (log2 p - log2 E) so no normaliser is needed.
-      float best = -INFINITY;
-      int bidx = INT32_MAX;
-      for (int g4 = tid; g4 * 4 < n; g4 += kThreads) {
-        const int gx = x0 + g4 * 4;
-        const Philox4 w = philox4x32_10((uint32_t)(gx >> 2), (uint32_t)k, (uint32_t)b, 1u, p.seed_lo, p.seed_hi);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int x = g4 * 4 + e;
-          if (x < n) {
-            const float E = -__logf(word_to_uniform(w.v[e]));
-            const float key = buf[x] * c2 - __log2f(E);
-            if (key > best) { best = key; bidx = x0 + x; }
-          }
-        }
-      }
-      block_argmax(sh, best, bidx);
-      if (tid == 0) sh.race[0] = Part{best, 0.f, bidx, 0};
-      cluster_sync_all();
-      float bv;
-      int bi;
-      cluster_best(sh_race, bv, bi, nullptr);
+      // ---- every draft accepted: bonus token from p_k, raced in log2 units
       m = k;
-      token = bi;
+      token = race(2, 0.f, 1.f, nullptr, k, 0, nullptr);
       break;
     }
     // ---- sampling statistics of p_j = softmax(l / T): slice max, then sum of exp
@@ -332,49 +378,13 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       issue_row(j + 1);
       continue;
     }
-    // ---- rejected at j: race over max(0, p_j - q_j) (falls back to p_j if all zero)
+    // ---- rejected at j: race over max(0, p_j - q_j), or over p_j if that is all zero
     m = j;
     const float invZ = 1.f / Z;
     const float* qrow = p.probs + ((int64_t)b * k + j) * V + x0;
-    for (int pass = 0; pass < 2; ++pass) {
-      float best = -1.f, wsum = 0.f;
-      int bidx = INT32_MAX;
-      for (int g4 = tid; g4 * 4 < n; g4 += kThreads) {
-        const int gx = x0 + g4 * 4;
-        float qv[4];
-        if (vec && g4 * 4 + 3 < n) {
-          const float4 q4 = __ldg(reinterpret_cast<const float4*>(qrow + g4 * 4));
-          qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) qv[e] = (g4 * 4 + e < n) ? qrow[g4 * 4 + e] : 0.f;
-        }
-        const Philox4 w = philox4x32_10((uint32_t)(gx >> 2), (uint32_t)j, (uint32_t)b, 1u, p.seed_lo, p.seed_hi);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int x = g4 * 4 + e;
-          if (x < n) {
-            const float px = fast_exp2((buf[x] - M) * c2) * invZ;
-            const float wt = pass == 0 ? fmaxf(px - qv[e], 0.f) : px;
-            wsum += wt;
-            if (wt > 0.f) {
-              const float E = -__logf(word_to_uniform(w.v[e]));
-              const float key = __fdividef(wt, E);
-              if (key > best) { best = key; bidx = x0 + x; }
-            }
-          }
-        }
-      }
-      block_argmax(sh, best, bidx);
-      wsum = block_sum(sh, wsum);
-      if (tid == 0) sh.race[pass] = Part{best, wsum, bidx, 0};
-      cluster_sync_all();
-      float bv, total;
-      int bi;
-      cluster_best(sh_race + pass * sizeof(Part), bv, bi, &total);
-      token = bi;
-      if (total > 0.f) break;  // identical in every CTA: the same partials, the same order
-    }
+    float total = 0.f;
+    token = race(0, M, invZ, qrow, j, 0, &total);
+    if (!(total > 0.f)) token = race(1, M, invZ, nullptr, j, 1, nullptr);  // same in every CTA
     break;
   }
 
