@@ -57,6 +57,8 @@ typedef struct CUstream_st* spec_stream_t;
 #define SPEC_ERR_UNSUPPORTED (-2)   /* a shape this build has no kernel for    */
 #define SPEC_ERR_LAUNCH (-3)        /* cudaLaunch* failed (see cudaGetLastError) */
 #define SPEC_ERR_WORKSPACE (-4)     /* workspace missing or smaller than asked  */
+#define SPEC_ERR_SCRATCH_LIMIT (-5) /* shape needs more than the fixed scratch of
+                                       spec_verify_attention_noalloc           */
 
 /* Bits OR-ed into *dev_err by the kernels. */
 #define SPEC_DEVERR_BLOCK_ID 1     /* block_table entry outside [0, num_blocks)  */
@@ -127,6 +129,38 @@ int spec_verify_attention(const void* q, const void* k_cache, const void* v_cach
                           int32_t k_draft, float* out, const spec_attn_desc* d,
                           void* workspace, size_t workspace_bytes, int32_t* dev_err,
                           spec_stream_t stream);
+
+/*
+ * Allocation-free form of spec_verify_attention (the pages have no
+ * counterpart; this is a convenience of this library).
+ *
+ * For callers that may not allocate device memory when they call in: a
+ * serving engine's per-step enqueue path that must not touch the allocator,
+ * a plugin hook of an inference runtime whose enqueue contract forbids
+ * allocation, or a process that reserved all device memory up front. It
+ * computes the same result as spec_verify_attention but takes no workspace:
+ * its scratch is a fixed array of spec_verify_attention_noalloc_limit() bytes
+ * (32 MiB) inside the library, which every GPU that loads the library holds
+ * until the process exits. It never calls cudaMalloc or cudaFree.
+ *
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array and leaves its contents behind; the call
+ *    clears the part that must start at zero (an asynchronous memset on
+ *    `stream`). Calls whose kernels overlap on the GPU (other streams, or
+ *    other host threads) race on the array: serialise them.
+ *  - A shape whose scratch would exceed the array returns
+ *    SPEC_ERR_SCRATCH_LIMIT before anything is launched.
+ * Arguments, layouts and device errors are those of spec_verify_attention.
+ */
+int spec_verify_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, const int32_t* ctx_lens,
+                                  int32_t k_draft, float* out, const spec_attn_desc* d,
+                                  int32_t* dev_err, spec_stream_t stream);
+
+/* Bytes of the fixed scratch array used by spec_verify_attention_noalloc. */
+size_t spec_verify_attention_noalloc_limit(void);
 
 /* ------------------------------------------------------------------------ */
 /* 2. Acceptance: greedy prefix match or speculative sampling                  */

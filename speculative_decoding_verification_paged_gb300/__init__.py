@@ -25,7 +25,8 @@ from . import buildlib as _build_mod
 
 __all__ = [
     "SpecError", "build", "library_path", "load_library", "spec_verify_attention",
-    "spec_verify_attention_workspace", "new_attention_workspace", "spec_accept", "spec_commit_state", "status_string",
+    "spec_verify_attention_workspace", "new_attention_workspace", "spec_verify_attention_noalloc",
+    "spec_accept", "spec_commit_state", "status_string",
     "DEVERR", "MODE_GREEDY", "MODE_SAMPLE",
 ]
 
@@ -85,6 +86,10 @@ def load_library():
         lib.spec_verify_attention_workspace.restype = sz
         lib.spec_verify_attention.argtypes = [P, P, P, P, P, i32, P, ctypes.POINTER(_AttnDesc), P, sz, P, P]
         lib.spec_verify_attention.restype = ctypes.c_int
+        lib.spec_verify_attention_noalloc.argtypes = [P, P, P, P, P, i32, P, ctypes.POINTER(_AttnDesc), P, P]
+        lib.spec_verify_attention_noalloc.restype = ctypes.c_int
+        lib.spec_verify_attention_noalloc_limit.argtypes = []
+        lib.spec_verify_attention_noalloc_limit.restype = sz
         lib.spec_accept.argtypes = [P, P, P, u64, P, P, P, P, i32, i32, i32, P, P]
         lib.spec_accept.restype = ctypes.c_int
         lib.spec_commit_state.argtypes = [P, P, P, i32, i32, i32, i64, P, P]
@@ -169,6 +174,31 @@ def spec_verify_attention(q, k_cache, v_cache, block_table, ctx_lens, k_draft: i
                                    int(k_draft), _ptr(out), ctypes.byref(d), _ptr(workspace),
                                    workspace.numel(), _ptr(dev_err), _stream_handle(stream))
     _check("spec_verify_attention", rc)
+    return out
+
+
+def spec_verify_attention_noalloc(q, k_cache, v_cache, block_table, ctx_lens, k_draft: int, out,
+                                  dev_err: Optional[torch.Tensor] = None,
+                                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """spec_verify_attention without a workspace argument, for callers that may not
+    allocate device memory at call time; its scratch is a fixed array inside the
+    library (see spec_verify.h for the limit and the rules on overlapping calls)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k_cache, "k_cache", torch.bfloat16, 4)
+    _need(v_cache, "v_cache", torch.bfloat16, 4)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1)
+    _need(out, "out", torch.float32, 4)
+    B, R, Hq, D = q.shape
+    if v_cache.shape != k_cache.shape or R != k_draft + 1 or out.shape != q.shape \
+            or block_table.shape[0] != B or ctx_lens.shape[0] != B:
+        raise ValueError("inconsistent verify-attention shapes")
+    d = _attn_desc(q, k_cache, block_table)
+    rc = lib.spec_verify_attention_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                           _ptr(ctx_lens), int(k_draft), _ptr(out), ctypes.byref(d),
+                                           _ptr(dev_err), _stream_handle(stream))
+    _check("spec_verify_attention_noalloc", rc)
     return out
 
 

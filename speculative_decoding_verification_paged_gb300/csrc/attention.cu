@@ -831,3 +831,137 @@ extern "C" int spec_verify_attention(const void* q, const void* k_cache, const v
     default: return attn::launch_main_d<256>(p, mt, tq, tk_map, tv_map, stream);
   }
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of spec_verify_attention.
+//
+// Some callers may not allocate device memory when they call us: a serving
+// engine's per-step enqueue path that must not touch the allocator, a plugin
+// hook of an inference runtime whose enqueue contract forbids allocation, or a
+// process that reserved all device memory up front. This entry point takes no
+// workspace: its scratch is the fixed array below, which every GPU that loads
+// the library keeps until the process exits.
+// ---------------------------------------------------------------------------
+namespace specv {
+namespace attn {
+
+constexpr size_t kNoAllocScratchBytes = 32u << 20;  // 32 MiB per device
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Persistent grid the launch will use (the same occupancy query as launch_main).
+template <int D, int MT>
+static int noalloc_grid(int batch, int* grid) {
+  auto kern = verify_attention_kernel<D, MT>;
+  const size_t smem = smem_bytes<D, MT>(batch);
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  if (per_sm < 1) return SPEC_ERR_UNSUPPORTED;
+  *grid = sms * per_sm > kMaxGrid ? kMaxGrid : sms * per_sm;
+  return SPEC_OK;
+}
+
+template <int D>
+static int noalloc_grid_d(int mt, int batch, int* grid) {
+  switch (mt) {
+    case 1: return noalloc_grid<D, 1>(batch, grid);
+    case 2: return noalloc_grid<D, 2>(batch, grid);
+    default: return noalloc_grid<D, 4>(batch, grid);
+  }
+}
+
+}  // namespace attn
+}  // namespace specv
+
+extern "C" size_t spec_verify_attention_noalloc_limit(void) { return attn::kNoAllocScratchBytes; }
+
+extern "C" int spec_verify_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                             const int32_t* block_table, const int32_t* ctx_lens, int32_t k_draft,
+                                             float* out, const spec_attn_desc* d, int32_t* dev_err,
+                                             spec_stream_t stream_) {
+  if (!attn::desc_ok(d, k_draft)) return SPEC_ERR_INVALID_ARG;
+  if (d->batch == 0) return SPEC_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !out) return SPEC_ERR_INVALID_ARG;
+  if (!attn::shape_supported(d, k_draft)) return SPEC_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out)) & 15)
+    return SPEC_ERR_INVALID_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  // Set-up, once per device, with that device current: the device address of
+  // the scratch array (host code cannot use the symbol itself).
+  static void* scratch_addr[attn::kNoAllocMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= attn::kNoAllocMaxDevices) return SPEC_ERR_LAUNCH;
+  if (scratch_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, attn::g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return SPEC_ERR_LAUNCH;
+    scratch_addr[dev] = ptr;
+  }
+
+  const int R = k_draft + 1, G = d->num_q_heads / d->num_kv_heads, D = d->head_dim;
+  const int bs = d->block_size;
+  const int mt = R * G <= 16 ? 1 : (R * G <= 32 ? 2 : 4);
+  int grid = 0, rc = SPEC_OK;
+  switch (D) {
+    case 64: rc = attn::noalloc_grid_d<64>(mt, d->batch, &grid); break;
+    case 128: rc = attn::noalloc_grid_d<128>(mt, d->batch, &grid); break;
+    default: rc = attn::noalloc_grid_d<256>(mt, d->batch, &grid); break;
+  }
+  if (rc != SPEC_OK) return rc;
+  // Scratch layout for this grid: arrival counters, then two partial slots per CTA.
+  const int64_t n_rows = (int64_t)R * G;
+  const int64_t slots = 2 * (int64_t)grid;
+  const size_t counters_bytes = attn::align256((size_t)d->batch * d->num_kv_heads * 4);
+  const size_t lse_off = counters_bytes;
+  const size_t opart_off = lse_off + attn::align256((size_t)(slots * n_rows * 4));
+  const size_t total = opart_off + attn::align256((size_t)(slots * n_rows * D * 4));
+  if (total > attn::kNoAllocScratchBytes) return SPEC_ERR_SCRATCH_LIMIT;
+
+  uint8_t* ws = static_cast<uint8_t*>(scratch_addr[dev]);
+  // The counters must start at zero; every call shares the array, so clear them here.
+  if (cudaMemsetAsync(ws, 0, counters_bytes, stream) != cudaSuccess) return SPEC_ERR_LAUNCH;
+
+  const int tk = attn::tile_keys(D, mt);
+  CUtensorMap tq, tk_map, tv_map;
+  if (!attn::make_map(&tq, q, D, d->num_q_heads, (uint64_t)d->batch * R, (uint32_t)G, (uint32_t)R) ||
+      !attn::make_map(&tk_map, k_cache, D, d->num_kv_heads, (uint64_t)d->num_blocks * bs, 1,
+                      (uint32_t)(bs < tk ? bs : tk)) ||
+      !attn::make_map(&tv_map, v_cache, D, d->num_kv_heads, (uint64_t)d->num_blocks * bs, 1,
+                      (uint32_t)(bs < tk ? bs : tk)))
+    return SPEC_ERR_LAUNCH;
+
+  attn::Params p;
+  p.block_table = block_table;
+  p.ctx_lens = ctx_lens;
+  p.out = out;
+  p.counters = reinterpret_cast<int32_t*>(ws);
+  p.lse = reinterpret_cast<float*>(ws + lse_off);
+  p.opart = reinterpret_cast<float*>(ws + opart_off);
+  p.dev_err = dev_err;
+  p.num_blocks = d->num_blocks;
+  p.batch = d->batch;
+  p.rows_per_seq = R;
+  p.num_q_heads = d->num_q_heads;
+  p.num_kv_heads = d->num_kv_heads;
+  p.gqa = G;
+  p.n_rows = R * G;
+  int shift = 0;
+  while ((1 << shift) < bs) ++shift;
+  p.block_shift = shift;
+  p.max_blocks = d->max_blocks_per_seq;
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
+
+  switch (D) {
+    case 64: return attn::launch_main_d<64>(p, mt, tq, tk_map, tv_map, stream);
+    case 128: return attn::launch_main_d<128>(p, mt, tq, tk_map, tv_map, stream);
+    default: return attn::launch_main_d<256>(p, mt, tq, tk_map, tv_map, stream);
+  }
+}

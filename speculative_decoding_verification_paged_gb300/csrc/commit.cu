@@ -107,6 +107,7 @@ extern "C" const char* spec_status_string(int status) {
     case SPEC_ERR_UNSUPPORTED: return "unsupported shape";
     case SPEC_ERR_LAUNCH: return "kernel launch failed";
     case SPEC_ERR_WORKSPACE: return "workspace missing or too small";
+    case SPEC_ERR_SCRATCH_LIMIT: return "shape needs more than the fixed scratch of the allocation-free call";
     default: return "unknown status";
   }
 }
