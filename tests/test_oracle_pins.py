@@ -325,6 +325,25 @@ def test_sampling_bonus_token_follows_last_target_row(oracle_mod):
     assert _chi2_ok(tok[:, k], _softmax(lk.astype(np.float64))) > 1e-3
 
 
+def test_race_across_groups_and_chunks_follows_target(oracle_mod):
+    """The bonus token follows p_k when its mass spans several 8192-entry groups and chunks."""
+    B, k, V = 20000, 1, 20000
+    support = np.array([5, 4100, 8191, 8192, 12000, 19999])
+    lk = np.full(V, -1e30, np.float32)
+    lk[support] = np.array([0.0, 0.5, -0.3, 1.0, 0.2, -1.0], np.float32)
+    L = np.zeros((B, k + 1, V), np.float32)
+    L[:, k] = lk
+    d = np.full((B, k), 7, np.int32)
+    Q = np.zeros((B, k, V), np.float32)
+    Q[:, 0, 7] = 1e-30  # u q < p always: the draft is kept, the bonus is raced
+    tok, alen, _, _, _ = oracle_mod.accept(L, d, Q, 4242, np.ones(B, np.int32), np.ones(B, np.float32))
+    assert np.all(alen == k)
+    p = _softmax(lk[support].astype(np.float64))
+    idx = np.searchsorted(support, tok[:, k])
+    assert np.all(support[idx] == tok[:, k])
+    assert _chi2_ok(idx, p) > 1e-3
+
+
 def test_sampling_zero_target_probability_always_rejects(oracle_mod):
     B, k, V = 1000, 3, 10
     L = np.zeros((B, k + 1, V), np.float32)
@@ -369,25 +388,45 @@ def test_sampling_uniform_uses_documented_counter(oracle_mod):
         assert (alen[b] >= 1) == (u0 < 0.5)
 
 
-def test_final_draw_is_exponential_race_of_documented_uniforms(oracle_mod):
-    """With every draft accepted (q = p), the bonus token is argmax_x p_k(x) / E_x with
-    E_x = -ln U(word x mod 4 of Philox counter (x/4, k, b, 1))."""
+@pytest.mark.parametrize("V", [16, 20000])
+def test_final_draw_follows_documented_three_level_race(oracle_mod, V):
+    """With every draft accepted (q = p) the bonus token comes from the documented race:
+    8192-entry groups raced by their sums (Philox counter (g/4, k, b, 2)), then the group's
+    256 chunks {8192g + 1024i + 4c + e} by their sums (counter ((256g+c)/4, k, b, 3)), then
+    the chunk's entries (counter (x/4, k, b, 1)); keys weight / (-ln U), argmax via numpy."""
     rng = np.random.default_rng(14)
-    B, k, V = 200, 2, 16
+    B, k = 24, 2
     seed = 777
     L = np.zeros((B, k + 1, V), np.float32)
     L[:, k] = rng.normal(0, 1.5, (B, V)).astype(np.float32)
-    Q = np.full((B, k, V), 1.0 / 16, np.float32)
+    Q = np.full((B, k, V), 1.0 / V, np.float32)
+    L[:, :k] = 0.0
     d = rng.integers(0, V, (B, k)).astype(np.int32)
+    if V & (V - 1):  # q = 1/V exactly only for powers of two: accept by construction instead
+        Q[:] = 0.0
+        Q[np.arange(B)[:, None], np.arange(k)[None, :], d] = 1e-30
     tok, alen, _, gap, _ = oracle_mod.accept(L, d, Q, seed, np.ones(B, np.int32), np.ones(B, np.float32))
     assert np.all(alen == k)
     key = [seed & 0xFFFFFFFF, seed >> 32]
+
+    def e_of(index, level, b):
+        w = oracle_mod.philox4x32_10([index // 4, k, b, level], key)[index % 4]
+        return -np.log(oracle_mod.uniform(int(w)))
+
+    x_all = np.arange(V)
+    chunk = ((x_all % 8192) % 1024) // 4
     for b in range(B):
+        if gap[b] < 1e-9:
+            continue
         p = _softmax(L[b, k].astype(np.float64))
-        words = np.concatenate([oracle_mod.philox4x32_10([x4, k, b, 1], key) for x4 in range(V // 4)])
-        e = -np.log(np.array([oracle_mod.uniform(int(w)) for w in words]))
-        if gap[b] > 1e-12:
-            assert tok[b, k] == int(np.argmax(p / e))
+        groups = [p[g * 8192:(g + 1) * 8192].sum() for g in range((V + 8191) // 8192)]
+        g = int(np.argmax([w / e_of(i, 2, b) for i, w in enumerate(groups)]))
+        in_g = (x_all // 8192) == g
+        sums = np.array([p[in_g & (chunk == c)].sum() for c in range(256)])
+        c = int(np.argmax([w / e_of(256 * g + i, 3, b) if w > 0 else 0.0 for i, w in enumerate(sums)]))
+        xs = x_all[in_g & (chunk == c)]
+        want = int(xs[np.argmax([p[x] / e_of(int(x), 1, b) for x in xs])])
+        assert tok[b, k] == want
 
 
 def test_sampling_is_deterministic_per_seed(oracle_mod):
