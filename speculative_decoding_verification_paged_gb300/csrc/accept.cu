@@ -19,11 +19,13 @@
 // reduces it (max / sum of exp / argmax) with warp shuffles, and publishes a
 // partial that every CTA of the cluster reads through distributed shared
 // memory, in rank order, so all CTAs reach bit-identical decisions without
-// any global-memory round trip. The correction / bonus token is an
-// exponential race over the slice already in shared memory: Philox uniforms
-// are generated on the fly (one block per 4 logits) and the draft
-// probabilities of the rejected position are loaded in batches, so the race
-// costs one memory latency per batch rather than per element.
+// any global-memory round trip. The correction / bonus token is a three-level
+// exponential race (groups of 8192 logits, their 256 chunks of 32, then the
+// chunk's logits): every CTA sums the weights of its groups and chunks in one
+// pass over the slice already in shared memory, all CTAs race the groups from
+// the published sums, and only the CTA holding the winning group races its
+// chunks and the winning chunk's entries, so Philox and logarithms are needed
+// for ~300 candidates per draw instead of one per logit.
 #include <math.h>
 
 #include "common.cuh"
@@ -34,8 +36,9 @@ namespace acc {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 16;
-constexpr int kSliceTarget = 8192;   // logits per CTA (32 KB of shared memory)
-constexpr int kMaxSlice = 48 * 1024;
+constexpr int kGroup = 8192;         // logits per race group; a CTA's slice is whole groups
+constexpr int kChunks = 256;         // chunks per group (one per thread)
+constexpr int kMaxGroupsPerCta = 6;  // slice <= 48K logits (192 KB of shared memory)
 constexpr int kMaxK = 31;
 
 struct Params {
@@ -48,7 +51,7 @@ struct Params {
   int32_t* accept_len;
   int32_t* dev_err;
   uint32_t seed_lo, seed_hi;
-  int batch, k, vocab, slice, csize;
+  int batch, k, vocab, slice, csize, gpc;  // gpc: race groups per CTA (slice = gpc * kGroup)
   int bulk;      // 1: rows are 16-byte aligned, use bulk copies
   int prefetch;  // 1: prefetch the next position's slice into L2
 };
@@ -63,7 +66,9 @@ struct __align__(16) Part {
 
 struct Shared {
   Part pos[kMaxK + 1];
-  Part race[2];
+  Part race[2];                              // winning token of each race (owner CTA)
+  float group_w[2][kMaxGroupsPerCta];        // this CTA's group weight sums, per race
+  float chunk_w[kMaxGroupsPerCta * kChunks];  // this CTA's chunk weight sums (current race)
   float wf[kWarps];
   float wg[kWarps];
   int32_t wi[kWarps];
@@ -261,70 +266,125 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
     Z = zz;
   };
 
-  // Exponential race over this row's slice at position `pos`: the token is
-  // argmax_x w(x) / E_x with E_x = -ln U_x, U_x from word (x mod 4) of Philox
-  // counter (x / 4, pos, b, 1). kind 0: w = max(0, p - q) with
-  // p = exp2((l - M) c2) * invZ; kind 1: w = p; kind 2: keys compared in log2
-  // units, l c2 - log2 E_x (no normaliser needed). Returns the winner (same in
-  // every CTA) and, in *total, the sum of the weights over the row (kinds 0, 1).
-  auto race = [&](int kind, float M, float invZ, const float* qrow, int pos, int slot, float* total) -> int {
-    constexpr int kBatch = 8;  // float4 groups whose draft probabilities are loaded together
-    float best = kind == 2 ? -INFINITY : -1.f, wsum = 0.f;
-    int bidx = INT32_MAX;
-    for (int base = tid; base * 4 < n; base += kThreads * kBatch) {
-      float qv[kBatch][4];
+  // Three-level exponential race over this row's weights at position `pos`
+  // (an exact sampler of w / sum(w)): group g (8192 consecutive logits) wins
+  // with key W_g / E, E = -ln U from word g%4 of Philox counter (g/4, pos, b, 2);
+  // in that group chunk c = {8192g + 1024i + 4c + e} wins with key S_c / E from
+  // counter ((256g+c)/4, pos, b, 3); in that chunk entry x wins with w_x / E
+  // from counter (x/4, pos, b, 1). Ties go to the lowest index. Weights:
+  // residual max(0, p - q) with p = exp2((l - M) c2) * invZ, or p itself.
+  // Returns the token (valid in rank 0) or -1 in every CTA if all weights are 0.
+  auto race = [&](bool residual, float M, float invZ, const float* qrow, int pos, int slot) -> int {
+    auto weight = [&](int x, float qx) {
+      const float px = fast_exp2((buf[x] - M) * c2) * invZ;
+      return residual ? fmaxf(px - qx, 0.f) : px;
+    };
+    // ---- pass over the slice: chunk sums (thread t owns chunk t of each group), group sums
+    for (int gl = 0; gl < p.gpc; ++gl) {
+      const int gbase = gl * kGroup;
+      float qv[8][4];
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int g4 = base + i * kThreads;
+      for (int i = 0; i < 8; ++i) {
+        const int off = gbase + 1024 * i + 4 * tid;
 #pragma unroll
         for (int e = 0; e < 4; ++e) qv[i][e] = 0.f;
-        if (kind == 0 && g4 * 4 < n) {
+        if (residual && off < n) {
           if (vec) {
-            const float4 q4 = __ldg(reinterpret_cast<const float4*>(qrow) + g4);
+            const float4 q4 = __ldg(reinterpret_cast<const float4*>(qrow + off));
             qv[i][0] = q4.x; qv[i][1] = q4.y; qv[i][2] = q4.z; qv[i][3] = q4.w;
           } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) qv[i][e] = (g4 * 4 + e < n) ? qrow[g4 * 4 + e] : 0.f;
+            for (int e = 0; e < 4; ++e) qv[i][e] = (off + e < n) ? qrow[off + e] : 0.f;
           }
         }
       }
+      float cs = 0.f;
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int g4 = base + i * kThreads;
-        if (g4 * 4 >= n) break;
-        const Philox4 w = philox4x32_10((uint32_t)((x0 >> 2) + g4), (uint32_t)pos, (uint32_t)b, 1u, p.seed_lo,
-                                        p.seed_hi);
+      for (int i = 0; i < 8; ++i) {
+        const int off = gbase + 1024 * i + 4 * tid;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int x = g4 * 4 + e;
-          if (x < n) {
-            // accurate log: the winner's U is often close to 1, where E is small
-            const float E = -logf(word_to_uniform(w.v[e]));
-            if (kind == 2) {
-              const float key = buf[x] * c2 - log2f(E);
-              if (key > best) { best = key; bidx = x0 + x; }
-            } else {
-              const float px = fast_exp2((buf[x] - M) * c2) * invZ;
-              const float wt = kind == 0 ? fmaxf(px - qv[i][e], 0.f) : px;
-              wsum += wt;
-              if (wt > 0.f) {
-                const float key = __fdividef(wt, E);
-                if (key > best) { best = key; bidx = x0 + x; }
+        for (int e = 0; e < 4; ++e)
+          if (off + e < n) cs += weight(off + e, qv[i][e]);
+      }
+      sh.chunk_w[gl * kChunks + tid] = cs;
+      const float gsum = block_sum(sh, cs);
+      if (tid == 0) sh.group_w[slot][gl] = gsum;
+    }
+    cluster_sync_all();
+    // ---- level 1, the same in every CTA: race the groups from the published sums
+    const int n_groups = (V + kGroup - 1) / kGroup;
+    float gbest = -1.f, total = 0.f;
+    int gwin = INT32_MAX;
+    for (int gi = lane; gi < ((n_groups + 31) & ~31); gi += 32) {
+      float wg = 0.f;
+      if (gi < n_groups) {
+        const int r = gi / p.gpc, gl = gi - r * p.gpc;
+        wg = ld_cluster_f32(map_to_rank(smem_u32(&sh.group_w[slot][gl]), (uint32_t)r));
+      }
+      float key = 0.f;
+      if (wg > 0.f) {
+        const Philox4 w = philox4x32_10((uint32_t)gi >> 2, (uint32_t)pos, (uint32_t)b, 2u, p.seed_lo, p.seed_hi);
+        key = wg / -logf(word_to_uniform(w.v[gi & 3]));
+      }
+      float kk = key, tt = wg;
+      int ii = gi < n_groups ? gi : INT32_MAX;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ok = __shfl_xor_sync(0xffffffffu, kk, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, ii, o);
+        tt += __shfl_xor_sync(0xffffffffu, tt, o);
+        if (ok > kk || (ok == kk && oi < ii)) { kk = ok; ii = oi; }
+      }
+      total += tt;
+      if (kk > gbest || (kk == gbest && ii < gwin)) { gbest = kk; gwin = ii; }
+    }
+    if (!(total > 0.f)) return -1;  // the same in every CTA
+    const int owner = gwin / p.gpc, glw = gwin - owner * p.gpc;
+    if (rank == owner) {
+      // ---- level 2: race the winning group's chunks
+      const float sc = sh.chunk_w[glw * kChunks + tid];
+      float key = 0.f;
+      if (sc > 0.f) {
+        const uint32_t ci = (uint32_t)(gwin * kChunks + tid);
+        const Philox4 w = philox4x32_10(ci >> 2, (uint32_t)pos, (uint32_t)b, 3u, p.seed_lo, p.seed_hi);
+        key = sc / -logf(word_to_uniform(w.v[ci & 3]));
+      }
+      int cwin = tid;
+      block_argmax(sh, key, cwin);
+      // ---- level 3: race the winning chunk's 32 entries (warp 0, lane i: entries 1024 i + 4c + e)
+      if (tid < 32) {
+        float best = -1.f;
+        int bx = INT32_MAX;
+        if (tid < 8) {
+          const int off = glw * kGroup + 1024 * tid + 4 * cwin;
+          if (off < n) {
+            const Philox4 w = philox4x32_10((uint32_t)((x0 + off) >> 2), (uint32_t)pos, (uint32_t)b, 1u, p.seed_lo,
+                                            p.seed_hi);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (off + e < n) {
+                const float wt = weight(off + e, residual ? qrow[off + e] : 0.f);
+                if (wt > 0.f) {
+                  const float kx = wt / -logf(word_to_uniform(w.v[e]));
+                  if (kx > best) { best = kx; bx = x0 + off + e; }
+                }
               }
             }
           }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bx, o);
+          if (ov > best || (ov == best && oi < bx)) { best = ov; bx = oi; }
+        }
+        if (tid == 0) sh.race[slot] = Part{best, 0.f, bx, 0};
       }
     }
-    block_argmax(sh, best, bidx);
-    if (kind != 2) wsum = block_sum(sh, wsum);
-    if (tid == 0) sh.race[slot] = Part{best, wsum, bidx, 0};
     cluster_sync_all();
-    float bv, tot;
-    int bi;
-    cluster_best(sh_race + slot * sizeof(Part), bv, bi, &tot);
-    if (total) *total = tot;
-    return bi;
+    int tok = 0;
+    if (rank == 0) tok = ld_cluster_s32(map_to_rank(sh_race + slot * sizeof(Part), (uint32_t)owner) + 8);
+    return tok;
   };
 
   int m = k;
@@ -354,9 +414,16 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       break;
     }
     if (j == k) {
-      // ---- every draft accepted: bonus token from p_k, raced in log2 units
+      // ---- every draft accepted: bonus token from p_k, weights exp((l - max)/T)
+      float mx = -INFINITY;
+      for_slice(buf, n, vec, [&](int, float l) { mx = fmaxf(mx, l); });
+      mx = block_max(sh, mx);
+      if (tid == 0) sh.pos[j] = Part{mx, 0.f, 0, 0};
+      cluster_sync_all();
+      float M, Zunused;
+      cluster_stats(sh_pos + j * sizeof(Part), M, Zunused);
       m = k;
-      token = race(2, 0.f, 1.f, nullptr, k, 0, nullptr);
+      token = race(false, M, 1.f, nullptr, k, 0);
       break;
     }
     // ---- sampling statistics of p_j = softmax(l / T): slice max, then sum of exp
@@ -382,9 +449,8 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
     m = j;
     const float invZ = 1.f / Z;
     const float* qrow = p.probs + ((int64_t)b * k + j) * V + x0;
-    float total = 0.f;
-    token = race(0, M, invZ, qrow, j, 0, &total);
-    if (!(total > 0.f)) token = race(1, M, invZ, nullptr, j, 1, nullptr);  // same in every CTA
+    token = race(true, M, invZ, qrow, j, 0);
+    if (token < 0) token = race(false, M, invZ, nullptr, j, 1);  // all-zero residual: the same in every CTA
     break;
   }
 
@@ -401,13 +467,14 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
   cluster_sync_all();  // peers may still be reading this CTA's partials
 }
 
-static int pick_cluster(int vocab, int& slice) {
-  int c = (vocab + kSliceTarget - 1) / kSliceTarget;
-  if (c < 1) c = 1;
-  if (c > kMaxCluster) c = kMaxCluster;
-  slice = (vocab + c - 1) / c;
-  slice = (slice + 3) & ~3;
-  c = (vocab + slice - 1) / slice;  // every CTA owns at least one logit
+// Cluster size and slice: the slice is a whole number of race groups, at most
+// 16 CTAs per cluster (the limit on one GPC), at most kMaxGroupsPerCta groups each.
+static int pick_cluster(int vocab, int max_csize, int& slice, int& gpc) {
+  const int n_groups = (vocab + kGroup - 1) / kGroup;
+  int c = n_groups < max_csize ? n_groups : max_csize;
+  gpc = (n_groups + c - 1) / c;
+  c = (n_groups + gpc - 1) / gpc;  // every CTA owns at least one logit
+  slice = gpc * kGroup;
   return c;
 }
 
@@ -425,9 +492,9 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
   if (!target_logits || !draft_tokens || !mode || !temperature || !out_tokens || !accept_len)
     return SPEC_ERR_INVALID_ARG;
   if (k_draft > acc::kMaxK) return SPEC_ERR_UNSUPPORTED;
-  int slice = 0;
-  const int csize = acc::pick_cluster(vocab, slice);
-  if (slice > acc::kMaxSlice) return SPEC_ERR_UNSUPPORTED;
+  int slice = 0, gpc = 0;
+  const int csize = acc::pick_cluster(vocab, acc::kMaxCluster, slice, gpc);
+  if (gpc > acc::kMaxGroupsPerCta) return SPEC_ERR_UNSUPPORTED;
   if ((int64_t)batch * csize > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
@@ -447,6 +514,7 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
   p.vocab = vocab;
   p.slice = slice;
   p.csize = csize;
+  p.gpc = gpc;
   const bool aligned = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(target_logits) & 15) == 0) &&
                        (draft_probs == nullptr || (reinterpret_cast<uintptr_t>(draft_probs) & 15) == 0);
   p.bulk = aligned ? 1 : 0;
@@ -459,12 +527,13 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
   // Function attributes and the cluster-size probe depend only on (device, slice):
   // remember the last answer so steady-state calls make no extra runtime queries.
-  static int cached_dev = -1, cached_vocab = -1, cached_csize = 0, cached_slice = 0;
+  static int cached_dev = -1, cached_vocab = -1, cached_csize = 0, cached_slice = 0, cached_gpc = 0;
   static size_t cached_smem = 0;
   const bool cached = dev == cached_dev && vocab == cached_vocab;
   if (cached) {
     p.csize = cached_csize;
     p.slice = cached_slice;
+    p.gpc = cached_gpc;
   }
   // Clusters larger than 8 CTAs are not guaranteed to fit a GPC; if the device
   // cannot hold one, use 8 CTAs with larger slices.
@@ -492,15 +561,15 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0) break;
     (void)cudaGetLastError();
-    p.csize = 8;
-    p.slice = (((vocab + 7) / 8) + 3) & ~3;
-    if (p.slice > acc::kMaxSlice) return SPEC_ERR_UNSUPPORTED;
+    p.csize = acc::pick_cluster(vocab, 8, p.slice, p.gpc);
+    if (p.gpc > acc::kMaxGroupsPerCta) return SPEC_ERR_UNSUPPORTED;
   }
   if (!cached) {
     cached_dev = dev;
     cached_vocab = vocab;
     cached_csize = p.csize;
     cached_slice = p.slice;
+    cached_gpc = p.gpc;
   }
   if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return SPEC_ERR_LAUNCH;
   return SPEC_OK;
