@@ -65,10 +65,12 @@ struct __align__(16) Part {
 };
 
 struct Shared {
-  Part pos[kMaxK + 1];
-  Part race[2];                              // winning token of each race (owner CTA)
-  float group_w[2][kMaxGroupsPerCta];        // this CTA's group weight sums, per race
-  float chunk_w[kMaxGroupsPerCta * kChunks];  // this CTA's chunk weight sums (current race)
+  // Cluster exchange, push model: each CTA writes its partials into slot
+  // [its rank] of every peer before a cluster barrier, so everything read after
+  // the barrier is local and no CTA touches another's memory after its last one.
+  Part pos[kMaxK + 1][kMaxCluster];                   // per position: (max, sum) or (max, argmax)
+  float group_w[2][kMaxCluster * kMaxGroupsPerCta];   // per race: weight sum of every group
+  float chunk_w[kMaxGroupsPerCta * kChunks];          // this CTA's chunk weight sums (current race)
   float wf[kWarps];
   float wg[kWarps];
   int32_t wi[kWarps];
@@ -140,7 +142,7 @@ __device__ __forceinline__ void for_slice(const float* buf, int n, bool vec, F f
   }
 }
 
-__global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
   extern __shared__ __align__(128) float buf[];
   __shared__ Shared sh;
   const int tid = threadIdx.x;
@@ -175,8 +177,7 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
   }
   const bool greedy = md == SPEC_MODE_GREEDY;
   const float c2 = (1.0f / T) * 1.4426950408889634f;  // logit -> log2 units of p
-  const uint32_t sh_pos = smem_u32(&sh.pos[0]);
-  const uint32_t sh_race = smem_u32(&sh.race[0]);
+  const int lane = tid & 31;
   bool bulk = p.bulk != 0;
   const bool vec = bulk;  // 16-byte aligned slices
 
@@ -224,46 +225,53 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
     }
     __syncthreads();
   };
-  // (best value, lowest index) over the ranks' published partials. Lane r of every
-  // warp reads rank r's partial (the DSMEM loads overlap) and the warp reduces
-  // them with shuffles in a fixed tree, so every CTA gets a bit-identical result.
-  const int lane = tid & 31;
-  auto cluster_best = [&](uint32_t local, float& bv, int& bi, float* sum) {
-    float v = -INFINITY, acc = 0.f;
+  // Push this CTA's partial for position j into slot [rank] of every peer, then
+  // wait for all of the cluster's partials (all reads after this are local).
+  auto exchange = [&](int j, Part v) {
+    if (tid < csize) st_cluster_v4(map_to_rank(smem_u32(&sh.pos[j][rank]), (uint32_t)tid), v.f0, v.f1, v.i0, 0);
+    cluster_sync_all();
+  };
+  // (best value, lowest index) over the cluster's partials of position j, by a
+  // fixed shuffle tree, so every CTA gets a bit-identical result.
+  auto cluster_best = [&](int j, float& bv, int& bi) {
+    float v = -INFINITY;
     int i = INT32_MAX;
     if (lane < csize) {
-      const uint32_t a = map_to_rank(local, (uint32_t)lane);
-      v = ld_cluster_f32(a);
-      i = ld_cluster_s32(a + 8);
-      acc = ld_cluster_f32(a + 4);
+      v = sh.pos[j][lane].f0;
+      i = sh.pos[j][lane].i0;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, v, o);
       const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-      acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
     }
     bv = v;
     bi = i;
-    if (sum) *sum = acc;
   };
-  // Softmax statistics of the whole row from the ranks' (slice max, slice sum) pairs.
-  auto cluster_stats = [&](uint32_t local, float& M, float& Z) {
+  // Softmax statistics of the whole row from the cluster's (slice max, slice sum) pairs.
+  auto cluster_stats = [&](int j, float& M, float& Z) {
     float mr = -INFINITY, zr = 0.f;
     if (lane < csize) {
-      const uint32_t a = map_to_rank(local, (uint32_t)lane);
-      mr = ld_cluster_f32(a);
-      zr = ld_cluster_f32(a + 4);
+      mr = sh.pos[j][lane].f0;
+      zr = sh.pos[j][lane].f1;
     }
     float mm = mr;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-    float zz = lane < csize ? zr * fast_exp2((mr - mm) * c2) : 0.f;
+    float zz = (lane < csize && mr != -INFINITY) ? zr * fast_exp2((mr - mm) * c2) : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
     M = mm;
     Z = zz;
+  };
+  // Write the row's result: accepted drafts, the final token, -1 padding.
+  auto write_row = [&](int m, int token) {
+    int32_t* o = p.out_tokens + (int64_t)b * R;
+    for (int j = 0; j < m; ++j) o[j] = d[j];
+    o[m] = token;
+    for (int j = m + 1; j < R; ++j) o[j] = -1;
+    p.accept_len[b] = m;
   };
 
   // Three-level exponential race over this row's weights at position `pos`
@@ -271,15 +279,15 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
   // with key W_g / E, E = -ln U from word g%4 of Philox counter (g/4, pos, b, 2);
   // in that group chunk c = {8192g + 1024i + 4c + e} wins with key S_c / E from
   // counter ((256g+c)/4, pos, b, 3); in that chunk entry x wins with w_x / E
-  // from counter (x/4, pos, b, 1). Ties go to the lowest index. Weights:
-  // residual max(0, p - q) with p = exp2((l - M) c2) * invZ, or p itself.
-  // Returns the token (valid in rank 0) or -1 in every CTA if all weights are 0.
-  auto race = [&](bool residual, float M, float invZ, const float* qrow, int pos, int slot) -> int {
-    auto weight = [&](int x, float qx) {
-      const float px = fast_exp2((buf[x] - M) * c2) * invZ;
-      return residual ? fmaxf(px - qx, 0.f) : px;
-    };
-    // ---- pass over the slice: chunk sums (thread t owns chunk t of each group), group sums
+  // from counter (x/4, pos, b, 1). Ties go to the lowest index.
+  // Weights, written over the slice in place as they are computed:
+  //   residual: buf holds e_x = exp2((l - m) c2) from the statistics pass and
+  //             w = max(0, e_x * f - q_x) with f = exp2((m - M) c2) / Z;
+  //   plain:    buf holds logits and w = exp2((l - M) c2).
+  // The CTA holding the winning group writes the output row (accept length m).
+  // Returns false in every CTA if all weights are 0 (nothing written).
+  auto race = [&](bool residual, float M, float f, const float* qrow, int pos, int slot, int m) -> bool {
+    // ---- pass over the slice: weights (in place), chunk sums (thread t owns chunk t of each group), group sums
     for (int gl = 0; gl < p.gpc; ++gl) {
       const int gbase = gl * kGroup;
       float qv[8][4];
@@ -303,24 +311,28 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       for (int i = 0; i < 8; ++i) {
         const int off = gbase + 1024 * i + 4 * tid;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (off + e < n) cs += weight(off + e, qv[i][e]);
+        for (int e = 0; e < 4; ++e) {
+          if (off + e < n) {
+            const float v = buf[off + e];
+            const float wt = residual ? fmaxf(v * f - qv[i][e], 0.f) : fast_exp2((v - M) * c2);
+            buf[off + e] = wt;
+            cs += wt;
+          }
+        }
       }
       sh.chunk_w[gl * kChunks + tid] = cs;
       const float gsum = block_sum(sh, cs);
-      if (tid == 0) sh.group_w[slot][gl] = gsum;
+      // push this group's sum to every CTA of the cluster
+      if (tid < csize)
+        st_cluster_f32(map_to_rank(smem_u32(&sh.group_w[slot][rank * p.gpc + gl]), (uint32_t)tid), gsum);
     }
     cluster_sync_all();
-    // ---- level 1, the same in every CTA: race the groups from the published sums
+    // ---- level 1, the same in every CTA: race the groups from the exchanged sums
     const int n_groups = (V + kGroup - 1) / kGroup;
     float gbest = -1.f, total = 0.f;
     int gwin = INT32_MAX;
     for (int gi = lane; gi < ((n_groups + 31) & ~31); gi += 32) {
-      float wg = 0.f;
-      if (gi < n_groups) {
-        const int r = gi / p.gpc, gl = gi - r * p.gpc;
-        wg = ld_cluster_f32(map_to_rank(smem_u32(&sh.group_w[slot][gl]), (uint32_t)r));
-      }
+      const float wg = gi < n_groups ? sh.group_w[slot][gi] : 0.f;
       float key = 0.f;
       if (wg > 0.f) {
         const Philox4 w = philox4x32_10((uint32_t)gi >> 2, (uint32_t)pos, (uint32_t)b, 2u, p.seed_lo, p.seed_hi);
@@ -338,57 +350,51 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       total += tt;
       if (kk > gbest || (kk == gbest && ii < gwin)) { gbest = kk; gwin = ii; }
     }
-    if (!(total > 0.f)) return -1;  // the same in every CTA
+    if (!(total > 0.f)) return false;  // the same in every CTA
     const int owner = gwin / p.gpc, glw = gwin - owner * p.gpc;
-    if (rank == owner) {
-      // ---- level 2: race the winning group's chunks
-      const float sc = sh.chunk_w[glw * kChunks + tid];
-      float key = 0.f;
-      if (sc > 0.f) {
-        const uint32_t ci = (uint32_t)(gwin * kChunks + tid);
-        const Philox4 w = philox4x32_10(ci >> 2, (uint32_t)pos, (uint32_t)b, 3u, p.seed_lo, p.seed_hi);
-        key = sc / -logf(word_to_uniform(w.v[ci & 3]));
-      }
-      int cwin = tid;
-      block_argmax(sh, key, cwin);
-      // ---- level 3: race the winning chunk's 32 entries (warp 0, lane i: entries 1024 i + 4c + e)
-      if (tid < 32) {
-        float best = -1.f;
-        int bx = INT32_MAX;
-        if (tid < 8) {
-          const int off = glw * kGroup + 1024 * tid + 4 * cwin;
-          if (off < n) {
-            const Philox4 w = philox4x32_10((uint32_t)((x0 + off) >> 2), (uint32_t)pos, (uint32_t)b, 1u, p.seed_lo,
-                                            p.seed_hi);
+    if (rank != owner) return true;
+    // ---- level 2 (owner CTA): race the winning group's chunks
+    const float sc = sh.chunk_w[glw * kChunks + tid];
+    float key = 0.f;
+    if (sc > 0.f) {
+      const uint32_t ci = (uint32_t)(gwin * kChunks + tid);
+      const Philox4 w = philox4x32_10(ci >> 2, (uint32_t)pos, (uint32_t)b, 3u, p.seed_lo, p.seed_hi);
+      key = sc / -logf(word_to_uniform(w.v[ci & 3]));
+    }
+    int cwin = tid;
+    block_argmax(sh, key, cwin);
+    // ---- level 3: race the winning chunk's entries (warp 0, lane i: entries 1024 i + 4c + e)
+    if (tid < 32) {
+      float best = -1.f;
+      int bx = INT32_MAX;
+      if (tid < 8) {
+        const int off = glw * kGroup + 1024 * tid + 4 * cwin;
+        if (off < n) {
+          const Philox4 w =
+              philox4x32_10((uint32_t)((x0 + off) >> 2), (uint32_t)pos, (uint32_t)b, 1u, p.seed_lo, p.seed_hi);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              if (off + e < n) {
-                const float wt = weight(off + e, residual ? qrow[off + e] : 0.f);
-                if (wt > 0.f) {
-                  const float kx = wt / -logf(word_to_uniform(w.v[e]));
-                  if (kx > best) { best = kx; bx = x0 + off + e; }
-                }
+          for (int e = 0; e < 4; ++e) {
+            if (off + e < n) {
+              const float wt = buf[off + e];
+              if (wt > 0.f) {
+                const float kx = wt / -logf(word_to_uniform(w.v[e]));
+                if (kx > best) { best = kx; bx = x0 + off + e; }
               }
             }
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bx, o);
-          if (ov > best || (ov == best && oi < bx)) { best = ov; bx = oi; }
-        }
-        if (tid == 0) sh.race[slot] = Part{best, 0.f, bx, 0};
       }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bx, o);
+        if (ov > best || (ov == best && oi < bx)) { best = ov; bx = oi; }
+      }
+      if (tid == 0) write_row(m, bx);
     }
-    cluster_sync_all();
-    int tok = 0;
-    if (rank == 0) tok = ld_cluster_s32(map_to_rank(sh_race + slot * sizeof(Part), (uint32_t)owner) + 8);
-    return tok;
+    return true;
   };
 
-  int m = k;
-  int token = -1;
   issue_row(0);
   for (int j = 0; j <= k; ++j) {
     wait_row();
@@ -400,17 +406,15 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
         if (l > v) { v = l; idx = x0 + x; }
       });
       block_argmax(sh, v, idx);
-      if (tid == 0) sh.pos[j] = Part{v, 0.f, idx, 0};
-      cluster_sync_all();
+      exchange(j, Part{v, 0.f, idx, 0});
       float bv;
       int bi;
-      cluster_best(sh_pos + j * sizeof(Part), bv, bi, nullptr);
+      cluster_best(j, bv, bi);
       if (j < k && d[j] == bi) {
         issue_row(j + 1);
         continue;
       }
-      m = j;
-      token = bi;
+      if (rank == 0 && tid == 0) write_row(j, bi);
       break;
     }
     if (j == k) {
@@ -418,25 +422,38 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       float mx = -INFINITY;
       for_slice(buf, n, vec, [&](int, float l) { mx = fmaxf(mx, l); });
       mx = block_max(sh, mx);
-      if (tid == 0) sh.pos[j] = Part{mx, 0.f, 0, 0};
-      cluster_sync_all();
+      exchange(j, Part{mx, 0.f, 0, 0});
       float M, Zunused;
-      cluster_stats(sh_pos + j * sizeof(Part), M, Zunused);
-      m = k;
-      token = race(false, M, 1.f, nullptr, k, 0);
+      cluster_stats(j, M, Zunused);
+      race(false, M, 1.f, nullptr, k, 0, k);
       break;
     }
-    // ---- sampling statistics of p_j = softmax(l / T): slice max, then sum of exp
+    // ---- sampling statistics of p_j = softmax(l / T): slice max, then
+    // e = exp2((l - max) c2) written over the slice (the race reuses it) and summed
     float mx = -INFINITY;
     for_slice(buf, n, vec, [&](int, float l) { mx = fmaxf(mx, l); });
     mx = block_max(sh, mx);
     float z = 0.f;
-    for_slice(buf, n, vec, [&](int, float l) { z += fast_exp2((l - mx) * c2); });
+    if (vec) {
+      float4* b4 = reinterpret_cast<float4*>(buf);
+      for (int g4 = tid; g4 * 4 < n; g4 += kThreads) {
+        float4 v = b4[g4];
+        v.x = fast_exp2((v.x - mx) * c2); v.y = fast_exp2((v.y - mx) * c2);
+        v.z = fast_exp2((v.z - mx) * c2); v.w = fast_exp2((v.w - mx) * c2);
+        b4[g4] = v;
+        z += (v.x + v.y) + (v.z + v.w);
+      }
+    } else {
+      for (int x = tid; x < n; x += kThreads) {
+        const float e = fast_exp2((buf[x] - mx) * c2);
+        buf[x] = e;
+        z += e;
+      }
+    }
     z = block_sum(sh, z);
-    if (tid == 0) sh.pos[j] = Part{mx, z, 0, 0};
-    cluster_sync_all();
+    exchange(j, Part{mx, z, 0, 0});
     float M, Z;
-    cluster_stats(sh_pos + j * sizeof(Part), M, Z);
+    cluster_stats(j, M, Z);
     const float pd = fast_exp2((sh.l_draft[j] - M) * c2) / Z;
     const float qd = sh.q_draft[j];
     const Philox4 wu = philox4x32_10(0u, (uint32_t)j, (uint32_t)b, 0u, p.seed_lo, p.seed_hi);
@@ -446,25 +463,24 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const Params p) {
       continue;
     }
     // ---- rejected at j: race over max(0, p_j - q_j), or over p_j if that is all zero
-    m = j;
-    const float invZ = 1.f / Z;
+    const float f = fast_exp2((mx - M) * c2) / Z;  // e_x * f = p_j(x) on this slice
     const float* qrow = p.probs + ((int64_t)b * k + j) * V + x0;
-    token = race(true, M, invZ, qrow, j, 0);
-    if (token < 0) token = race(false, M, invZ, nullptr, j, 1);  // all-zero residual: the same in every CTA
+    if (!race(true, M, f, qrow, j, 0, j)) {
+      // all-zero residual (rare): reload the logits over the overwritten slice and race over p_j
+      __syncthreads();
+      const float* src = row_ptr(j);
+      for (int x = tid; x < n; x += kThreads) buf[x] = src[x];
+      __syncthreads();
+      race(false, M, 1.f, nullptr, j, 1, j);
+    }
     break;
   }
 
   if (pending) {  // an issued copy must land before this CTA's shared memory goes away
     if (!mbar_wait_bounded(&sh.bar, phase) && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
   }
-  if (rank == 0 && tid == 0) {
-    int32_t* o = p.out_tokens + (int64_t)b * R;
-    for (int j = 0; j < m; ++j) o[j] = d[j];
-    o[m] = token;
-    for (int j = m + 1; j < R; ++j) o[j] = -1;
-    p.accept_len[b] = m;
-  }
-  cluster_sync_all();  // peers may still be reading this CTA's partials
+  // No cluster barrier here: every remote access (a push) precedes the last
+  // barrier, and nothing after it reads or writes another CTA's memory.
 }
 
 // Cluster size and slice: the slice is a whole number of race groups, at most

@@ -141,6 +141,15 @@ SPEC_DEVICE float ld_cluster_f32(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
+// Store 16 bytes into (possibly another CTA's) shared memory of this cluster.
+SPEC_DEVICE void st_cluster_v4(uint32_t addr, float a, float b, int32_t c, int32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(__float_as_uint(a)),
+               "r"(__float_as_uint(b)), "r"(c), "r"(d)
+               : "memory");
+}
+SPEC_DEVICE void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(addr), "f"(v) : "memory");
+}
 SPEC_DEVICE int32_t ld_cluster_s32(uint32_t addr) {
   int32_t v;
   asm volatile("ld.shared::cluster.s32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
