@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--gdn-layers", type=int, default=None,
+                    help="override the workload's recurrent-state layer count (small profiler captures); "
+                         "the line's config reports the count used")
     return ap.parse_args()
 
 
@@ -176,6 +179,15 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def workload_for(args):
+    w = wl.WORKLOADS[args.config]
+    if args.gdn_layers is not None:
+        if not w.gdn_layers or args.gdn_layers < 1:
+            raise SystemExit(f"--gdn-layers needs a workload with recurrent state and a count >= 1 ({w.name})")
+        w = w.replace(gdn_layers=args.gdn_layers)
+    return w
+
+
 def recorded_traffic(workload):
     """DRAM bytes per attention call from an ncu capture, if taken on the current source."""
     if not os.path.exists(TRAFFIC_FILE):
@@ -198,7 +210,7 @@ def run_native(args, world, rank, local):
     sv.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = wl.WORKLOADS[args.config]
+    w = workload_for(args)
     mode = args.mode or w.mode
     a = wl.make_attention_inputs(w, device=dev, seed=w.seed + 1000 * rank)
     acc_in = wl.make_accept_inputs(w, device=dev, seed=w.seed + 1000 * rank, mode=mode)
@@ -428,7 +440,7 @@ def oracle_step_estimate(w, mode, budget_s, seed_offset=0):
 
 
 def run_reference(args, world, rank):
-    w = wl.WORKLOADS[args.config]
+    w = workload_for(args)
     mode = args.mode or w.mode
     per_step_budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     times, tokens, sample, threads = [], 0.0, "", 1
@@ -462,7 +474,7 @@ def main():
     result = run_native(args, world, rank, local)
     if rank == 0:
         if not args.no_cpu_baseline:
-            w = wl.WORKLOADS[args.config]
+            w = workload_for(args)
             s, tokens, sample, threads = oracle_step_estimate(w, args.mode or w.mode, args.cpu_seconds)
             result["cpu_baseline"] = {"value": tokens / s, "unit": UNIT, "cores": threads, "kind": "oracle",
                                       "sample": sample}

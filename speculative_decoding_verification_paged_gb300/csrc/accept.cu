@@ -327,11 +327,12 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
         st_cluster_f32(map_to_rank(smem_u32(&sh.group_w[slot][rank * p.gpc + gl]), (uint32_t)tid), gsum);
     }
     cluster_sync_all();
-    // ---- level 1, the same in every CTA: race the groups from the exchanged sums
+    // ---- level 1, the same in every CTA: warp 0 races the groups from the exchanged
+    // sums and broadcasts (winner, total) through shared memory
     const int n_groups = (V + kGroup - 1) / kGroup;
     float gbest = -1.f, total = 0.f;
     int gwin = INT32_MAX;
-    for (int gi = lane; gi < ((n_groups + 31) & ~31); gi += 32) {
+    for (int gi = lane; tid < 32 && gi < ((n_groups + 31) & ~31); gi += 32) {
       const float wg = gi < n_groups ? sh.group_w[slot][gi] : 0.f;
       float key = 0.f;
       if (wg > 0.f) {
@@ -350,6 +351,14 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
       total += tt;
       if (kk > gbest || (kk == gbest && ii < gwin)) { gbest = kk; gwin = ii; }
     }
+    if (tid == 0) {
+      sh.wf[0] = total;
+      sh.wi[0] = gwin;
+    }
+    __syncthreads();
+    total = sh.wf[0];
+    gwin = sh.wi[0];
+    __syncthreads();  // sh.wf / sh.wi are reused by the block reductions below
     if (!(total > 0.f)) return false;  // the same in every CTA
     const int owner = gwin / p.gpc, glw = gwin - owner * p.gpc;
     if (rank != owner) return true;

@@ -32,6 +32,8 @@
 //    and a bf16 remainder and both are multiplied with V, so PV keeps ~16
 //    mantissa bits of P; softmax statistics and the output stay fp32.
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <cuda.h>
 
@@ -661,6 +663,535 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, MT>::MIN_BLOCKS) verify_atten
 }
 
 // ---------------------------------------------------------------------------
+// Tensor-core (tcgen05) kernel for D = 128.
+//
+// The keys are the MMA's M dimension (128 per tile) and the packed query rows
+// are N (16, 32 or 64), so every M = 128 MMA is fully used for any row count:
+//   S^T[128 keys x N] = K[128 x 128] . Q^T            (K, Q K-major in smem)
+//   O^T[128 d x N]   += V^T[128 x 128 keys] . P^T     (V MN-major, P K-major)
+// with S^T and O^T in tensor memory. Warp 0 stages K/V/Q with TMA, warp 1
+// issues the MMAs (one thread), warps 2-5 run the softmax: each owns one
+// 32-lane quarter of tensor memory, i.e. 32 keys of S^T and 32 dims of O^T.
+// P is written to shared memory as a bf16 high part and a bf16 remainder and
+// both are multiplied with V. The running row max may lag by up to 8 (log2
+// units); a tile that exceeds it takes the slow path: exact row max, and the
+// accumulated O^T and row sums are rescaled in place.
+// ---------------------------------------------------------------------------
+namespace tc {
+
+constexpr int D = 128;
+constexpr int TK = 128;                     // keys per tile (MMA M)
+constexpr int kSoftmaxWarps = 4;
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kThreads = 64 + kSoftmaxThreads;  // producer warp, MMA warp, softmax warps
+constexpr int kBarSoftmax = 2;              // named barrier of the softmax warps
+constexpr int kBarTail = 3;                 // named barrier of the MMA + softmax warps
+constexpr int kTmemCols = 128;              // S^T at column 0, O^T at column 64
+
+template <int MT>
+struct Cfg {
+  static constexpr int N = 16 * MT;                     // packed query rows (MMA N)
+  static constexpr int TILE_BYTES = TK * D * 2;         // 32 KB: two [128][64] slices
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K + V
+  static constexpr int Q_BYTES = N * D * 2;             // two [N][64] slices
+  static constexpr int P_BYTES = N * TK * 2;            // one of P_hi / P_lo: two [N][64] slices
+};
+
+// Dynamic shared memory of the S-stage kernel: stages + query buffers, P, barriers,
+// reductions, and the per-sequence plan (which grows with the batch).
+template <int MT, int S>
+size_t smem_bytes(int batch) {
+  using C = Cfg<MT>;
+  return 1024 + (size_t)S * (C::STAGE_BYTES + C::Q_BYTES) + 2 * C::P_BYTES + 64 * 8 + 4 * 64 * 4 + 64 * 4 + 32 +
+         align256((size_t)(batch + 2) * 4) + align256((size_t)batch * 4) + 128;
+}
+
+template <int MT, int S>
+__global__ void __launch_bounds__(kThreads, 1) verify_attention_tc_kernel(const Params p,
+                                                                         const __grid_constant__ CUtensorMap tm_q,
+                                                                         const __grid_constant__ CUtensorMap tm_k,
+                                                                         const __grid_constant__ CUtensorMap tm_v) {
+  using C = Cfg<MT>;
+  constexpr int N = C::N;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint8_t* qbuf = ring + S * C::STAGE_BYTES;
+  uint8_t* pbuf = qbuf + S * C::Q_BYTES;  // P_hi then P_lo
+  uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + 2 * C::P_BYTES);
+  uint64_t* empty = full + S;
+  uint64_t* s_full = empty + S;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* fin_bar = p_full + 1;
+  float* s_red = reinterpret_cast<float*>(full + 64);  // [4][64] cross-warp reductions
+  float* s_mrun = s_red + 4 * 64;                      // [64] running row max
+  int32_t* s_bad = reinterpret_cast<int32_t*>(s_mrun + 64);  // [4]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bad + 4);  // tensor-memory base
+  int32_t* s_prefix = reinterpret_cast<int32_t*>(s_tmem + 4);
+  int32_t* s_ctx = s_prefix + ((p.batch + 2 + 63) & ~63);
+  int32_t* s_misc = s_ctx + ((p.batch + 63) & ~63);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = p.batch, Hkv = p.num_kv_heads, G = p.gqa, R = p.rows_per_seq;
+  const int64_t max_ctx = (int64_t)p.max_blocks << p.block_shift;
+
+  // ---- 1. split plan (every CTA): per-sequence tile counts and their prefix
+  {
+    const int per = (B + kThreads - 1) / kThreads;
+    const int b0 = tid * per;
+    int mine = 0;
+    for (int i = 0; i < per; ++i) {
+      const int b = b0 + i;
+      if (b < B) {
+        const int c = p.ctx_lens[b];
+        if (c >= R && (int64_t)c <= max_ctx) mine += (c + TK - 1) / TK;
+      }
+    }
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_misc[warp] = incl;
+    __syncthreads();
+    int run = incl - mine;
+    for (int w = 0; w < warp; ++w) run += s_misc[w];
+    if (tid == kThreads - 1) s_prefix[B] = run + mine;
+    for (int i = 0; i < per; ++i) {
+      const int b = b0 + i;
+      if (b < B) {
+        s_prefix[b] = run;
+        const int c = p.ctx_lens[b];
+        s_ctx[b] = c;
+        if (c >= R && (int64_t)c <= max_ctx) run += (c + TK - 1) / TK;
+      }
+    }
+    if (tid == 0) {
+      for (int s = 0; s < S; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&empty[s], 1);
+      }
+      mbar_init(s_full, 1);
+      mbar_init(p_full, kSoftmaxWarps);
+      mbar_init(fin_bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+  }
+  for (int b = blockIdx.x; b < B; b += gridDim.x) {
+    if (s_prefix[b + 1] != s_prefix[b]) continue;
+    if (tid == 0) raise_error(p.dev_err, SPEC_DEVERR_CTX_LEN);
+    float4* dst = reinterpret_cast<float4*>(p.out + (int64_t)b * R * p.num_q_heads * D);
+    for (int i = tid; i < R * p.num_q_heads * D / 4; i += kThreads) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int64_t T = (int64_t)s_prefix[B] * Hkv;
+  if (T == 0) return;
+  const int64_t W = (T + gridDim.x - 1) / gridDim.x;
+  const int64_t f0 = (int64_t)blockIdx.x * W;
+  const int64_t f1 = min(T, f0 + W);
+  if (f0 >= f1) return;
+
+  // tensor memory: allocated by the MMA warp, address broadcast through shared memory
+  if (warp == 1) {
+    tmem_alloc(smem_u32(s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  // padded query rows stay zero in every query buffer (TMA writes rows < R*G only)
+  for (int i = tid; i < S * 2 * (N - p.n_rows) * 8; i += kThreads) {
+    const int ch = i % 8, rest = i / 8;
+    const int r = p.n_rows + rest % (N - p.n_rows);
+    const int bsub = rest / (N - p.n_rows);
+    const int buf = bsub / 2, sub = bsub % 2;
+    *reinterpret_cast<uint4*>(qbuf + buf * C::Q_BYTES + sub * N * 128 + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();  // zeroed rows are read by the tensor core
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t tmem_s = tmem, tmem_o = tmem + 64;
+  const uint32_t ring_u32 = smem_u32(ring), q_u32 = smem_u32(qbuf), p_u32 = smem_u32(pbuf);
+
+  if (warp == 0) {
+    // =================== producer: TMA, S stages ahead ===================
+    const int bs = 1 << p.block_shift;
+    const int BH = bs < TK ? bs : TK;
+    const int pieces = TK / BH;
+    Cursor ld = cursor_at(f0, s_prefix, B, Hkv);
+    bool fresh = true;
+    int win_b = -1, win_base = 0, win_val = 0;
+    for (int64_t f = f0; f < f1; ++f) {
+      const int s = (int)((f - f0) % S);
+      const int64_t rnd = (f - f0) / S;
+      const int b = ld.b, g = ld.g;
+      const int ctx = s_ctx[b];
+      const int t0 = ld.tile * TK;
+      const int slot = ld.seq % S;
+      int zc[TK / 16];
+      bool bad = false;
+#pragma unroll
+      for (int pc = 0; pc < TK / 16; ++pc) {
+        if (pc >= pieces) break;
+        const int t = t0 + pc * BH;
+        int z = -BH;
+        if (t < ctx) {
+          const int n = t >> p.block_shift;
+          if (b != win_b || n < win_base || n >= win_base + 32) {
+            win_b = b;
+            win_base = n;
+            const int nb = (ctx + bs - 1) >> p.block_shift;
+            win_val = (n + lane < nb) ? __ldg(p.block_table + (int64_t)b * p.max_blocks + n + lane) : 0;
+          }
+          const int32_t phys = __shfl_sync(0xffffffffu, win_val, n - win_base);
+          if (phys < 0 || (int64_t)phys >= p.num_blocks) bad = true;
+          else z = (int)(((int64_t)phys << p.block_shift) + (t & (bs - 1)));
+        }
+        zc[pc] = z;
+      }
+      if (lane == 0) {
+        if (rnd > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((rnd - 1) & 1)))
+          raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+        if (fresh) s_bad[slot] = 0;
+        if (bad) s_bad[slot] = 1;
+        const uint32_t q_bytes = fresh ? (uint32_t)(R * G * D * 2) : 0u;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)C::STAGE_BYTES + q_bytes);
+        if (fresh) {
+          const uint32_t qdst = q_u32 + slot * C::Q_BYTES;
+          tma_load_3d(qdst, &tm_q, 0, g * G, b * R, &full[s]);
+          tma_load_3d(qdst + N * 128, &tm_q, 64, g * G, b * R, &full[s]);
+        }
+        const uint32_t kdst = ring_u32 + s * C::STAGE_BYTES;
+        const uint32_t vdst = kdst + C::TILE_BYTES;
+#pragma unroll
+        for (int pc = 0; pc < TK / 16; ++pc) {
+          if (pc >= pieces) break;
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub) {
+            const uint32_t off = sub * TK * 128 + pc * BH * 128;
+            tma_load_3d(kdst + off, &tm_k, sub * 64, g, zc[pc], &full[s]);
+            tma_load_3d(vdst + off, &tm_v, sub * 64, g, zc[pc], &full[s]);
+          }
+        }
+      }
+      __syncwarp();
+      const int before = ld.seq;
+      cursor_advance(ld, s_prefix, B, Hkv);
+      fresh = ld.seq != before;
+    }
+    return;
+  }
+
+  if (warp == 1) {
+    // =================== MMA issuer (one thread) ===================
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = umma_idesc_bf16(128, N, 0, 0);
+      constexpr uint32_t idesc_pv = umma_idesc_bf16(128, N, 1, 0);
+      Cursor cu = cursor_at(f0, s_prefix, B, Hkv);
+      bool fresh = true;
+      for (int64_t f = f0; f < f1; ++f) {
+        const int64_t i = f - f0;
+        const int s = (int)(i % S);
+        if (!mbar_wait_bounded(&full[s], (uint32_t)((i / S) & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+        tc_fence_after();
+        const uint32_t kb = ring_u32 + s * C::STAGE_BYTES;
+        const uint32_t vb = kb + C::TILE_BYTES;
+        const uint32_t qb = q_u32 + (cu.seq % S) * C::Q_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (ks & 3) * 32;
+          const uint64_t ad = smem_desc_sw128(kb + (ks >> 2) * TK * 128 + koff, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(qb + (ks >> 2) * N * 128 + koff, 16, 1024);
+          umma_bf16(tmem_s, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);
+        if (!mbar_wait_bounded(p_full, (uint32_t)(i & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+        tc_fence_after();
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t pb = p_u32 + part * C::P_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < TK / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(vb + kk * 2048, TK * 128, 1024);
+            const uint64_t bd = smem_desc_sw128(pb + (kk >> 2) * N * 128 + (kk & 3) * 32, 16, 1024);
+            umma_bf16(tmem_o, ad, bd, idesc_pv, (fresh && part == 0 && kk == 0) ? 0u : 1u);
+          }
+        }
+        umma_commit(&empty[s]);  // the stage (and P) is free once these MMAs are done
+        if (f == f1 - 1) umma_commit(fin_bar);
+        const int before = cu.seq;
+        cursor_advance(cu, s_prefix, B, Hkv);
+        fresh = cu.seq != before;
+      }
+    }
+    __syncwarp();
+    named_sync(kBarTail, 32 + kSoftmaxThreads);  // softmax warps are done with tensor memory
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+    return;
+  }
+
+  // =================== softmax / epilogue warps ===================
+  const int q4 = warp & 3;            // tensor-memory lane quarter of this warp
+  const int st = tid - 64;            // 0..127
+  const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+  const int key_in_tile = q4 * 32 + lane;  // the S^T lane this thread reads
+  float l_part[N];
+#pragma unroll
+  for (int r = 0; r < N; ++r) l_part[r] = 0.f;
+  Cursor cu = cursor_at(f0, s_prefix, B, Hkv);
+  bool cu_fresh = true, from_zero = true, pending = false, fin_bad = false;
+  Fin fin;
+  int ctx = 0, prefix_len = 0;
+
+  // Write the finished unit piece: output rows (whole unit) or a normalised partial.
+  auto epilogue = [&](const Fin& F) {
+    // row sums over all 128 key lanes
+#pragma unroll
+    for (int r = 0; r < N; ++r) {
+      float v = l_part[r];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) s_red[q4 * 64 + r] = v;
+    }
+    const bool bad = named_sync_or(kBarSoftmax, kSoftmaxThreads, fin_bad);
+    const int d = q4 * 32 + lane;  // the O^T lane this thread reads
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) {
+      float ov[16];
+      tmem_ld16(tmem_o + lane_off + c * 16, ov);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int r = c * 16 + e;
+        if (r < p.n_rows) {
+          const float L = s_red[r] + s_red[64 + r] + s_red[128 + r] + s_red[192 + r];
+          const float M = s_mrun[r];
+          const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
+          float* dst;
+          if (F.complete) {
+            const int i = r / G, j = r - i * G;
+            dst = p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
+          } else {
+            dst = p.opart + ((int64_t)F.slot * p.n_rows + r) * D;
+            if (d == 0) {
+              float lse2 = L > 0.f ? M + __log2f(L) : -INFINITY;
+              if (bad) lse2 = __int_as_float(0x7fc00000);
+              p.lse[(int64_t)F.slot * p.n_rows + r] = lse2;
+            }
+          }
+          dst[d] = ov[e] * inv;
+        }
+      }
+    }
+    if (bad && st == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
+    if (!F.complete) {
+      __threadfence();
+      named_sync(kBarSoftmax, kSoftmaxThreads);
+      const int unit = F.b * Hkv + F.g;
+      if (st == 0) s_misc[8] = (atomicAdd(p.counters + unit, 1) == F.nseg - 1) ? 1 : 0;
+      named_sync(kBarSoftmax, kSoftmaxThreads);
+      if (s_misc[8]) {
+        __threadfence();
+        for (int idx = st; idx < p.n_rows * (D / 4); idx += kSoftmaxThreads) {
+          const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+          float Mx = -INFINITY;
+          bool nan = false;
+          for (int sg = 0; sg < F.nseg; ++sg) {
+            const int slot = piece_slot(F.c0 + sg, F.c0, F.u0, W);
+            const float l = __ldcg(p.lse + (int64_t)slot * p.n_rows + r);
+            nan |= l != l;
+            Mx = fmaxf(Mx, l);
+          }
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (!nan && Mx != -INFINITY) {
+            float wsum = 0.f;
+            for (int sg = 0; sg < F.nseg; ++sg) {
+              const int slot = piece_slot(F.c0 + sg, F.c0, F.u0, W);
+              const float wgt = exp2f(__ldcg(p.lse + (int64_t)slot * p.n_rows + r) - Mx);
+              if (wgt > 0.f) {
+                const float4 v =
+                    __ldcg(reinterpret_cast<const float4*>(p.opart + ((int64_t)slot * p.n_rows + r) * D) + d4);
+                acc.x += wgt * v.x;
+                acc.y += wgt * v.y;
+                acc.z += wgt * v.z;
+                acc.w += wgt * v.w;
+              }
+              wsum += wgt;
+            }
+            const float inv = 1.f / wsum;
+            acc.x *= inv;
+            acc.y *= inv;
+            acc.z *= inv;
+            acc.w *= inv;
+          }
+          const int i = r / G, j = r - i * G;
+          reinterpret_cast<float4*>(p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D)[d4] = acc;
+        }
+        if (st == 0) p.counters[unit] = 0;
+      }
+    }
+    named_sync(kBarSoftmax, kSoftmaxThreads);  // s_red / s_mrun are reused
+  };
+
+  for (int64_t f = f0; f < f1; ++f) {
+    const int64_t i = f - f0;
+    const int stage = (int)(i % S);
+    if (!mbar_wait_bounded(s_full, (uint32_t)(i & 1)) && st == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+    tc_fence_after();
+    if (pending) {  // every MMA of the previous unit is complete: write it out
+      epilogue(fin);
+      pending = false;
+    }
+    if (cu_fresh) {
+      from_zero = cu.tile == 0;
+      ctx = s_ctx[cu.b];
+      prefix_len = ctx - R;
+#pragma unroll
+      for (int r = 0; r < N; ++r) l_part[r] = 0.f;
+      if (st < N) s_mrun[st] = -INFINITY;
+      named_sync(kBarSoftmax, kSoftmaxThreads);
+    }
+    const int t0 = cu.tile * TK;
+    const int tkey = t0 + key_in_tile;
+    // row r sees this key iff r >= rmin (rows of draft position i see keys <= prefix_len + i)
+    const int rmin = tkey >= ctx ? (1 << 30) : (tkey > prefix_len ? (tkey - prefix_len) * G : 0);
+    // ---- pass 1: does any score exceed its row's running max by more than 8?
+    bool grow = false;
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) {
+      float sv[16];
+      tmem_ld16(tmem_s + lane_off + c * 16, sv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int r = c * 16 + e;
+        const float x = r < rmin ? -INFINITY : sv[e] * p.scale_log2;
+        grow |= x > s_mrun[r] + 8.f;
+      }
+    }
+    if (named_sync_or(kBarSoftmax, kSoftmaxThreads, grow)) {
+      // ---- slow path: exact tile max per row, rescale O^T and the row sums
+#pragma unroll
+      for (int c = 0; c < N / 16; ++c) {
+        float sv[16];
+        tmem_ld16(tmem_s + lane_off + c * 16, sv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int r = c * 16 + e;
+          float x = r < rmin ? -INFINITY : sv[e] * p.scale_log2;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+          if (lane == 0) s_red[q4 * 64 + r] = x;
+        }
+      }
+      named_sync(kBarSoftmax, kSoftmaxThreads);
+      const bool rescale_o = !cu_fresh;  // O^T holds earlier tiles of this unit
+#pragma unroll
+      for (int c = 0; c < N / 16; ++c) {
+        float alpha[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int r = c * 16 + e;
+          const float tm = fmaxf(fmaxf(s_red[r], s_red[64 + r]), fmaxf(s_red[128 + r], s_red[192 + r]));
+          const float mo = s_mrun[r];
+          const float mn = fmaxf(mo, tm);
+          alpha[e] = (mo == -INFINITY || mn == -INFINITY) ? (mo == -INFINITY ? 0.f : 1.f) : fast_exp2(mo - mn);
+          l_part[r] *= alpha[e];
+        }
+        if (rescale_o) {
+          float ov[16];
+          tmem_ld16(tmem_o + lane_off + c * 16, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ov[e] *= alpha[e];
+          tmem_st16(tmem_o + lane_off + c * 16, ov);
+        }
+      }
+      if (rescale_o) tmem_wait_st();
+      named_sync(kBarSoftmax, kSoftmaxThreads);  // everyone has read the old running max
+      if (st < N) {
+        const float tm = fmaxf(fmaxf(s_red[st], s_red[64 + st]), fmaxf(s_red[128 + st], s_red[192 + st]));
+        s_mrun[st] = fmaxf(s_mrun[st], tm);
+      }
+      named_sync(kBarSoftmax, kSoftmaxThreads);
+    }
+    // ---- keys past the context in the last tile may hold stale bytes: zero those V rows
+    if (t0 + TK > ctx) {
+      const int valid = ctx - t0;
+      uint8_t* vt = ring + stage * C::STAGE_BYTES + C::TILE_BYTES;
+      for (int j = st; j < (TK - valid) * 16; j += kSoftmaxThreads) {
+        const int row = valid + j / 16, ch = j % 16;
+        *reinterpret_cast<uint4*>(vt + (ch >> 3) * TK * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
+    // ---- pass 2: P = exp2(x - m) as bf16 hi + lo, written K-major [N rows][128 keys]
+    const int kk = key_in_tile;
+    const uint32_t psub = (uint32_t)(kk >> 6) * N * 128;
+#pragma unroll
+    for (int c = 0; c < N / 16; ++c) {
+      float sv[16];
+      tmem_ld16(tmem_s + lane_off + c * 16, sv);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        float pv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = c * 16 + e + h;
+          const float x = r < rmin ? -INFINITY : sv[e + h] * p.scale_log2;
+          const float m = s_mrun[r];
+          pv[h] = fast_exp2(x - (m == -INFINITY ? 0.f : m));
+          l_part[r] += pv[h];
+        }
+        // lanes (2i, 2i+1): the even lane stores row r for both keys, the odd lane row r+1
+        const float o0 = __shfl_xor_sync(0xffffffffu, pv[0], 1);
+        const float o1 = __shfl_xor_sync(0xffffffffu, pv[1], 1);
+        const bool even = (lane & 1) == 0;
+        const int r = c * 16 + e + (even ? 0 : 1);
+        const float a = even ? pv[0] : o1;   // key kk & ~1
+        const float bb = even ? o0 : pv[1];  // key kk | 1
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, bb);
+        const float2 hf = __bfloat1622float2(h2);
+        const uint32_t lo = pack_bf16(a - hf.x, bb - hf.y);
+        const uint32_t off = psub + r * 128 + ((((kk & 63) >> 3) ^ (r & 7)) << 4) + ((kk & 6) << 1);
+        *reinterpret_cast<__nv_bfloat162*>(pbuf + off) = h2;
+        *reinterpret_cast<uint32_t*>(pbuf + C::P_BYTES + off) = lo;
+      }
+    }
+    fence_proxy_async_smem();  // P and zeroed V rows are read by the tensor core
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_full);
+    if (f == f1 - 1 || cu.tile == cu.ntiles - 1) {
+      const int64_t u0 = (int64_t)s_prefix[cu.b] * Hkv + (int64_t)cu.g * cu.ntiles;
+      fin.b = cu.b;
+      fin.g = cu.g;
+      fin.seq = cu.seq;
+      fin.complete = from_zero && cu.tile == cu.ntiles - 1;
+      fin.u0 = u0;
+      fin.c0 = (int)(u0 / W);
+      fin.nseg = (int)((u0 + cu.ntiles - 1) / W) - fin.c0 + 1;
+      fin.slot = piece_slot((int)blockIdx.x, fin.c0, u0, W);
+      fin_bad = s_bad[cu.seq % S] != 0;  // every tile of the unit in range is loaded by now
+      pending = true;
+    }
+    const int before = cu.seq;
+    cursor_advance(cu, s_prefix, B, Hkv);
+    cu_fresh = cu.seq != before;
+  }
+  if (!mbar_wait_bounded(fin_bar, 0) && st == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+  tc_fence_after();
+  if (pending) epilogue(fin);
+  tc_fence_before();
+  named_sync(kBarTail, 32 + kSoftmaxThreads);
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 struct Layout {
@@ -765,6 +1296,82 @@ static int launch_main_d(const Params& p, int mt, const CUtensorMap& tq, const C
   }
 }
 
+// The tcgen05 kernel: one CTA per SM (its grid never exceeds the mma.sync kernel's).
+template <int MT, int S>
+static int launch_tc(const Params& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                     cudaStream_t stream) {
+  auto kern = tc::verify_attention_tc_kernel<MT, S>;
+  const size_t smem = tc::smem_bytes<MT, S>(p.batch);
+  static int cached_dev = -1, cached_grid = 0;
+  static size_t cached_smem = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  if (dev != cached_dev || smem != cached_smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return SPEC_ERR_LAUNCH;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+    cached_grid = sms > kMaxGrid ? kMaxGrid : sms;
+    cached_dev = dev;
+    cached_smem = smem;
+  }
+  kern<<<cached_grid, tc::kThreads, smem, stream>>>(p, tq, tk, tv);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+enum class Kernel { kMma, kTc };
+
+// Which kernel runs a call. The environment variable SPEC_ATTN_KERNEL=tc
+// selects the tcgen05 kernel for D = 128 when its shared memory fits the batch;
+// otherwise (and by default) the mma.sync kernel runs. Both compute the same
+// result within rounding.
+static Kernel choose_kernel(int D, int mt, int batch, int* stages) {
+  *stages = 0;
+  if (D != 128) return Kernel::kMma;
+  const char* env = getenv("SPEC_ATTN_KERNEL");
+  if (env == nullptr || strcmp(env, "tc") != 0) return Kernel::kMma;
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return Kernel::kMma;
+  size_t need3 = SIZE_MAX, need2 = SIZE_MAX;
+  switch (mt) {
+    case 1: need3 = tc::smem_bytes<1, 3>(batch); need2 = tc::smem_bytes<1, 2>(batch); break;
+    case 2: need2 = tc::smem_bytes<2, 2>(batch); break;
+    default: need2 = tc::smem_bytes<4, 2>(batch); break;
+  }
+  if (need3 <= (size_t)optin) *stages = 3;
+  else if (need2 <= (size_t)optin) *stages = 2;
+  else return Kernel::kMma;
+  return Kernel::kTc;
+}
+
+// Builds the tensor maps for the chosen kernel's key tile and launches it.
+static int dispatch(const Params& p, int D, int bs, const void* q, const void* k_cache, const void* v_cache,
+                    int64_t num_blocks, cudaStream_t stream) {
+  const int R = p.rows_per_seq, G = p.gqa;
+  const int mt = R * G <= 16 ? 1 : (R * G <= 32 ? 2 : 4);
+  int stages = 0;
+  const Kernel kind = choose_kernel(D, mt, p.batch, &stages);
+  const int tk = kind == Kernel::kTc ? tc::TK : tile_keys(D, mt);
+  CUtensorMap tq, tk_map, tv_map;
+  if (!make_map(&tq, q, D, p.num_q_heads, (uint64_t)p.batch * R, (uint32_t)G, (uint32_t)R) ||
+      !make_map(&tk_map, k_cache, D, p.num_kv_heads, (uint64_t)num_blocks * bs, 1, (uint32_t)(bs < tk ? bs : tk)) ||
+      !make_map(&tv_map, v_cache, D, p.num_kv_heads, (uint64_t)num_blocks * bs, 1, (uint32_t)(bs < tk ? bs : tk)))
+    return SPEC_ERR_LAUNCH;
+  if (kind == Kernel::kTc) {
+    if (mt == 1) return stages == 3 ? launch_tc<1, 3>(p, tq, tk_map, tv_map, stream)
+                                    : launch_tc<1, 2>(p, tq, tk_map, tv_map, stream);
+    if (mt == 2) return launch_tc<2, 2>(p, tq, tk_map, tv_map, stream);
+    return launch_tc<4, 2>(p, tq, tk_map, tv_map, stream);
+  }
+  switch (D) {
+    case 64: return launch_main_d<64>(p, mt, tq, tk_map, tv_map, stream);
+    case 128: return launch_main_d<128>(p, mt, tq, tk_map, tv_map, stream);
+    default: return launch_main_d<256>(p, mt, tq, tk_map, tv_map, stream);
+  }
+}
+
 }  // namespace attn
 }  // namespace specv
 
@@ -793,15 +1400,6 @@ extern "C" int spec_verify_attention(const void* q, const void* k_cache, const v
 
   const int R = k_draft + 1, G = d->num_q_heads / d->num_kv_heads, D = d->head_dim;
   const int bs = d->block_size;
-  const int mt = R * G <= 16 ? 1 : (R * G <= 32 ? 2 : 4);
-  const int tk = attn::tile_keys(D, mt);
-  CUtensorMap tq, tk_map, tv_map;
-  if (!attn::make_map(&tq, q, D, d->num_q_heads, (uint64_t)d->batch * R, (uint32_t)G, (uint32_t)R) ||
-      !attn::make_map(&tk_map, k_cache, D, d->num_kv_heads, (uint64_t)d->num_blocks * bs, 1,
-                      (uint32_t)(bs < tk ? bs : tk)) ||
-      !attn::make_map(&tv_map, v_cache, D, d->num_kv_heads, (uint64_t)d->num_blocks * bs, 1,
-                      (uint32_t)(bs < tk ? bs : tk)))
-    return SPEC_ERR_LAUNCH;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   attn::Params p;
@@ -824,12 +1422,7 @@ extern "C" int spec_verify_attention(const void* q, const void* k_cache, const v
   p.block_shift = shift;
   p.max_blocks = d->max_blocks_per_seq;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
-
-  switch (D) {
-    case 64: return attn::launch_main_d<64>(p, mt, tq, tk_map, tv_map, stream);
-    case 128: return attn::launch_main_d<128>(p, mt, tq, tk_map, tv_map, stream);
-    default: return attn::launch_main_d<256>(p, mt, tq, tk_map, tv_map, stream);
-  }
+  return attn::dispatch(p, D, bs, q, k_cache, v_cache, d->num_blocks, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -850,7 +1443,8 @@ constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Persistent grid the launch will use (the same occupancy query as launch_main).
+// Largest persistent grid a launch can use: the mma.sync kernel's occupancy (the
+// tcgen05 kernel runs one CTA per SM, never more CTAs than this).
 template <int D, int MT>
 static int noalloc_grid(int batch, int* grid) {
   auto kern = verify_attention_kernel<D, MT>;
@@ -929,15 +1523,6 @@ extern "C" int spec_verify_attention_noalloc(const void* q, const void* k_cache,
   // The counters must start at zero; every call shares the array, so clear them here.
   if (cudaMemsetAsync(ws, 0, counters_bytes, stream) != cudaSuccess) return SPEC_ERR_LAUNCH;
 
-  const int tk = attn::tile_keys(D, mt);
-  CUtensorMap tq, tk_map, tv_map;
-  if (!attn::make_map(&tq, q, D, d->num_q_heads, (uint64_t)d->batch * R, (uint32_t)G, (uint32_t)R) ||
-      !attn::make_map(&tk_map, k_cache, D, d->num_kv_heads, (uint64_t)d->num_blocks * bs, 1,
-                      (uint32_t)(bs < tk ? bs : tk)) ||
-      !attn::make_map(&tv_map, v_cache, D, d->num_kv_heads, (uint64_t)d->num_blocks * bs, 1,
-                      (uint32_t)(bs < tk ? bs : tk)))
-    return SPEC_ERR_LAUNCH;
-
   attn::Params p;
   p.block_table = block_table;
   p.ctx_lens = ctx_lens;
@@ -958,10 +1543,5 @@ extern "C" int spec_verify_attention_noalloc(const void* q, const void* k_cache,
   p.block_shift = shift;
   p.max_blocks = d->max_blocks_per_seq;
   p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
-
-  switch (D) {
-    case 64: return attn::launch_main_d<64>(p, mt, tq, tk_map, tv_map, stream);
-    case 128: return attn::launch_main_d<128>(p, mt, tq, tk_map, tv_map, stream);
-    default: return attn::launch_main_d<256>(p, mt, tq, tk_map, tv_map, stream);
-  }
+  return attn::dispatch(p, D, bs, q, k_cache, v_cache, d->num_blocks, stream);
 }

@@ -3,7 +3,8 @@
 Small cases are checked in full; the named workloads at their full sizes are
 checked on sampled sequences (the oracle recomputes those sequences one by one
 from the same device inputs). Tolerances: max-abs <= 1e-2 and relative L2 <=
-2e-3 per case.
+2e-3 per case. Head dim 128 has two kernels (mma.sync by default, tcgen05 with
+SPEC_ATTN_KERNEL=tc); every head-dim-128 case runs both.
 """
 
 import zlib
@@ -34,6 +35,31 @@ SMALL = [
 ]
 
 
+# Head-dim-128 cases aimed at the tcgen05 kernel: 128-key tiles made of 8, 4, 2 or 1
+# TMA pieces, contexts just below / at / above tile edges, every packed-row count
+# (16, 24 -> 32, 32, 64), k = 1 and k = 7, and batches whose plan pushes the kernel
+# to two stages (1600) or back to mma.sync (4096 with 64 rows).
+TC_CASES = [
+    ("tc_mt1_bs32_edges", 6, (4, 127, 128, 129, 255, 1100), 32, 32, 8, 128, 3),
+    ("tc_mt1_k1_bs64", 4, (2, 64, 129, 3000), 64, 8, 1, 128, 1),
+    ("tc_mt2_rows24_bs128", 4, (4, 128, 385, 2100), 128, 24, 4, 128, 3),
+    ("tc_mt2_k7_bs64", 4, (8, 200, 513, 1500), 64, 16, 4, 128, 7),
+    ("tc_mt4_bs16", 3, (5, 300, 1200), 16, 64, 4, 128, 3),
+    ("tc_mt4_k7_bs32", 3, (8, 640, 1030), 32, 16, 2, 128, 7),
+]
+
+
+@pytest.fixture(params=["tc", "mma"])
+def attn_kernel(request, monkeypatch):
+    monkeypatch.setenv("SPEC_ATTN_KERNEL", request.param)
+    return request.param
+
+
+def _ragged(B, lo, hi, seed):
+    rng = np.random.default_rng(seed)
+    return tuple(int(x) for x in rng.integers(lo, hi + 1, size=B))
+
+
 def run_attention(sv, a, w, **kw):
     out = torch.full((w.batch, w.rows, w.num_q_heads, w.head_dim), float("nan"), dtype=torch.float32, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -43,9 +69,11 @@ def run_attention(sv, a, w, **kw):
     return out, int(err.item())
 
 
-@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
-def test_attention_small_cases_full_parity(sv, oracle_mod, case):
+@pytest.mark.parametrize("case", SMALL + TC_CASES, ids=[c[0] for c in SMALL + TC_CASES])
+def test_attention_small_cases_full_parity(sv, oracle_mod, case, attn_kernel):
     name, B, ctx, bs, Hq, Hkv, D, k = case
+    if D != 128 and attn_kernel == "tc":
+        pytest.skip("one kernel for this head dim")
     w = wl.Workload(name=name, batch=B, ctx_lens=ctx, block_size=bs, num_q_heads=Hq, num_kv_heads=Hkv,
                     head_dim=D, k_draft=k, seed=zlib.crc32(name.encode()) % 1000)
     a = wl.make_attention_inputs(w, device=DEV)
@@ -66,8 +94,10 @@ def test_attention_tiny_workload(sv, oracle_mod):
 
 
 @pytest.mark.parametrize("name", ["llama8b_eagle3", "serving128", "hybrid_gdn", "longctx"])
-def test_attention_full_size_sampled_sequences(sv, oracle_mod, name):
+def test_attention_full_size_sampled_sequences(sv, oracle_mod, name, attn_kernel):
     w = wl.WORKLOADS[name]
+    if w.head_dim != 128 and attn_kernel == "tc":
+        pytest.skip("one kernel for this head dim")
     a = wl.make_attention_inputs(w, device=DEV)
     out, err = run_attention(sv, a, w)
     assert err == 0
@@ -81,7 +111,19 @@ def test_attention_full_size_sampled_sequences(sv, oracle_mod, name):
     assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
 
 
-def test_attention_is_deterministic_and_reuses_workspace(sv):
+@pytest.mark.parametrize("B,Hq,k", [(1600, 32, 3), (4096, 16, 7)], ids=["b1600_mt1", "b4096_mt4"])
+def test_attention_large_batch_plans(sv, oracle_mod, attn_kernel, B, Hq, k):
+    """Batches whose per-sequence plan fills shared memory: every sequence is checked."""
+    w = wl.Workload(name=f"big{B}", batch=B, ctx_lens=_ragged(B, k + 1, 160, B), block_size=16,
+                    num_q_heads=Hq, num_kv_heads=2 if Hq == 16 else 8, head_dim=128, k_draft=k, seed=B % 997)
+    a = wl.make_attention_inputs(w, device=DEV)
+    out, err = run_attention(sv, a, w)
+    assert err == 0
+    mx, rel = attention_errors(out.cpu().numpy(), oracle_attention_for(oracle_mod, a))
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+
+
+def test_attention_is_deterministic_and_reuses_workspace(sv, attn_kernel):
     w = wl.WORKLOADS["llama8b_eagle3"].replace(batch=8, ctx_lens=(2048,) * 8)
     a = wl.make_attention_inputs(w, device=DEV)
     ws = sv.new_attention_workspace(
@@ -91,7 +133,7 @@ def test_attention_is_deterministic_and_reuses_workspace(sv):
     assert torch.equal(o1, o2)
 
 
-def test_attention_bad_block_and_bad_ctx_give_zero_rows(sv, oracle_mod):
+def test_attention_bad_block_and_bad_ctx_give_zero_rows(sv, oracle_mod, attn_kernel):
     w = wl.Workload(name="bad", batch=4, ctx_lens=(300, 300, 300, 300), block_size=16, num_q_heads=8,
                     num_kv_heads=2, head_dim=128, k_draft=3, seed=5)
     a = wl.make_attention_inputs(w, device=DEV)
