@@ -680,54 +680,122 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, MT>::MIN_BLOCKS) verify_atten
 namespace tc {
 
 constexpr int D = 128;
-constexpr int TK = 128;                     // keys per tile (MMA M)
-constexpr int kSoftmaxWarps = 4;
+constexpr int TK = 128;                      // keys per tile (MMA M)
+constexpr int kSoftmaxWarps = 8;             // two warpgroups, each owning half the query rows
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kThreads = 64 + kSoftmaxThreads;  // producer warp, MMA warp, softmax warps
-constexpr int kBarSoftmax = 2;              // named barrier of the softmax warps
-constexpr int kBarTail = 3;                 // named barrier of the MMA + softmax warps
-constexpr int kTmemCols = 128;              // S^T at column 0, O^T at column 64
+// Register budget: up to three warps share an SM sub-partition (16K registers),
+// so a thread may hold at most 168 registers; declaring 384 threads caps it there.
+constexpr int kRegBudgetThreads = 384;
+constexpr int kBarGroup0 = 2;                // named barriers: one per softmax warpgroup,
+constexpr int kBarSoftmax = 4;               // all softmax warps,
+constexpr int kBarTail = 5;                  // MMA warp + softmax warps
+constexpr int kTmemCols = 256;               // S^T buffers at columns 0 and N, O^T at 2N
 
 template <int MT>
 struct Cfg {
   static constexpr int N = 16 * MT;                     // packed query rows (MMA N)
+  static constexpr int CW = N / 2;                      // rows (tensor-memory columns) per warpgroup
   static constexpr int TILE_BYTES = TK * D * 2;         // 32 KB: two [128][64] slices
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K + V
   static constexpr int Q_BYTES = N * D * 2;             // two [N][64] slices
   static constexpr int P_BYTES = N * TK * 2;            // one of P_hi / P_lo: two [N][64] slices
 };
 
-// Dynamic shared memory of the S-stage kernel: stages + query buffers, P, barriers,
-// reductions, and the per-sequence plan (which grows with the batch).
-template <int MT, int S>
+// Dynamic shared memory: stages + query buffers, NP P buffers (hi + lo), barriers,
+// reductions, output row offsets, and the per-sequence plan (which grows with the batch).
+template <int MT, int S, int NP>
 size_t smem_bytes(int batch) {
   using C = Cfg<MT>;
-  return 1024 + (size_t)S * (C::STAGE_BYTES + C::Q_BYTES) + 2 * C::P_BYTES + 64 * 8 + 4 * 64 * 4 + 64 * 4 + 32 +
-         align256((size_t)(batch + 2) * 4) + align256((size_t)batch * 4) + 128;
+  return 1024 + (size_t)S * (C::STAGE_BYTES + C::Q_BYTES) + (size_t)NP * 2 * C::P_BYTES + 64 * 8 + 4 * 64 * 4 +
+         64 * 4 + 64 * 8 + 64 + align256((size_t)(batch + 2) * 4) + align256((size_t)batch * 4) + 128;
 }
 
-template <int MT, int S>
-__global__ void __launch_bounds__(kThreads, 1) verify_attention_tc_kernel(const Params p,
-                                                                         const __grid_constant__ CUtensorMap tm_q,
-                                                                         const __grid_constant__ CUtensorMap tm_k,
-                                                                         const __grid_constant__ CUtensorMap tm_v) {
+// Reduction of CW columns over the 32 lanes of a warp by recursive halving: at
+// level j every lane keeps half of its remaining columns (chosen by lane bit j)
+// and receives the partner lane's values for that half, so CW - 1 shuffles cover
+// the first log2(CW) levels; the rest is a plain butterfly on one value. Lane l
+// ends with the result for column reduced_col<CW>(l); v is destroyed.
+template <int CW>
+__device__ __forceinline__ int reduced_col(int lane) {
+  int c = 0;
+#pragma unroll
+  for (int j = 0; (CW >> j) > 1; ++j) c += ((lane >> j) & 1) * (CW >> (j + 1));
+  return c;
+}
+template <int CW, bool kMax>
+__device__ __forceinline__ float reduce_cols(float (&v)[CW], int lane) {
+#pragma unroll
+  for (int j = 0; (CW >> j) > 1; ++j) {
+    const int half = (CW >> j) / 2;
+    const bool upper = (lane >> j) & 1;
+#pragma unroll
+    for (int t = 0; t < half; ++t) {
+      const float mine = upper ? v[t + half] : v[t];
+      const float other = upper ? v[t] : v[t + half];
+      const float recv = __shfl_xor_sync(0xffffffffu, other, 1 << j);
+      v[t] = kMax ? fmaxf(mine, recv) : mine + recv;
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int j = 0; j < 5; ++j) {
+    if ((CW >> j) > 1) continue;
+    const float o = __shfl_xor_sync(0xffffffffu, r, 1 << j);
+    r = kMax ? fmaxf(r, o) : r + o;
+  }
+  return r;
+}
+
+// CW consecutive columns of this thread's lane, starting at `taddr`.
+template <int CW>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[CW]) {
+  if constexpr (CW == 8) {
+    tmem_ld8(taddr, v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < CW / 16; ++c) tmem_ld16(taddr + c * 16, *reinterpret_cast<float(*)[16]>(&v[c * 16]));
+  }
+  tmem_wait_ld_regs<CW>(v);
+}
+template <int CW>
+__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)[CW]) {
+  if constexpr (CW == 8) {
+    tmem_st8(taddr, v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < CW / 16; ++c) tmem_st16(taddr + c * 16, *reinterpret_cast<const float(*)[16]>(&v[c * 16]));
+  }
+  tmem_wait_st();
+}
+
+template <int MT, int S, int NP>
+__global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kernel(
+    const Params p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v) {
   using C = Cfg<MT>;
-  constexpr int N = C::N;
+  constexpr int N = C::N, CW = C::CW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
   uint8_t* qbuf = ring + S * C::STAGE_BYTES;
-  uint8_t* pbuf = qbuf + S * C::Q_BYTES;  // P_hi then P_lo
-  uint64_t* full = reinterpret_cast<uint64_t*>(pbuf + 2 * C::P_BYTES);
-  uint64_t* empty = full + S;
-  uint64_t* s_full = empty + S;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* fin_bar = p_full + 1;
-  float* s_red = reinterpret_cast<float*>(full + 64);  // [4][64] cross-warp reductions
-  float* s_mrun = s_red + 4 * 64;                      // [64] running row max
-  int32_t* s_bad = reinterpret_cast<int32_t*>(s_mrun + 64);  // [4]
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bad + 4);  // tensor-memory base
-  int32_t* s_prefix = reinterpret_cast<int32_t*>(s_tmem + 4);
+  uint8_t* pbuf = qbuf + S * C::Q_BYTES;  // NP x (P_hi, P_lo)
+  // K and V of a stage arrive and are released separately: K is free once QK is
+  // done, a tile earlier than V, so the producer can fetch the next K sooner.
+  uint64_t* full_k = reinterpret_cast<uint64_t*>(pbuf + NP * 2 * C::P_BYTES);
+  uint64_t* full_v = full_k + S;
+  uint64_t* empty_k = full_v + S;
+  uint64_t* empty_v = empty_k + S;
+  uint64_t* s_full = empty_v + S;   // [2]: S^T buffer b holds QK of the tile
+  uint64_t* p_full = s_full + 2;  // [2]: P of tile i written (one arrival per softmax warp)
+  uint64_t* pv_done = p_full + 2; // [NP]: P.V of the tile that used P buffer j is complete
+  uint64_t* fin_bar = pv_done + NP;
+  float* s_red = reinterpret_cast<float*>(full_k + 64);   // [4][64] per-quarter row reductions
+  float* s_mrun = s_red + 4 * 64;                         // [64] running row max (64-row tiles)
+  int64_t* s_rowoff = reinterpret_cast<int64_t*>(s_mrun + 64);  // [64] output offset of each row
+  int32_t* s_bad = reinterpret_cast<int32_t*>(s_rowoff + 64);  // [4]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bad + 4);   // tensor-memory base
+  int32_t* s_prefix = reinterpret_cast<int32_t*>(s_bad + 16);
   int32_t* s_ctx = s_prefix + ((p.batch + 2 + 63) & ~63);
   int32_t* s_misc = s_ctx + ((p.batch + 63) & ~63);
 
@@ -769,11 +837,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attention_tc_kernel(const 
     }
     if (tid == 0) {
       for (int s = 0; s < S; ++s) {
-        mbar_init(&full[s], 1);
-        mbar_init(&empty[s], 1);
+        mbar_init(&full_k[s], 1);
+        mbar_init(&full_v[s], 1);
+        mbar_init(&empty_k[s], 1);
+        mbar_init(&empty_v[s], 1);
       }
-      mbar_init(s_full, 1);
-      mbar_init(p_full, kSoftmaxWarps);
+      for (int j = 0; j < 2; ++j) {
+        mbar_init(&s_full[j], 1);
+        mbar_init(&p_full[j], kSoftmaxWarps);
+      }
+      for (int j = 0; j < NP; ++j) mbar_init(&pv_done[j], 1);
       mbar_init(fin_bar, 1);
       fence_mbar_init();
     }
@@ -791,8 +864,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attention_tc_kernel(const 
   const int64_t f0 = (int64_t)blockIdx.x * W;
   const int64_t f1 = min(T, f0 + W);
   if (f0 >= f1) return;
+  const int n_tiles = (int)(f1 - f0);
 
-  // tensor memory: allocated by the MMA warp, address broadcast through shared memory
   if (warp == 1) {
     tmem_alloc(smem_u32(s_tmem), kTmemCols);
     tmem_relinquish();
@@ -810,118 +883,154 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attention_tc_kernel(const 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  const uint32_t tmem_s = tmem, tmem_o = tmem + 64;
+  const uint32_t tmem_o = tmem + 2 * N;
   const uint32_t ring_u32 = smem_u32(ring), q_u32 = smem_u32(qbuf), p_u32 = smem_u32(pbuf);
 
   if (warp == 0) {
     // =================== producer: TMA, S stages ahead ===================
+    // Iteration j loads K (and the unit's queries) of tile j once QK of tile j-S is
+    // done, then V of tile j-1 once P.V of tile j-1-S is done.
     const int bs = 1 << p.block_shift;
     const int BH = bs < TK ? bs : TK;
     const int pieces = TK / BH;
     Cursor ld = cursor_at(f0, s_prefix, B, Hkv);
     bool fresh = true;
     int win_b = -1, win_base = 0, win_val = 0;
-    for (int64_t f = f0; f < f1; ++f) {
-      const int s = (int)((f - f0) % S);
-      const int64_t rnd = (f - f0) / S;
-      const int b = ld.b, g = ld.g;
-      const int ctx = s_ctx[b];
-      const int t0 = ld.tile * TK;
-      const int slot = ld.seq % S;
-      int zc[TK / 16];
-      bool bad = false;
+    int zc[TK / 16] = {}, zprev[TK / 16] = {};
+    int g_prev = 0;
+    for (int j = 0; j <= n_tiles; ++j) {
 #pragma unroll
-      for (int pc = 0; pc < TK / 16; ++pc) {
-        if (pc >= pieces) break;
-        const int t = t0 + pc * BH;
-        int z = -BH;
-        if (t < ctx) {
-          const int n = t >> p.block_shift;
-          if (b != win_b || n < win_base || n >= win_base + 32) {
-            win_b = b;
-            win_base = n;
-            const int nb = (ctx + bs - 1) >> p.block_shift;
-            win_val = (n + lane < nb) ? __ldg(p.block_table + (int64_t)b * p.max_blocks + n + lane) : 0;
+      for (int pc = 0; pc < TK / 16; ++pc) zprev[pc] = zc[pc];
+      const int g = ld.g;
+      if (j < n_tiles) {
+        const int b = ld.b;
+        const int ctx = s_ctx[b];
+        const int t0 = ld.tile * TK;
+        const int slot = ld.seq % S;
+        const int s = j % S;
+        bool bad = false;
+#pragma unroll
+        for (int pc = 0; pc < TK / 16; ++pc) {
+          if (pc >= pieces) break;
+          const int t = t0 + pc * BH;
+          int z = -BH;
+          if (t < ctx) {
+            const int n = t >> p.block_shift;
+            if (b != win_b || n < win_base || n >= win_base + 32) {
+              win_b = b;
+              win_base = n;
+              const int nb = (ctx + bs - 1) >> p.block_shift;
+              win_val = (n + lane < nb) ? __ldg(p.block_table + (int64_t)b * p.max_blocks + n + lane) : 0;
+            }
+            const int32_t phys = __shfl_sync(0xffffffffu, win_val, n - win_base);
+            if (phys < 0 || (int64_t)phys >= p.num_blocks) bad = true;
+            else z = (int)(((int64_t)phys << p.block_shift) + (t & (bs - 1)));
           }
-          const int32_t phys = __shfl_sync(0xffffffffu, win_val, n - win_base);
-          if (phys < 0 || (int64_t)phys >= p.num_blocks) bad = true;
-          else z = (int)(((int64_t)phys << p.block_shift) + (t & (bs - 1)));
+          zc[pc] = z;
         }
-        zc[pc] = z;
+        if (lane == 0) {
+          if (j >= S && !mbar_wait_bounded(&empty_k[s], (uint32_t)(((j - S) / S) & 1)))
+            raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+          if (fresh) s_bad[slot] = 0;
+          if (bad) s_bad[slot] = 1;
+          const uint32_t q_bytes = fresh ? (uint32_t)(R * G * D * 2) : 0u;
+          mbar_arrive_expect_tx(&full_k[s], (uint32_t)C::TILE_BYTES + q_bytes);
+          if (fresh) {
+            const uint32_t qdst = q_u32 + slot * C::Q_BYTES;
+            tma_load_3d(qdst, &tm_q, 0, g * G, b * R, &full_k[s]);
+            tma_load_3d(qdst + N * 128, &tm_q, 64, g * G, b * R, &full_k[s]);
+          }
+          const uint32_t kdst = ring_u32 + s * C::STAGE_BYTES;
+#pragma unroll
+          for (int pc = 0; pc < TK / 16; ++pc) {
+            if (pc >= pieces) break;
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub)
+              tma_load_3d(kdst + sub * TK * 128 + pc * BH * 128, &tm_k, sub * 64, g, zc[pc], &full_k[s]);
+          }
+        }
       }
-      if (lane == 0) {
-        if (rnd > 0 && !mbar_wait_bounded(&empty[s], (uint32_t)((rnd - 1) & 1)))
+      if (j >= 1 && lane == 0) {
+        const int jv = j - 1, s = jv % S;
+        if (jv >= S && !mbar_wait_bounded(&empty_v[s], (uint32_t)(((jv - S) / S) & 1)))
           raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
-        if (fresh) s_bad[slot] = 0;
-        if (bad) s_bad[slot] = 1;
-        const uint32_t q_bytes = fresh ? (uint32_t)(R * G * D * 2) : 0u;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)C::STAGE_BYTES + q_bytes);
-        if (fresh) {
-          const uint32_t qdst = q_u32 + slot * C::Q_BYTES;
-          tma_load_3d(qdst, &tm_q, 0, g * G, b * R, &full[s]);
-          tma_load_3d(qdst + N * 128, &tm_q, 64, g * G, b * R, &full[s]);
-        }
-        const uint32_t kdst = ring_u32 + s * C::STAGE_BYTES;
-        const uint32_t vdst = kdst + C::TILE_BYTES;
+        mbar_arrive_expect_tx(&full_v[s], (uint32_t)C::TILE_BYTES);
+        const uint32_t vdst = ring_u32 + s * C::STAGE_BYTES + C::TILE_BYTES;
 #pragma unroll
         for (int pc = 0; pc < TK / 16; ++pc) {
           if (pc >= pieces) break;
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
-            const uint32_t off = sub * TK * 128 + pc * BH * 128;
-            tma_load_3d(kdst + off, &tm_k, sub * 64, g, zc[pc], &full[s]);
-            tma_load_3d(vdst + off, &tm_v, sub * 64, g, zc[pc], &full[s]);
-          }
+          for (int sub = 0; sub < 2; ++sub)
+            tma_load_3d(vdst + sub * TK * 128 + pc * BH * 128, &tm_v, sub * 64, g_prev, zprev[pc], &full_v[s]);
         }
       }
       __syncwarp();
-      const int before = ld.seq;
-      cursor_advance(ld, s_prefix, B, Hkv);
-      fresh = ld.seq != before;
+      g_prev = g;
+      if (j < n_tiles) {
+        const int before = ld.seq;
+        cursor_advance(ld, s_prefix, B, Hkv);
+        fresh = ld.seq != before;
+      }
     }
     return;
   }
 
   if (warp == 1) {
     // =================== MMA issuer (one thread) ===================
+    // QK of tile i+1 is issued before P.V of tile i, so it runs while the softmax
+    // warps work on tile i. Descriptors differ only in their start address, so each
+    // one is a precomputed base plus the operand's address / 16.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(128, N, 0, 0);
       constexpr uint32_t idesc_pv = umma_idesc_bf16(128, N, 1, 0);
-      Cursor cu = cursor_at(f0, s_prefix, B, Hkv);
-      bool fresh = true;
-      for (int64_t f = f0; f < f1; ++f) {
-        const int64_t i = f - f0;
-        const int s = (int)(i % S);
-        if (!mbar_wait_bounded(&full[s], (uint32_t)((i / S) & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+      const uint64_t kmaj = smem_desc_sw128(0, 16, 1024);          // K, Q, P: K-major
+      const uint64_t vmn = smem_desc_sw128(0, TK * 128, 1024);     // V: MN-major
+      Cursor cq = cursor_at(f0, s_prefix, B, Hkv);  // next tile to multiply by Q
+      bool pv_fresh = true;                          // tile i starts a unit (for P.V)
+      int q_seq = 0;
+      auto issue_qk = [&](int i) {
+        const int s = i % S;
+        if (!mbar_wait_bounded(&full_k[s], (uint32_t)((i / S) & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
         tc_fence_after();
-        const uint32_t kb = ring_u32 + s * C::STAGE_BYTES;
-        const uint32_t vb = kb + C::TILE_BYTES;
-        const uint32_t qb = q_u32 + (cu.seq % S) * C::Q_BYTES;
+        const uint32_t kb = (ring_u32 + s * C::STAGE_BYTES) >> 4;
+        const uint32_t qb = (q_u32 + (q_seq % S) * C::Q_BYTES) >> 4;
+        const uint32_t dst = tmem + (uint32_t)((i & 1) * N);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = (ks & 3) * 32;
-          const uint64_t ad = smem_desc_sw128(kb + (ks >> 2) * TK * 128 + koff, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(qb + (ks >> 2) * N * 128 + koff, 16, 1024);
-          umma_bf16(tmem_s, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+          const uint32_t off = ((ks >> 2) * TK * 128 + (ks & 3) * 32) >> 4;
+          const uint32_t qoff = ((ks >> 2) * N * 128 + (ks & 3) * 32) >> 4;
+          umma_bf16(dst, kmaj + kb + off, kmaj + qb + qoff, idesc_qk, ks > 0 ? 1u : 0u);
         }
-        umma_commit(s_full);
-        if (!mbar_wait_bounded(p_full, (uint32_t)(i & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+        umma_commit(&s_full[i & 1]);
+        umma_commit(&empty_k[s]);  // K of the stage can be refilled
+        cursor_advance(cq, s_prefix, B, Hkv);
+        q_seq = cq.seq;
+      };
+      issue_qk(0);
+      Cursor cpv = cursor_at(f0, s_prefix, B, Hkv);
+      for (int i = 0; i < n_tiles; ++i) {
+        if (i + 1 < n_tiles) issue_qk(i + 1);
+        if (!mbar_wait_bounded(&p_full[i & 1], (uint32_t)((i >> 1) & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+        if (!mbar_wait_bounded(&full_v[i % S], (uint32_t)((i / S) & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
         tc_fence_after();
+        const uint32_t vb = (ring_u32 + (i % S) * C::STAGE_BYTES + C::TILE_BYTES) >> 4;
+        const uint32_t pb = (p_u32 + (i % NP) * 2 * C::P_BYTES) >> 4;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
-          const uint32_t pb = p_u32 + part * C::P_BYTES;
 #pragma unroll
           for (int kk = 0; kk < TK / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(vb + kk * 2048, TK * 128, 1024);
-            const uint64_t bd = smem_desc_sw128(pb + (kk >> 2) * N * 128 + (kk & 3) * 32, 16, 1024);
-            umma_bf16(tmem_o, ad, bd, idesc_pv, (fresh && part == 0 && kk == 0) ? 0u : 1u);
+            const uint32_t voff = (kk * 2048) >> 4;
+            const uint32_t poff = (part * C::P_BYTES + (kk >> 2) * N * 128 + (kk & 3) * 32) >> 4;
+            umma_bf16(tmem_o, vmn + vb + voff, kmaj + pb + poff, idesc_pv,
+                      (pv_fresh && part == 0 && kk == 0) ? 0u : 1u);
           }
         }
-        umma_commit(&empty[s]);  // the stage (and P) is free once these MMAs are done
-        if (f == f1 - 1) umma_commit(fin_bar);
-        const int before = cu.seq;
-        cursor_advance(cu, s_prefix, B, Hkv);
-        fresh = cu.seq != before;
+        umma_commit(&pv_done[i % NP]);  // P buffer free, O^T holds tiles <= i
+        umma_commit(&empty_v[i % S]);   // V of the stage can be refilled
+        if (i == n_tiles - 1) umma_commit(fin_bar);
+        const int before = cpv.seq;
+        cursor_advance(cpv, s_prefix, B, Hkv);
+        pv_fresh = cpv.seq != before;
       }
     }
     __syncwarp();
@@ -932,114 +1041,160 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attention_tc_kernel(const 
   }
 
   // =================== softmax / epilogue warps ===================
-  const int q4 = warp & 3;            // tensor-memory lane quarter of this warp
-  const int st = tid - 64;            // 0..127
+  const int sw = warp - 2;             // 0..7
+  const int h = sw >> 2;               // warpgroup: rows [h*CW, h*CW + CW)
+  const int c0 = h * CW;
+  const int q4 = warp & 3;             // tensor-memory lane quarter of this warp
+  const int gt = tid - 64 - h * 128;   // thread index inside the warpgroup
+  const int st = tid - 64;             // thread index over all softmax warps
   const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
   const int key_in_tile = q4 * 32 + lane;  // the S^T lane this thread reads
-  float l_part[N];
+  const int bar_group = kBarGroup0 + h;
+  // Running row max: registers, or shared memory for 64-row tiles (register budget);
+  // every thread of a warpgroup holds the same values for its rows.
+  constexpr bool kMaxInSmem = CW >= 32;
+  float l_part[CW], m_reg[kMaxInSmem ? 1 : CW];
 #pragma unroll
-  for (int r = 0; r < N; ++r) l_part[r] = 0.f;
+  for (int e = 0; e < CW; ++e) l_part[e] = 0.f;
+#pragma unroll
+  for (int e = 0; e < (kMaxInSmem ? 1 : CW); ++e) m_reg[e] = -INFINITY;
+  auto m_get = [&](int e) -> float { return kMaxInSmem ? s_mrun[c0 + e] : m_reg[kMaxInSmem ? 0 : e]; };
   Cursor cu = cursor_at(f0, s_prefix, B, Hkv);
   bool cu_fresh = true, from_zero = true, pending = false, fin_bad = false;
   Fin fin;
   int ctx = 0, prefix_len = 0;
 
+  // Wait until P.V of tile j (local index) is complete.
+  auto wait_pv = [&](int j) {
+    const uint32_t parity = (uint32_t)((NP == 2 ? (j >> 1) : j) & 1);
+    if (!mbar_wait_bounded(&pv_done[j % NP], parity) && st == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+    tc_fence_after();
+  };
+
   // Write the finished unit piece: output rows (whole unit) or a normalised partial.
+  // A unit split over several CTAs is merged by the last one to finish its piece.
   auto epilogue = [&](const Fin& F) {
-    // row sums over all 128 key lanes
-#pragma unroll
-    for (int r = 0; r < N; ++r) {
-      float v = l_part[r];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) s_red[q4 * 64 + r] = v;
+    {
+      const float lsum = reduce_cols<CW, false>(l_part, lane);  // l_part is reset after this
+      if (lane < CW) s_red[q4 * 64 + c0 + reduced_col<CW>(lane)] = lsum;
     }
-    const bool bad = named_sync_or(kBarSoftmax, kSoftmaxThreads, fin_bad);
+    if (F.complete && gt < CW && c0 + gt < p.n_rows) {
+      const int r = c0 + gt, i = r / G, j = r - i * G;
+      s_rowoff[r] = (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
+    }
+    named_sync(bar_group, 128);
+    const bool bad = fin_bad;
     const int d = q4 * 32 + lane;  // the O^T lane this thread reads
+    constexpr int CH = CW < 16 ? CW : 16;  // columns per step
 #pragma unroll
-    for (int c = 0; c < N / 16; ++c) {
-      float ov[16];
-      tmem_ld16(tmem_o + lane_off + c * 16, ov);
-      tmem_wait_ld();
+    for (int c = 0; c < CW; c += CH) {
+      float inv[CH];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int r = c * 16 + e;
+      for (int e = 0; e < CH; ++e) {
+        const int r = c0 + c + e;
+        const float L = s_red[r] + s_red[64 + r] + s_red[128 + r] + s_red[192 + r];
+        inv[e] = (L > 0.f && !bad) ? 1.f / L : 0.f;
+        if (!F.complete && q4 == 0 && lane == 0 && r < p.n_rows) {
+          float lse2 = L > 0.f ? m_get(c + e) + __log2f(L) : -INFINITY;
+          if (bad) lse2 = __int_as_float(0x7fc00000);
+          __stcg(p.lse + (int64_t)F.slot * p.n_rows + r, lse2);
+        }
+      }
+      float ov[CH];
+      tmem_load_cols<CH>(tmem_o + lane_off + c0 + c, ov);
+#pragma unroll
+      for (int e = 0; e < CH; ++e) {
+        const int r = c0 + c + e;
         if (r < p.n_rows) {
-          const float L = s_red[r] + s_red[64 + r] + s_red[128 + r] + s_red[192 + r];
-          const float M = s_mrun[r];
-          const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
-          float* dst;
-          if (F.complete) {
-            const int i = r / G, j = r - i * G;
-            dst = p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
-          } else {
-            dst = p.opart + ((int64_t)F.slot * p.n_rows + r) * D;
-            if (d == 0) {
-              float lse2 = L > 0.f ? M + __log2f(L) : -INFINITY;
-              if (bad) lse2 = __int_as_float(0x7fc00000);
-              p.lse[(int64_t)F.slot * p.n_rows + r] = lse2;
-            }
-          }
-          dst[d] = ov[e] * inv;
+          const int64_t off = F.complete ? s_rowoff[r] : ((int64_t)F.slot * p.n_rows + r) * D;
+          __stcg((F.complete ? p.out : p.opart) + off + d, ov[e] * inv[e]);
         }
       }
     }
     if (bad && st == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
     if (!F.complete) {
-      __threadfence();
+      // release: every partial store of the CTA is ordered before the arrival
       named_sync(kBarSoftmax, kSoftmaxThreads);
       const int unit = F.b * Hkv + F.g;
-      if (st == 0) s_misc[8] = (atomicAdd(p.counters + unit, 1) == F.nseg - 1) ? 1 : 0;
+      if (st == 0) {
+        __threadfence();
+        const int last = atomicAdd(p.counters + unit, 1) == F.nseg - 1;
+        if (last) __threadfence();  // acquire: the other pieces are visible
+        s_misc[8] = last;
+      }
       named_sync(kBarSoftmax, kSoftmaxThreads);
       if (s_misc[8]) {
-        __threadfence();
-        for (int idx = st; idx < p.n_rows * (D / 4); idx += kSoftmaxThreads) {
-          const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+        // per-row max and 1 / (sum of weights) over the pieces' log-sum-exp
+        if (st < p.n_rows) {
+          const int r = st;
           float Mx = -INFINITY;
           bool nan = false;
+#pragma unroll 4
           for (int sg = 0; sg < F.nseg; ++sg) {
-            const int slot = piece_slot(F.c0 + sg, F.c0, F.u0, W);
-            const float l = __ldcg(p.lse + (int64_t)slot * p.n_rows + r);
+            const float l = __ldcg(p.lse + (int64_t)piece_slot(F.c0 + sg, F.c0, F.u0, W) * p.n_rows + r);
             nan |= l != l;
             Mx = fmaxf(Mx, l);
           }
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (!nan && Mx != -INFINITY) {
-            float wsum = 0.f;
-            for (int sg = 0; sg < F.nseg; ++sg) {
-              const int slot = piece_slot(F.c0 + sg, F.c0, F.u0, W);
-              const float wgt = exp2f(__ldcg(p.lse + (int64_t)slot * p.n_rows + r) - Mx);
-              if (wgt > 0.f) {
-                const float4 v =
-                    __ldcg(reinterpret_cast<const float4*>(p.opart + ((int64_t)slot * p.n_rows + r) * D) + d4);
-                acc.x += wgt * v.x;
-                acc.y += wgt * v.y;
-                acc.z += wgt * v.z;
-                acc.w += wgt * v.w;
-              }
-              wsum += wgt;
-            }
-            const float inv = 1.f / wsum;
-            acc.x *= inv;
-            acc.y *= inv;
-            acc.z *= inv;
-            acc.w *= inv;
-          }
+          float wsum = 0.f;
+#pragma unroll 4
+          for (int sg = 0; sg < F.nseg; ++sg)
+            wsum += exp2f(__ldcg(p.lse + (int64_t)piece_slot(F.c0 + sg, F.c0, F.u0, W) * p.n_rows + r) - Mx);
+          const bool zero = nan || Mx == -INFINITY;
+          s_red[r] = zero ? 0.f : Mx;
+          s_red[64 + r] = zero ? 0.f : 1.f / wsum;
           const int i = r / G, j = r - i * G;
-          reinterpret_cast<float4*>(p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D)[d4] = acc;
+          s_rowoff[r] = (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
+        }
+        named_sync(kBarSoftmax, kSoftmaxThreads);
+        // out[row] = sum over pieces of weight * partial. A thread owns float4
+        // columns idx = st + k * 256 and, per piece, loads those of kItems items at
+        // once, so one pass costs about one L2 round trip per piece.
+        constexpr int kItems = 4;
+        for (int base = st; base < p.n_rows * (D / 4); base += kItems * kSoftmaxThreads) {
+          float4 acc[kItems];
+#pragma unroll
+          for (int k = 0; k < kItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int sg = 0; sg < F.nseg; ++sg) {
+            const int64_t slot = piece_slot(F.c0 + sg, F.c0, F.u0, W);
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+              const int idx = base + k * kSoftmaxThreads;
+              if (idx < p.n_rows * (D / 4)) {
+                const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+                const float wgt = exp2f(__ldcg(p.lse + slot * p.n_rows + r) - s_red[r]);
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(p.opart + (slot * p.n_rows + r) * D) + d4);
+                acc[k].x += wgt * v.x;
+                acc[k].y += wgt * v.y;
+                acc[k].z += wgt * v.z;
+                acc[k].w += wgt * v.w;
+              }
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < kItems; ++k) {
+            const int idx = base + k * kSoftmaxThreads;
+            if (idx < p.n_rows * (D / 4)) {
+              const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+              const float sc = s_red[64 + r];  // 0: a piece is invalid or the row saw no key
+              const float4 o = sc == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                         : make_float4(acc[k].x * sc, acc[k].y * sc, acc[k].z * sc, acc[k].w * sc);
+              __stcg(reinterpret_cast<float4*>(p.out + s_rowoff[r]) + d4, o);
+            }
+          }
         }
         if (st == 0) p.counters[unit] = 0;
       }
     }
-    named_sync(kBarSoftmax, kSoftmaxThreads);  // s_red / s_mrun are reused
+    named_sync(kBarSoftmax, kSoftmaxThreads);  // s_red, s_rowoff and s_misc are reused
   };
 
-  for (int64_t f = f0; f < f1; ++f) {
-    const int64_t i = f - f0;
-    const int stage = (int)(i % S);
-    if (!mbar_wait_bounded(s_full, (uint32_t)(i & 1)) && st == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+  for (int i = 0; i < n_tiles; ++i) {
+    const int stage = i % S;
+    if (!mbar_wait_bounded(&s_full[i & 1], (uint32_t)((i >> 1) & 1)) && st == 0)
+      raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
     tc_fence_after();
-    if (pending) {  // every MMA of the previous unit is complete: write it out
+    if (pending) {  // the previous unit ended with tile i-1: write it out
+      wait_pv(i - 1);
       epilogue(fin);
       pending = false;
     }
@@ -1048,77 +1203,78 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attention_tc_kernel(const 
       ctx = s_ctx[cu.b];
       prefix_len = ctx - R;
 #pragma unroll
-      for (int r = 0; r < N; ++r) l_part[r] = 0.f;
-      if (st < N) s_mrun[st] = -INFINITY;
-      named_sync(kBarSoftmax, kSoftmaxThreads);
+      for (int e = 0; e < CW; ++e) l_part[e] = 0.f;
+      if constexpr (kMaxInSmem) {
+        if (gt < CW) s_mrun[c0 + gt] = -INFINITY;
+        named_sync(bar_group, 128);
+      } else {
+#pragma unroll
+        for (int e = 0; e < CW; ++e) m_reg[kMaxInSmem ? 0 : e] = -INFINITY;
+      }
     }
     const int t0 = cu.tile * TK;
     const int tkey = t0 + key_in_tile;
     // row r sees this key iff r >= rmin (rows of draft position i see keys <= prefix_len + i)
     const int rmin = tkey >= ctx ? (1 << 30) : (tkey > prefix_len ? (tkey - prefix_len) * G : 0);
-    // ---- pass 1: does any score exceed its row's running max by more than 8?
+    const bool edge = t0 + TK - 1 > prefix_len;  // the tile holds keys some rows must not see
+    float x[CW];
+    tmem_load_cols<CW>(tmem + (uint32_t)((i & 1) * N) + lane_off + c0, x);
     bool grow = false;
 #pragma unroll
-    for (int c = 0; c < N / 16; ++c) {
-      float sv[16];
-      tmem_ld16(tmem_s + lane_off + c * 16, sv);
-      tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int r = c * 16 + e;
-        const float x = r < rmin ? -INFINITY : sv[e] * p.scale_log2;
-        grow |= x > s_mrun[r] + 8.f;
-      }
+    for (int e = 0; e < CW; ++e) {
+      x[e] *= p.scale_log2;
+      if (edge && c0 + e < rmin) x[e] = -INFINITY;
+      grow |= x[e] > m_get(e) + 8.f;
     }
-    if (named_sync_or(kBarSoftmax, kSoftmaxThreads, grow)) {
+    if (named_sync_or(bar_group, 128, grow)) {
       // ---- slow path: exact tile max per row, rescale O^T and the row sums
+      {
+        float tmp[CW];
 #pragma unroll
-      for (int c = 0; c < N / 16; ++c) {
-        float sv[16];
-        tmem_ld16(tmem_s + lane_off + c * 16, sv);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int r = c * 16 + e;
-          float x = r < rmin ? -INFINITY : sv[e] * p.scale_log2;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-          if (lane == 0) s_red[q4 * 64 + r] = x;
-        }
+        for (int e = 0; e < CW; ++e) tmp[e] = x[e];
+        const float mx = reduce_cols<CW, true>(tmp, lane);
+        if (lane < CW) s_red[q4 * 64 + c0 + reduced_col<CW>(lane)] = mx;
       }
-      named_sync(kBarSoftmax, kSoftmaxThreads);
-      const bool rescale_o = !cu_fresh;  // O^T holds earlier tiles of this unit
+      named_sync(bar_group, 128);
+      // O^T holds earlier tiles of this unit unless the unit starts here: wait for the
+      // last P.V before rescaling it
+      if (!cu_fresh) wait_pv(i - 1);
+      constexpr int CH = CW < 16 ? CW : 16;  // columns rescaled per step
 #pragma unroll
-      for (int c = 0; c < N / 16; ++c) {
-        float alpha[16];
+      for (int c = 0; c < CW; c += CH) {
+        float alpha[CH];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int r = c * 16 + e;
+        for (int e = 0; e < CH; ++e) {
+          const int r = c0 + c + e;
           const float tm = fmaxf(fmaxf(s_red[r], s_red[64 + r]), fmaxf(s_red[128 + r], s_red[192 + r]));
-          const float mo = s_mrun[r];
+          const float mo = m_get(c + e);
           const float mn = fmaxf(mo, tm);
-          alpha[e] = (mo == -INFINITY || mn == -INFINITY) ? (mo == -INFINITY ? 0.f : 1.f) : fast_exp2(mo - mn);
-          l_part[r] *= alpha[e];
+          alpha[e] = mo == -INFINITY ? 0.f : fast_exp2(mo - mn);
+          l_part[c + e] *= alpha[e];
+          if constexpr (!kMaxInSmem) m_reg[kMaxInSmem ? 0 : c + e] = mn;
         }
-        if (rescale_o) {
-          float ov[16];
-          tmem_ld16(tmem_o + lane_off + c * 16, ov);
-          tmem_wait_ld();
+        if (!cu_fresh) {
+          float ov[CH];
+          tmem_load_cols<CH>(tmem_o + lane_off + c0 + c, ov);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ov[e] *= alpha[e];
-          tmem_st16(tmem_o + lane_off + c * 16, ov);
+          for (int e = 0; e < CH; ++e) ov[e] *= alpha[e];
+          tmem_store_cols<CH>(tmem_o + lane_off + c0 + c, ov);
         }
       }
-      if (rescale_o) tmem_wait_st();
-      named_sync(kBarSoftmax, kSoftmaxThreads);  // everyone has read the old running max
-      if (st < N) {
-        const float tm = fmaxf(fmaxf(s_red[st], s_red[64 + st]), fmaxf(s_red[128 + st], s_red[192 + st]));
-        s_mrun[st] = fmaxf(s_mrun[st], tm);
+      if constexpr (kMaxInSmem) {
+        named_sync(bar_group, 128);  // every thread has read the old maxima
+        if (gt < CW) {
+          const int r = c0 + gt;
+          const float tm = fmaxf(fmaxf(s_red[r], s_red[64 + r]), fmaxf(s_red[128 + r], s_red[192 + r]));
+          s_mrun[r] = fmaxf(s_mrun[r], tm);
+        }
       }
-      named_sync(kBarSoftmax, kSoftmaxThreads);
+      named_sync(bar_group, 128);  // s_red is reused; new maxima visible
     }
     // ---- keys past the context in the last tile may hold stale bytes: zero those V rows
     if (t0 + TK > ctx) {
+      if (!mbar_wait_bounded(&full_v[stage], (uint32_t)((i / S) & 1)) && st == 0)
+        raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);  // V of this tile has landed
       const int valid = ctx - t0;
       uint8_t* vt = ring + stage * C::STAGE_BYTES + C::TILE_BYTES;
       for (int j = st; j < (TK - valid) * 16; j += kSoftmaxThreads) {
@@ -1127,45 +1283,40 @@ __global__ void __launch_bounds__(kThreads, 1) verify_attention_tc_kernel(const 
             make_uint4(0, 0, 0, 0);
       }
     }
-    // ---- pass 2: P = exp2(x - m) as bf16 hi + lo, written K-major [N rows][128 keys]
+    // ---- P = exp2(x - m), row sums
+#pragma unroll
+    for (int e = 0; e < CW; ++e) {
+      const float m = m_get(e);
+      x[e] = fast_exp2(x[e] - (m == -INFINITY ? 0.f : m));
+      l_part[e] += x[e];
+    }
+    // the P buffer is free once the P.V that last read it is done
+    if (i >= NP) wait_pv(i - NP);
+    // ---- store P as bf16 hi + lo, K-major [N rows][128 keys]; lanes (2j, 2j+1) pair up so
+    // that each 32-bit store holds two adjacent keys of one row
+    uint8_t* pb = pbuf + (i % NP) * 2 * C::P_BYTES;
     const int kk = key_in_tile;
     const uint32_t psub = (uint32_t)(kk >> 6) * N * 128;
+    const bool even = (lane & 1) == 0;
 #pragma unroll
-    for (int c = 0; c < N / 16; ++c) {
-      float sv[16];
-      tmem_ld16(tmem_s + lane_off + c * 16, sv);
-      tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < 16; e += 2) {
-        float pv[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = c * 16 + e + h;
-          const float x = r < rmin ? -INFINITY : sv[e + h] * p.scale_log2;
-          const float m = s_mrun[r];
-          pv[h] = fast_exp2(x - (m == -INFINITY ? 0.f : m));
-          l_part[r] += pv[h];
-        }
-        // lanes (2i, 2i+1): the even lane stores row r for both keys, the odd lane row r+1
-        const float o0 = __shfl_xor_sync(0xffffffffu, pv[0], 1);
-        const float o1 = __shfl_xor_sync(0xffffffffu, pv[1], 1);
-        const bool even = (lane & 1) == 0;
-        const int r = c * 16 + e + (even ? 0 : 1);
-        const float a = even ? pv[0] : o1;   // key kk & ~1
-        const float bb = even ? o0 : pv[1];  // key kk | 1
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, bb);
-        const float2 hf = __bfloat1622float2(h2);
-        const uint32_t lo = pack_bf16(a - hf.x, bb - hf.y);
-        const uint32_t off = psub + r * 128 + ((((kk & 63) >> 3) ^ (r & 7)) << 4) + ((kk & 6) << 1);
-        *reinterpret_cast<__nv_bfloat162*>(pbuf + off) = h2;
-        *reinterpret_cast<uint32_t*>(pbuf + C::P_BYTES + off) = lo;
-      }
+    for (int e = 0; e < CW; e += 2) {
+      const float o0 = __shfl_xor_sync(0xffffffffu, x[e], 1);
+      const float o1 = __shfl_xor_sync(0xffffffffu, x[e + 1], 1);
+      const int r = c0 + e + (even ? 0 : 1);
+      const float a = even ? x[e] : o1;       // key kk & ~1
+      const float bb = even ? o0 : x[e + 1];  // key kk | 1
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, bb);
+      const float2 hf = __bfloat1622float2(h2);
+      const uint32_t lo = pack_bf16(a - hf.x, bb - hf.y);
+      const uint32_t off = psub + r * 128 + ((((kk & 63) >> 3) ^ (r & 7)) << 4) + ((kk & 6) << 1);
+      *reinterpret_cast<__nv_bfloat162*>(pb + off) = h2;
+      *reinterpret_cast<uint32_t*>(pb + C::P_BYTES + off) = lo;
     }
     fence_proxy_async_smem();  // P and zeroed V rows are read by the tensor core
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(p_full);
-    if (f == f1 - 1 || cu.tile == cu.ntiles - 1) {
+    if (lane == 0) mbar_arrive(&p_full[i & 1]);
+    if (i == n_tiles - 1 || cu.tile == cu.ntiles - 1) {
       const int64_t u0 = (int64_t)s_prefix[cu.b] * Hkv + (int64_t)cu.g * cu.ntiles;
       fin.b = cu.b;
       fin.g = cu.g;
@@ -1297,11 +1448,11 @@ static int launch_main_d(const Params& p, int mt, const CUtensorMap& tq, const C
 }
 
 // The tcgen05 kernel: one CTA per SM (its grid never exceeds the mma.sync kernel's).
-template <int MT, int S>
+template <int MT, int S, int NP>
 static int launch_tc(const Params& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      cudaStream_t stream) {
-  auto kern = tc::verify_attention_tc_kernel<MT, S>;
-  const size_t smem = tc::smem_bytes<MT, S>(p.batch);
+  auto kern = tc::verify_attention_tc_kernel<MT, S, NP>;
+  const size_t smem = tc::smem_bytes<MT, S, NP>(p.batch);
   static int cached_dev = -1, cached_grid = 0;
   static size_t cached_smem = 0;
   int dev = 0;
@@ -1334,11 +1485,12 @@ static Kernel choose_kernel(int D, int mt, int batch, int* stages) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return Kernel::kMma;
+  // stages x P buffers per row count, most overlap first
   size_t need3 = SIZE_MAX, need2 = SIZE_MAX;
   switch (mt) {
-    case 1: need3 = tc::smem_bytes<1, 3>(batch); need2 = tc::smem_bytes<1, 2>(batch); break;
-    case 2: need2 = tc::smem_bytes<2, 2>(batch); break;
-    default: need2 = tc::smem_bytes<4, 2>(batch); break;
+    case 1: need3 = tc::smem_bytes<1, 3, 2>(batch); need2 = tc::smem_bytes<1, 2, 2>(batch); break;
+    case 2: need2 = tc::smem_bytes<2, 2, 2>(batch); break;
+    default: need2 = tc::smem_bytes<4, 2, 1>(batch); break;
   }
   if (need3 <= (size_t)optin) *stages = 3;
   else if (need2 <= (size_t)optin) *stages = 2;
@@ -1360,10 +1512,10 @@ static int dispatch(const Params& p, int D, int bs, const void* q, const void* k
       !make_map(&tv_map, v_cache, D, p.num_kv_heads, (uint64_t)num_blocks * bs, 1, (uint32_t)(bs < tk ? bs : tk)))
     return SPEC_ERR_LAUNCH;
   if (kind == Kernel::kTc) {
-    if (mt == 1) return stages == 3 ? launch_tc<1, 3>(p, tq, tk_map, tv_map, stream)
-                                    : launch_tc<1, 2>(p, tq, tk_map, tv_map, stream);
-    if (mt == 2) return launch_tc<2, 2>(p, tq, tk_map, tv_map, stream);
-    return launch_tc<4, 2>(p, tq, tk_map, tv_map, stream);
+    if (mt == 1) return stages == 3 ? launch_tc<1, 3, 2>(p, tq, tk_map, tv_map, stream)
+                                    : launch_tc<1, 2, 2>(p, tq, tk_map, tv_map, stream);
+    if (mt == 2) return launch_tc<2, 2, 2>(p, tq, tk_map, tv_map, stream);
+    return launch_tc<4, 2, 1>(p, tq, tk_map, tv_map, stream);
   }
   switch (D) {
     case 64: return launch_main_d<64>(p, mt, tq, tk_map, tv_map, stream);
