@@ -120,11 +120,12 @@ size_t spec_verify_attention_workspace(const spec_attn_desc* d, int32_t k_draft)
  * CTAs (split-KV); a unit held by several CTAs is merged by its log-sum-exp
  * inside the same launch. The split is chosen on the device from ctx_lens, so
  * no host synchronisation is needed.
- * Kernels: mma.sync tiles by default. With the environment variable
- * SPEC_ATTN_KERNEL=tc, D = 128 runs on the 5th-generation tensor cores
- * (tcgen05, 128-key tiles, accumulators in tensor memory) whenever that
- * kernel's shared-memory plan fits the batch. Both give the same result within
- * rounding (fp32 accumulation in both).
+ * Kernels: D = 128 with (k_draft+1)*G >= 17 packed query rows runs on the
+ * 5th-generation tensor cores (tcgen05, 128-key tiles, accumulators in tensor
+ * memory) when that kernel's shared-memory plan fits the batch; other shapes
+ * run on mma.sync tiles. The environment variable SPEC_ATTN_KERNEL=tc or =mma
+ * overrides the choice for D = 128. Both give the same result within rounding
+ * (fp32 accumulation in both).
  * Device errors: a sequence with an out-of-range ctx_len (SPEC_DEVERR_CTX_LEN)
  * or block id (SPEC_DEVERR_BLOCK_ID) gets out rows of zeros.
  * Supported: D in {64,128,256}; bs in {16,32,64,128}; (k_draft+1)*G <= 64.

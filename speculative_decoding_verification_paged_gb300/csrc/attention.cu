@@ -699,7 +699,13 @@ struct Cfg {
   static constexpr int TILE_BYTES = TK * D * 2;         // 32 KB: two [128][64] slices
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K + V
   static constexpr int Q_BYTES = N * D * 2;             // two [N][64] slices
-  static constexpr int P_BYTES = N * TK * 2;            // one of P_hi / P_lo: two [N][64] slices
+  static constexpr int P_BYTES = N * TK * 2;            // one of P_hi / P_lo: [128 keys][N rows]
+  // P is the P.V operand B in MN-major layout: the N rows of a key are contiguous
+  // (N * 2 bytes) and swizzled at that width (32, 64 or 128 bytes), so a softmax
+  // thread, which owns one key, writes its rows with 16-byte stores.
+  static constexpr uint32_t P_LAYOUT = N == 16 ? 6u : (N == 32 ? 4u : 2u);
+  static constexpr int P_SWZ_SHIFT = N == 16 ? 2 : (N == 32 ? 1 : 0);  // key bits that pick the XOR
+  static constexpr int P_SWZ_MASK = N == 16 ? 1 : (N == 32 ? 3 : 7);
 };
 
 // Dynamic shared memory: stages + query buffers, NP P buffers (hi + lo), barriers,
@@ -982,9 +988,10 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     // one is a precomputed base plus the operand's address / 16.
     if (lane == 0) {
       constexpr uint32_t idesc_qk = umma_idesc_bf16(128, N, 0, 0);
-      constexpr uint32_t idesc_pv = umma_idesc_bf16(128, N, 1, 0);
-      const uint64_t kmaj = smem_desc_sw128(0, 16, 1024);          // K, Q, P: K-major
+      constexpr uint32_t idesc_pv = umma_idesc_bf16(128, N, 1, 1);
+      const uint64_t kmaj = smem_desc_sw128(0, 16, 1024);          // K, Q: K-major
       const uint64_t vmn = smem_desc_sw128(0, TK * 128, 1024);     // V: MN-major
+      const uint64_t pmn = smem_desc(0, 16, 16 * N, C::P_LAYOUT);  // P: MN-major, 8-key groups
       Cursor cq = cursor_at(f0, s_prefix, B, Hkv);  // next tile to multiply by Q
       bool pv_fresh = true;                          // tile i starts a unit (for P.V)
       int q_seq = 0;
@@ -1020,8 +1027,8 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
 #pragma unroll
           for (int kk = 0; kk < TK / 16; ++kk) {
             const uint32_t voff = (kk * 2048) >> 4;
-            const uint32_t poff = (part * C::P_BYTES + (kk >> 2) * N * 128 + (kk & 3) * 32) >> 4;
-            umma_bf16(tmem_o, vmn + vb + voff, kmaj + pb + poff, idesc_pv,
+            const uint32_t poff = (part * C::P_BYTES + kk * 32 * N) >> 4;
+            umma_bf16(tmem_o, vmn + vb + voff, pmn + pb + poff, idesc_pv,
                       (pv_fresh && part == 0 && kk == 0) ? 0u : 1u);
           }
         }
@@ -1062,6 +1069,8 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   Cursor cu = cursor_at(f0, s_prefix, B, Hkv);
   bool cu_fresh = true, from_zero = true, pending = false, fin_bad = false;
   Fin fin;
+  Fin pend[2];     // pieces of split units, merged when the CTA is done
+  int n_pend = 0;
   int ctx = 0, prefix_len = 0;
 
   // Wait until P.V of tile j (local index) is complete.
@@ -1112,80 +1121,76 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
       }
     }
     if (bad && st == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
-    if (!F.complete) {
-      // release: every partial store of the CTA is ordered before the arrival
-      named_sync(kBarSoftmax, kSoftmaxThreads);
-      const int unit = F.b * Hkv + F.g;
-      if (st == 0) {
-        __threadfence();
-        const int last = atomicAdd(p.counters + unit, 1) == F.nseg - 1;
-        if (last) __threadfence();  // acquire: the other pieces are visible
-        s_misc[8] = last;
-      }
-      named_sync(kBarSoftmax, kSoftmaxThreads);
-      if (s_misc[8]) {
-        // per-row max and 1 / (sum of weights) over the pieces' log-sum-exp
-        if (st < p.n_rows) {
-          const int r = st;
-          float Mx = -INFINITY;
-          bool nan = false;
-#pragma unroll 4
-          for (int sg = 0; sg < F.nseg; ++sg) {
-            const float l = __ldcg(p.lse + (int64_t)piece_slot(F.c0 + sg, F.c0, F.u0, W) * p.n_rows + r);
-            nan |= l != l;
-            Mx = fmaxf(Mx, l);
-          }
-          float wsum = 0.f;
-#pragma unroll 4
-          for (int sg = 0; sg < F.nseg; ++sg)
-            wsum += exp2f(__ldcg(p.lse + (int64_t)piece_slot(F.c0 + sg, F.c0, F.u0, W) * p.n_rows + r) - Mx);
-          const bool zero = nan || Mx == -INFINITY;
-          s_red[r] = zero ? 0.f : Mx;
-          s_red[64 + r] = zero ? 0.f : 1.f / wsum;
-          const int i = r / G, j = r - i * G;
-          s_rowoff[r] = (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
-        }
-        named_sync(kBarSoftmax, kSoftmaxThreads);
-        // out[row] = sum over pieces of weight * partial. A thread owns float4
-        // columns idx = st + k * 256 and, per piece, loads those of kItems items at
-        // once, so one pass costs about one L2 round trip per piece.
-        constexpr int kItems = 4;
-        for (int base = st; base < p.n_rows * (D / 4); base += kItems * kSoftmaxThreads) {
-          float4 acc[kItems];
-#pragma unroll
-          for (int k = 0; k < kItems; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int sg = 0; sg < F.nseg; ++sg) {
-            const int64_t slot = piece_slot(F.c0 + sg, F.c0, F.u0, W);
-#pragma unroll
-            for (int k = 0; k < kItems; ++k) {
-              const int idx = base + k * kSoftmaxThreads;
-              if (idx < p.n_rows * (D / 4)) {
-                const int r = idx / (D / 4), d4 = idx - r * (D / 4);
-                const float wgt = exp2f(__ldcg(p.lse + slot * p.n_rows + r) - s_red[r]);
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(p.opart + (slot * p.n_rows + r) * D) + d4);
-                acc[k].x += wgt * v.x;
-                acc[k].y += wgt * v.y;
-                acc[k].z += wgt * v.z;
-                acc[k].w += wgt * v.w;
-              }
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < kItems; ++k) {
-            const int idx = base + k * kSoftmaxThreads;
-            if (idx < p.n_rows * (D / 4)) {
-              const int r = idx / (D / 4), d4 = idx - r * (D / 4);
-              const float sc = s_red[64 + r];  // 0: a piece is invalid or the row saw no key
-              const float4 o = sc == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                         : make_float4(acc[k].x * sc, acc[k].y * sc, acc[k].z * sc, acc[k].w * sc);
-              __stcg(reinterpret_cast<float4*>(p.out + s_rowoff[r]) + d4, o);
-            }
-          }
-        }
-        if (st == 0) p.counters[unit] = 0;
-      }
+    if (!F.complete) pend[n_pend++] = F;  // arrival and merge happen when the CTA is done
+    named_sync(kBarSoftmax, kSoftmaxThreads);  // s_red and s_rowoff are reused
+  };
+
+  // A unit split over several CTAs is merged by the last CTA to arrive on its
+  // counter. A CTA holds at most two such pieces (its first and its last unit);
+  // it arrives for both once all its tiles are done, so no epilogue in the middle
+  // of the tile stream waits for an atomic. No CTA ever waits for another.
+  auto arrive_and_merge = [&]() {
+    named_sync(kBarSoftmax, kSoftmaxThreads);  // every partial store of the CTA is issued
+    if (st == 0) {
+      __threadfence();  // release the partials
+      int last[2] = {0, 0};
+      for (int k = 0; k < n_pend; ++k)
+        last[k] = atomicAdd(p.counters + pend[k].b * Hkv + pend[k].g, 1) == pend[k].nseg - 1;
+      if (last[0] | last[1]) __threadfence();  // acquire the other pieces
+      s_misc[8] = last[0];
+      s_misc[9] = last[1];
     }
-    named_sync(kBarSoftmax, kSoftmaxThreads);  // s_red, s_rowoff and s_misc are reused
+    named_sync(kBarSoftmax, kSoftmaxThreads);
+    for (int k = 0; k < n_pend; ++k) {
+      if (!s_misc[8 + k]) continue;
+      const Fin& F = pend[k];
+      if (st < p.n_rows) {
+        const int r = st, i = r / G, j = r - i * G;
+        s_rowoff[r] = (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
+      }
+      named_sync(kBarSoftmax, kSoftmaxThreads);
+      // out[row] = sum_pieces 2^(lse - M) * partial / sum_pieces 2^(lse - M), merged
+      // online; a thread's float4 columns load up to four pieces at a time
+      for (int idx = st; idx < p.n_rows * (D / 4); idx += kSoftmaxThreads) {
+        const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+        float M = -INFINITY, wsum = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        bool nan = false;
+        for (int sg0 = 0; sg0 < F.nseg; sg0 += 4) {
+          float l[4];
+          float4 v[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            l[u] = -INFINITY;
+            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (sg0 + u < F.nseg) {
+              const int64_t slot = piece_slot(F.c0 + sg0 + u, F.c0, F.u0, W);
+              l[u] = __ldcg(p.lse + slot * p.n_rows + r);
+              v[u] = __ldcg(reinterpret_cast<const float4*>(p.opart + (slot * p.n_rows + r) * D) + d4);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            nan |= l[u] != l[u];
+            if (l[u] == -INFINITY) continue;
+            const float Mn = fmaxf(M, l[u]);
+            const float a = exp2f(M - Mn), wgt = exp2f(l[u] - Mn);
+            acc.x = acc.x * a + wgt * v[u].x;
+            acc.y = acc.y * a + wgt * v[u].y;
+            acc.z = acc.z * a + wgt * v[u].z;
+            acc.w = acc.w * a + wgt * v[u].w;
+            wsum = wsum * a + wgt;
+            M = Mn;
+          }
+        }
+        const float sc = (nan || wsum == 0.f) ? 0.f : 1.f / wsum;  // 0: invalid piece or no key seen
+        const float4 o = sc == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                   : make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+        __stcg(reinterpret_cast<float4*>(p.out + s_rowoff[r]) + d4, o);
+      }
+      if (st == 0) p.counters[F.b * Hkv + F.g] = 0;
+      named_sync(kBarSoftmax, kSoftmaxThreads);  // s_rowoff is reused
+    }
   };
 
   for (int i = 0; i < n_tiles; ++i) {
@@ -1292,25 +1297,28 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     }
     // the P buffer is free once the P.V that last read it is done
     if (i >= NP) wait_pv(i - NP);
-    // ---- store P as bf16 hi + lo, K-major [N rows][128 keys]; lanes (2j, 2j+1) pair up so
-    // that each 32-bit store holds two adjacent keys of one row
+    // ---- store P as bf16 hi + lo: this thread's key, rows [c0, c0 + CW), 8 rows per
+    // 16-byte store, chunk index XOR-ed with the key bits of the swizzle
     uint8_t* pb = pbuf + (i % NP) * 2 * C::P_BYTES;
-    const int kk = key_in_tile;
-    const uint32_t psub = (uint32_t)(kk >> 6) * N * 128;
-    const bool even = (lane & 1) == 0;
+    {
+      const int k = key_in_tile;
+      const int sw = (k >> C::P_SWZ_SHIFT) & C::P_SWZ_MASK;
 #pragma unroll
-    for (int e = 0; e < CW; e += 2) {
-      const float o0 = __shfl_xor_sync(0xffffffffu, x[e], 1);
-      const float o1 = __shfl_xor_sync(0xffffffffu, x[e + 1], 1);
-      const int r = c0 + e + (even ? 0 : 1);
-      const float a = even ? x[e] : o1;       // key kk & ~1
-      const float bb = even ? o0 : x[e + 1];  // key kk | 1
-      const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, bb);
-      const float2 hf = __bfloat1622float2(h2);
-      const uint32_t lo = pack_bf16(a - hf.x, bb - hf.y);
-      const uint32_t off = psub + r * 128 + ((((kk & 63) >> 3) ^ (r & 7)) << 4) + ((kk & 6) << 1);
-      *reinterpret_cast<__nv_bfloat162*>(pb + off) = h2;
-      *reinterpret_cast<uint32_t*>(pb + C::P_BYTES + off) = lo;
+      for (int q = 0; q < CW / 8; ++q) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float a = x[8 * q + 2 * u], bb = x[8 * q + 2 * u + 1];
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, bb);
+          const float2 hf = __bfloat1622float2(h2);
+          hw[u] = *reinterpret_cast<const uint32_t*>(&h2);
+          lw[u] = pack_bf16(a - hf.x, bb - hf.y);
+        }
+        const int c = (c0 >> 3) + q;
+        const uint32_t off = (uint32_t)(k * N * 2) + ((uint32_t)(c ^ sw) << 4);
+        *reinterpret_cast<uint4*>(pb + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(pb + C::P_BYTES + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
     }
     fence_proxy_async_smem();  // P and zeroed V rows are read by the tensor core
     tc_fence_before();
@@ -1337,7 +1345,8 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   tc_fence_after();
   if (pending) epilogue(fin);
   tc_fence_before();
-  named_sync(kBarTail, 32 + kSoftmaxThreads);
+  named_sync(kBarTail, 32 + kSoftmaxThreads);  // tensor memory may be released
+  if (n_pend > 0) arrive_and_merge();
 }
 
 }  // namespace tc
@@ -1472,15 +1481,20 @@ static int launch_tc(const Params& p, const CUtensorMap& tq, const CUtensorMap& 
 
 enum class Kernel { kMma, kTc };
 
-// Which kernel runs a call. The environment variable SPEC_ATTN_KERNEL=tc
-// selects the tcgen05 kernel for D = 128 when its shared memory fits the batch;
-// otherwise (and by default) the mma.sync kernel runs. Both compute the same
-// result within rounding.
+// Which kernel runs a call. D = 128 with 32 or more packed query rows per kv head
+// takes the tcgen05 kernel (its MMAs stay wide, where mma.sync tiles become
+// compute-bound), 16 rows the mma.sync kernel (at that width both are bound by
+// HBM and the mma.sync kernel, two CTAs per SM, hides its per-unit work better).
+// The environment variable SPEC_ATTN_KERNEL=tc or =mma overrides the choice; the
+// tcgen05 kernel also needs its shared-memory plan to fit the batch. Both compute
+// the same result within rounding.
 static Kernel choose_kernel(int D, int mt, int batch, int* stages) {
   *stages = 0;
   if (D != 128) return Kernel::kMma;
   const char* env = getenv("SPEC_ATTN_KERNEL");
-  if (env == nullptr || strcmp(env, "tc") != 0) return Kernel::kMma;
+  const bool force_tc = env != nullptr && strcmp(env, "tc") == 0;
+  const bool force_mma = env != nullptr && strcmp(env, "mma") == 0;
+  if (force_mma || (!force_tc && mt < 2)) return Kernel::kMma;
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)

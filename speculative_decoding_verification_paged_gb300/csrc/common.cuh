@@ -286,6 +286,16 @@ SPEC_DEVICE uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo_bytes, uint32_t
   d |= (uint64_t)2 << 61;  // 128-byte swizzle
   return d;
 }
+// Same for any layout type: 2 = 128-byte swizzle, 4 = 64-byte, 6 = 32-byte.
+SPEC_DEVICE uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes, uint32_t sbo_bytes, uint32_t layout) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)(layout & 7u) << 61;
+  return d;
+}
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D; a_mn / b_mn select MN-major operands.
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4)                      // D format: f32

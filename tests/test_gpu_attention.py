@@ -3,8 +3,9 @@
 Small cases are checked in full; the named workloads at their full sizes are
 checked on sampled sequences (the oracle recomputes those sequences one by one
 from the same device inputs). Tolerances: max-abs <= 1e-2 and relative L2 <=
-2e-3 per case. Head dim 128 has two kernels (mma.sync by default, tcgen05 with
-SPEC_ATTN_KERNEL=tc); every head-dim-128 case runs both.
+2e-3 per case. Head dim 128 has two kernels (tcgen05, the default from 32 packed
+rows up, and mma.sync; SPEC_ATTN_KERNEL=tc / =mma forces one); every
+head-dim-128 case runs both, and one case runs the default choice.
 """
 
 import zlib
@@ -116,6 +117,18 @@ def test_attention_large_batch_plans(sv, oracle_mod, attn_kernel, B, Hq, k):
     """Batches whose per-sequence plan fills shared memory: every sequence is checked."""
     w = wl.Workload(name=f"big{B}", batch=B, ctx_lens=_ragged(B, k + 1, 160, B), block_size=16,
                     num_q_heads=Hq, num_kv_heads=2 if Hq == 16 else 8, head_dim=128, k_draft=k, seed=B % 997)
+    a = wl.make_attention_inputs(w, device=DEV)
+    out, err = run_attention(sv, a, w)
+    assert err == 0
+    mx, rel = attention_errors(out.cpu().numpy(), oracle_attention_for(oracle_mod, a))
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+
+
+@pytest.mark.parametrize("name", ["longctx", "llama8b_eagle3"])
+def test_attention_default_kernel_choice(sv, oracle_mod, monkeypatch, name):
+    """No override: the library picks the kernel (tcgen05 for 64 rows, mma.sync for 16)."""
+    monkeypatch.delenv("SPEC_ATTN_KERNEL", raising=False)
+    w = wl.WORKLOADS[name].replace(batch=3, ctx_lens=(129, 3000, 9), ctx_range=None)
     a = wl.make_attention_inputs(w, device=DEV)
     out, err = run_attention(sv, a, w)
     assert err == 0
