@@ -438,47 +438,75 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, MT>::MIN_BLOCKS) verify_atten
     }
     if (bad && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
     if (!F.complete) {
-      __threadfence();  // publish this piece before counting it
+      // release: every partial store of the CTA precedes the arrival
       named_sync(kBarConsumers, kConsumers);
       const int unit = F.b * Hkv + F.g;
-      if (tid == 0) s_misc[8] = (atomicAdd(p.counters + unit, 1) == F.nseg - 1) ? 1 : 0;
+      if (tid == 0) {
+        __threadfence();
+        const int last = atomicAdd(p.counters + unit, 1) == F.nseg - 1;
+        if (last) __threadfence();  // acquire: the other pieces are visible
+        s_misc[8] = last;
+      }
       named_sync(kBarConsumers, kConsumers);
       if (s_misc[8]) {
-        __threadfence();
-        for (int idx = tid; idx < p.n_rows * (D / 4); idx += kConsumers) {
-          const int r = idx / (D / 4), d4 = idx - r * (D / 4);
-          float Mx = -INFINITY;
-          bool nan = false;
-          for (int s = 0; s < F.nseg; ++s) {
-            const int slot = piece_slot(F.c0 + s, F.c0, F.u0, W);
-            const float l = __ldcg(p.lse + (int64_t)slot * p.n_rows + r);
-            nan |= l != l;
-            Mx = fmaxf(Mx, l);
+        // out = sum_pieces 2^(lse - M) * partial / sum_pieces 2^(lse - M), merged
+        // online; a thread takes kB float4 columns at once and loads a piece's
+        // values for all of them together, so each piece costs one L2 round trip
+        constexpr int kB = 4;
+        for (int base = tid; base < p.n_rows * (D / 4); base += kB * kConsumers) {
+          float M[kB], ws[kB];
+          float4 acc[kB];
+          bool bad[kB];
+#pragma unroll
+          for (int u = 0; u < kB; ++u) {
+            M[u] = -INFINITY;
+            ws[u] = 0.f;
+            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            bad[u] = false;
           }
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (!nan && Mx != -INFINITY) {
-            float wsum = 0.f;
-            for (int s = 0; s < F.nseg; ++s) {
-              const int slot = piece_slot(F.c0 + s, F.c0, F.u0, W);
-              const float wgt = exp2f(__ldcg(p.lse + (int64_t)slot * p.n_rows + r) - Mx);
-              if (wgt > 0.f) {
-                const float4 v =
-                    __ldcg(reinterpret_cast<const float4*>(p.opart + ((int64_t)slot * p.n_rows + r) * D) + d4);
-                acc.x += wgt * v.x;
-                acc.y += wgt * v.y;
-                acc.z += wgt * v.z;
-                acc.w += wgt * v.w;
+          for (int sg = 0; sg < F.nseg; ++sg) {
+            const int64_t slot = piece_slot(F.c0 + sg, F.c0, F.u0, W);
+            float l[kB];
+            float4 v[kB];
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+              const int idx = base + u * kConsumers;
+              l[u] = -INFINITY;
+              v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (idx < p.n_rows * (D / 4)) {
+                const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+                l[u] = __ldcg(p.lse + slot * p.n_rows + r);
+                v[u] = __ldcg(reinterpret_cast<const float4*>(p.opart + (slot * p.n_rows + r) * D) + d4);
               }
-              wsum += wgt;
             }
-            const float inv = 1.f / wsum;
-            acc.x *= inv;
-            acc.y *= inv;
-            acc.z *= inv;
-            acc.w *= inv;
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+              const float lv = l[u];
+              bad[u] |= lv != lv;
+              if (!(lv > -INFINITY)) continue;
+              const float Mn = fmaxf(M[u], lv);
+              const float a = exp2f(M[u] - Mn), wgt = exp2f(lv - Mn);
+              acc[u].x = acc[u].x * a + wgt * v[u].x;
+              acc[u].y = acc[u].y * a + wgt * v[u].y;
+              acc[u].z = acc[u].z * a + wgt * v[u].z;
+              acc[u].w = acc[u].w * a + wgt * v[u].w;
+              ws[u] = ws[u] * a + wgt;
+              M[u] = Mn;
+            }
           }
-          const int i = r / G, j = r - i * G;
-          reinterpret_cast<float4*>(p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D)[d4] = acc;
+#pragma unroll
+          for (int u = 0; u < kB; ++u) {
+            const int idx = base + u * kConsumers;
+            if (idx < p.n_rows * (D / 4)) {
+              const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+              const float sc = (bad[u] || !(ws[u] > 0.f)) ? 0.f : 1.f / ws[u];  // 0: bad piece or no key seen
+              const float4 o = sc == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                         : make_float4(acc[u].x * sc, acc[u].y * sc, acc[u].z * sc, acc[u].w * sc);
+              const int i = r / G, j = r - i * G;
+              __stcg(reinterpret_cast<float4*>(p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D) + d4,
+                     o);
+            }
+          }
         }
         if (tid == 0) p.counters[unit] = 0;  // ready for the next call
       }
