@@ -351,92 +351,161 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, MT>::MIN_BLOCKS) verify_atten
       l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
     }
     named_sync(kBarConsumers, kConsumers);  // every warp is done reading the stage used as scratch
+    // Parallel combine, when the freed stage holds every warp's O: each warp writes
+    // its O and row statistics, then every consumer thread merges one
+    // (row, 16-column) segment over the WN key-split warps and writes it with
+    // 16-byte stores. Otherwise warp column 0 merges the others' O alone.
+    constexpr bool kParallel = WN > 1 && (size_t)WN * MT * 16 * D * 4 <= (size_t)C::STAGE_BYTES;
+    if constexpr (kParallel) {
+      const int base = (wn * MT + mt) * 16;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        const int d = n * 8 + 2 * (lane & 3);
+        *reinterpret_cast<float2*>(&scratch[(base + row_in) * D + d]) = make_float2(o[n][0], o[n][1]);
+        *reinterpret_cast<float2*>(&scratch[(base + row_in + 8) * D + d]) = make_float2(o[n][2], o[n][3]);
+      }
+      if ((lane & 3) == 0) {
+        s_m[base + row_in] = m_run[0];
+        s_l[base + row_in] = l_run[0];
+        s_m[base + row_in + 8] = m_run[1];
+        s_l[base + row_in + 8] = l_run[1];
+      }
+      const bool bad = named_sync_or(kBarConsumers, kConsumers, s_bad[F.seq % S] != 0);
+      constexpr int kSeg = D / 16;  // 16-column segments per row
+      for (int item = tid; item < MT * 16 * kSeg; item += kConsumers) {
+        const int r = item / kSeg, seg = item - r * kSeg;
+        if (r >= p.n_rows) continue;
+        const int rt = r >> 4, ri = r & 15;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < WN; ++w) M = fmaxf(M, s_m[(w * MT + rt) * 16 + ri]);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        float L = 0.f;
+        float4 acc[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < WN; ++w) {
+          const int sr = (w * MT + rt) * 16 + ri;
+          const float f = fast_exp2(s_m[sr] - Mu);
+          L += s_l[sr] * f;
+          const float4* src = reinterpret_cast<const float4*>(&scratch[sr * D + seg * 16]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 v = src[c];
+            acc[c].x += v.x * f;
+            acc[c].y += v.y * f;
+            acc[c].z += v.z * f;
+            acc[c].w += v.w * f;
+          }
+        }
+        const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
+        float* dst;
+        if (F.complete) {
+          const int i = r / G, j = r - i * G;
+          dst = p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
+        } else {
+          dst = p.opart + ((int64_t)F.slot * p.n_rows + r) * D;
+          if (seg == 0) {
+            float lse2 = L > 0.f ? M + __log2f(L) : -INFINITY;
+            if (bad) lse2 = __int_as_float(0x7fc00000);  // NaN marks an unusable piece
+            __stcg(p.lse + (int64_t)F.slot * p.n_rows + r, lse2);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          __stcg(reinterpret_cast<float4*>(dst + seg * 16) + c,
+                 make_float4(acc[c].x * inv, acc[c].y * inv, acc[c].z * inv, acc[c].w * inv));
+      }
+      if (bad && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
+    } else {
     if constexpr (WN > 1) {
-      if (wn > 0) {
-        const int base = ((wn - 1) * MT + mt) * 16;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          const int d = n * 8 + 2 * (lane & 3);
-          *reinterpret_cast<float2*>(&scratch[(base + row_in) * D + d]) = make_float2(o[n][0], o[n][1]);
-          *reinterpret_cast<float2*>(&scratch[(base + row_in + 8) * D + d]) = make_float2(o[n][2], o[n][3]);
-        }
-        if ((lane & 3) == 0) {
-          s_m[base + row_in] = m_run[0];
-          s_l[base + row_in] = l_run[0];
-          s_m[base + row_in + 8] = m_run[1];
-          s_l[base + row_in + 8] = l_run[1];
-        }
-      }
-    }
-    const bool bad = named_sync_or(kBarConsumers, kConsumers, s_bad[F.seq % S] != 0);
-    if (wn == 0) {
-      float M[2] = {m_run[0], m_run[1]};
-      if constexpr (WN > 1) {
-#pragma unroll
-        for (int w = 1; w < WN; ++w) {
-          const int base = ((w - 1) * MT + mt) * 16 + row_in;
-          M[0] = fmaxf(M[0], s_m[base]);
-          M[1] = fmaxf(M[1], s_m[base + 8]);
-        }
-      }
-      float Mu[2], L[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        Mu[h] = M[h] == -INFINITY ? 0.f : M[h];
-        const float f = fast_exp2(m_run[h] - Mu[h]);
-        L[h] = l_run[h] * f;
-#pragma unroll
-        for (int n = 0; n < D / 8; ++n) {
-          o[n][2 * h] *= f;
-          o[n][2 * h + 1] *= f;
-        }
-      }
-      if constexpr (WN > 1) {
-#pragma unroll
-        for (int w = 1; w < WN; ++w) {
-          const int base = ((w - 1) * MT + mt) * 16 + row_in;
-          const float fa = fast_exp2(s_m[base] - Mu[0]);
-          const float fb = fast_exp2(s_m[base + 8] - Mu[1]);
-          L[0] += s_l[base] * fa;
-          L[1] += s_l[base + 8] * fb;
+        if (wn > 0) {
+          const int base = ((wn - 1) * MT + mt) * 16;
 #pragma unroll
           for (int n = 0; n < D / 8; ++n) {
             const int d = n * 8 + 2 * (lane & 3);
-            const float2 va = *reinterpret_cast<const float2*>(&scratch[base * D + d]);
-            const float2 vb = *reinterpret_cast<const float2*>(&scratch[(base + 8) * D + d]);
-            o[n][0] += va.x * fa;
-            o[n][1] += va.y * fa;
-            o[n][2] += vb.x * fb;
-            o[n][3] += vb.y * fb;
+            *reinterpret_cast<float2*>(&scratch[(base + row_in) * D + d]) = make_float2(o[n][0], o[n][1]);
+            *reinterpret_cast<float2*>(&scratch[(base + row_in + 8) * D + d]) = make_float2(o[n][2], o[n][3]);
+          }
+          if ((lane & 3) == 0) {
+            s_m[base + row_in] = m_run[0];
+            s_l[base + row_in] = l_run[0];
+            s_m[base + row_in + 8] = m_run[1];
+            s_l[base + row_in + 8] = l_run[1];
           }
         }
       }
+      const bool bad = named_sync_or(kBarConsumers, kConsumers, s_bad[F.seq % S] != 0);
+      if (wn == 0) {
+        float M[2] = {m_run[0], m_run[1]};
+        if constexpr (WN > 1) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int r = h == 0 ? r0 : r1;
-        if (r < p.n_rows) {
-          const float inv = (L[h] > 0.f && !bad) ? 1.f / L[h] : 0.f;
-          float* dst;
-          if (F.complete) {
-            const int i = r / G, j = r - i * G;
-            dst = p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
-          } else {
-            dst = p.opart + ((int64_t)F.slot * p.n_rows + r) * D;
-            if ((lane & 3) == 0) {
-              float lse2 = L[h] > 0.f ? M[h] + __log2f(L[h]) : -INFINITY;
-              if (bad) lse2 = __int_as_float(0x7fc00000);  // NaN marks an unusable piece
-              p.lse[(int64_t)F.slot * p.n_rows + r] = lse2;
+          for (int w = 1; w < WN; ++w) {
+            const int base = ((w - 1) * MT + mt) * 16 + row_in;
+            M[0] = fmaxf(M[0], s_m[base]);
+            M[1] = fmaxf(M[1], s_m[base + 8]);
+          }
+        }
+        float Mu[2], L[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          Mu[h] = M[h] == -INFINITY ? 0.f : M[h];
+          const float f = fast_exp2(m_run[h] - Mu[h]);
+          L[h] = l_run[h] * f;
+#pragma unroll
+          for (int n = 0; n < D / 8; ++n) {
+            o[n][2 * h] *= f;
+            o[n][2 * h + 1] *= f;
+          }
+        }
+        if constexpr (WN > 1) {
+#pragma unroll
+          for (int w = 1; w < WN; ++w) {
+            const int base = ((w - 1) * MT + mt) * 16 + row_in;
+            const float fa = fast_exp2(s_m[base] - Mu[0]);
+            const float fb = fast_exp2(s_m[base + 8] - Mu[1]);
+            L[0] += s_l[base] * fa;
+            L[1] += s_l[base + 8] * fb;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+              const int d = n * 8 + 2 * (lane & 3);
+              const float2 va = *reinterpret_cast<const float2*>(&scratch[base * D + d]);
+              const float2 vb = *reinterpret_cast<const float2*>(&scratch[(base + 8) * D + d]);
+              o[n][0] += va.x * fa;
+              o[n][1] += va.y * fa;
+              o[n][2] += vb.x * fb;
+              o[n][3] += vb.y * fb;
             }
           }
+        }
 #pragma unroll
-          for (int n = 0; n < D / 8; ++n) {
-            const int d = n * 8 + 2 * (lane & 3);
-            *reinterpret_cast<float2*>(dst + d) = make_float2(o[n][2 * h] * inv, o[n][2 * h + 1] * inv);
+        for (int h = 0; h < 2; ++h) {
+          const int r = h == 0 ? r0 : r1;
+          if (r < p.n_rows) {
+            const float inv = (L[h] > 0.f && !bad) ? 1.f / L[h] : 0.f;
+            float* dst;
+            if (F.complete) {
+              const int i = r / G, j = r - i * G;
+              dst = p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
+            } else {
+              dst = p.opart + ((int64_t)F.slot * p.n_rows + r) * D;
+              if ((lane & 3) == 0) {
+                float lse2 = L[h] > 0.f ? M[h] + __log2f(L[h]) : -INFINITY;
+                if (bad) lse2 = __int_as_float(0x7fc00000);  // NaN marks an unusable piece
+                p.lse[(int64_t)F.slot * p.n_rows + r] = lse2;
+              }
+            }
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+              const int d = n * 8 + 2 * (lane & 3);
+              *reinterpret_cast<float2*>(dst + d) = make_float2(o[n][2 * h] * inv, o[n][2 * h + 1] * inv);
+            }
           }
         }
       }
+      if (bad && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
     }
-    if (bad && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
     if (!F.complete) {
       // release: every partial store of the CTA precedes the arrival
       named_sync(kBarConsumers, kConsumers);
