@@ -14,7 +14,8 @@ Readings of the pages that the oracle fixes (the pages leave them open):
 ctx_lens counts the verify tokens; row i sits at absolute position
 ctx - (k+1) + i; GQA groups are contiguous; softmax scale 1/sqrt(D); greedy
 ties go to the lowest index; acceptance compares u*q < p; the residual falls
-back to p when max(0, p-q) is all zero; the correction/bonus draw is an
+back to p when max(0, p-q) is all zero; without draft probabilities q is one-hot
+at the drafted token; the correction/bonus draw is an
 exponential race keyed by Philox words as documented in spec_verify.h.
 """
 
@@ -152,6 +153,10 @@ def verify_attention(q_bits, k_bits, v_bits, block_table, ctx_lens, *, seqs=None
 def accept(target_logits, draft_tokens, draft_probs, seed: int, mode, temperature, *,
            n_threads: int = 0, check: bool = True):
     """Greedy / speculative-sampling acceptance, double precision.
+
+    draft_probs may be None: sampling rows then take the draft distribution as
+    one-hot at each drafted token (accept iff u < p(d); the residual is p with
+    the rejected token removed).
 
     Returns (out_tokens [B,k+1] int32, accept_len [B] int32, accept_margin [B],
     race_gap [B], status). accept_margin is the smallest |u - p/q| among the

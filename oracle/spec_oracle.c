@@ -335,9 +335,16 @@ static int exponential_race(const double* w, int V, uint64_t seed, int m, int b,
   return ex[best];
 }
 
+/* Draft probability q_j(x). Without a draft distribution (draft_probs NULL) the
+ * draft is taken as deterministic: q_j is one-hot at the drafted token d_j (the
+ * reject sampler of lmdeploy PR #3945 is called with draft_probs = None). */
+static double draft_q(const float* Q, const int32_t* d, int j, int V, int x) {
+  return Q ? (double)Q[(int64_t)j * V + x] : (x == d[j] ? 1.0 : 0.0);
+}
+
 /*
- * target_logits [B,k+1,V]; draft_tokens [B,k]; draft_probs [B,k,V] (may be
- * NULL when every row is greedy); mode [B] (0 greedy, 1 sampling);
+ * target_logits [B,k+1,V]; draft_tokens [B,k]; draft_probs [B,k,V] (NULL: every
+ * sampling row uses one-hot q, see draft_q); mode [B] (0 greedy, 1 sampling);
  * temperature [B]. Outputs out_tokens [B,k+1], accept_len [B], and for the
  * parity bookkeeping accept_margin [B] = min over the drafts that were tested
  * of |u - p/q| (+inf for greedy rows or when every q was 0) and race_gap [B] =
@@ -356,9 +363,6 @@ int oracle_accept(const float* target_logits, const int32_t* draft_tokens, const
   if (B < 0 || k < 1 || V < 1) return ORACLE_ERR_ARG;
   for (int b = 0; b < B; ++b)
     if (mode[b] != 0 && mode[b] != 1) return ORACLE_ERR_ARG;
-  if (!draft_probs)
-    for (int b = 0; b < B; ++b)
-      if (mode[b] == 1) return ORACLE_ERR_ARG;
   const int R = k + 1;
   int status = ORACLE_OK;
   set_threads(n_threads);
@@ -388,13 +392,13 @@ int oracle_accept(const float* target_logits, const int32_t* draft_tokens, const
       tok[m] = argmax_row(L + (int64_t)m * V, V);
     } else if (err == ORACLE_OK) {
       const double T = (double)temperature[b];
-      const float* Q = draft_probs + (int64_t)b * k * V;
+      const float* Q = draft_probs ? draft_probs + (int64_t)b * k * V : NULL;
       double mx = 0.0, z = 1.0;
       m = k;
       for (int j = 0; j < k; ++j) {
         softmax_stats(L + (int64_t)j * V, V, T, &mx, &z);
         const double p = exp((double)L[(int64_t)j * V + d[j]] / T - mx) / z;
-        const double qd = (double)Q[(int64_t)j * V + d[j]];
+        const double qd = draft_q(Q, d, j, V, d[j]);
         const double u = oracle_uniform(philox_word(seed, 0u, (uint32_t)j, (uint32_t)b, 0u, 0));
         if (qd > 0.0) {
           double mg = fabs(u - p / qd);
@@ -414,7 +418,7 @@ int oracle_accept(const float* target_logits, const int32_t* draft_tokens, const
           double total = 0.0;
           for (int x = 0; x < V; ++x) {
             double p = exp((double)L[(int64_t)m * V + x] / T - mx) / z;
-            double r = p - (double)Q[(int64_t)m * V + x];
+            double r = p - draft_q(Q, d, m, V, x);
             w[x] = r > 0.0 ? r : 0.0;
             total += w[x];
           }

@@ -372,6 +372,46 @@ def test_sampling_residual_support(oracle_mod):
     assert abs(np.mean(~rej) - 2 / 3) < 0.02
 
 
+def test_sampling_without_draft_probs_is_one_hot(oracle_mod):
+    """No draft distribution: q is one-hot at the drafted token, so a draft is kept
+    with probability p(d) and a rejection draws from p with d removed."""
+    rng = np.random.default_rng(31)
+    B, k, V = 100_000, 1, 8
+    l0 = rng.normal(0, 1.0, V).astype(np.float32)
+    l1 = rng.normal(0, 1.0, V).astype(np.float32)
+    L = np.broadcast_to(np.stack([l0, l1]), (B, k + 1, V))
+    d = np.full((B, k), 2, np.int32)
+    tok, alen, _, _, rc = oracle_mod.accept(L, d, None, 77, np.ones(B, np.int32), np.ones(B, np.float32))
+    assert rc == 0
+    p0 = _softmax(l0.astype(np.float64))
+    acc = alen == 1
+    assert abs(acc.mean() - p0[2]) < 5 * np.sqrt(p0[2] * (1 - p0[2]) / B)
+    # rejected rows: never the draft, distributed as p0 without entry 2
+    rej_tok = tok[~acc, 0]
+    assert np.all(rej_tok != 2)
+    resid = p0.copy()
+    resid[2] = 0.0
+    resid /= resid.sum()
+    assert _chi2_ok(rej_tok, resid) > 1e-3
+    assert _chi2_ok(rej_tok, p0) < 1e-3  # keeping d's mass must fail: the check has power
+    # accepted rows: the bonus token follows p_1
+    assert np.all(tok[acc, 0] == 2)
+    assert _chi2_ok(tok[acc, 1], _softmax(l1.astype(np.float64))) > 1e-3
+
+
+def test_sampling_without_draft_probs_equals_explicit_one_hot(oracle_mod):
+    rng = np.random.default_rng(32)
+    B, k, V = 64, 3, 50
+    L = rng.normal(0, 2.0, (B, k + 1, V)).astype(np.float32)
+    d = rng.integers(0, V, (B, k)).astype(np.int32)
+    Q = np.zeros((B, k, V), np.float32)
+    np.put_along_axis(Q, d[:, :, None], 1.0, axis=2)
+    temp = rng.uniform(0.5, 1.5, B).astype(np.float32)
+    a = oracle_mod.accept(L, d, None, 5, np.ones(B, np.int32), temp)
+    b = oracle_mod.accept(L, d, Q, 5, np.ones(B, np.int32), temp)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
 def test_sampling_uniform_uses_documented_counter(oracle_mod):
     """u_j is word 0 of Philox counter (0, j, b, 0) under key (seed lo, seed hi)."""
     B, k, V = 64, 2, 4
