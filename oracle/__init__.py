@@ -90,6 +90,8 @@ def _load():
         lib.oracle_accept.restype = i32
         lib.oracle_commit_state.argtypes = [P, P, P, i32, i32, i32, i64, i32]
         lib.oracle_commit_state.restype = i32
+        lib.oracle_commit_state_aligned.argtypes = [P, P, P, i32, i32, i32, i64, i32, i32, i32]
+        lib.oracle_commit_state_aligned.restype = i32
         _lib = lib
         return lib
 
@@ -194,6 +196,27 @@ def commit_state(snapshots, accept_len, live, *, n_threads: int = 0, check: bool
     L, B, S, E = sn.shape
     assert live.shape == (L, B, E) and al.shape == (B,)
     rc = lib.oracle_commit_state(_ptr(sn), _ptr(al), _ptr(live), L, B, S, E, n_threads)
+    if check and rc != 0:
+        raise OracleError(rc)
+    return rc
+
+
+def commit_state_aligned(snapshots, accept_len, live, n_tokens: int, alignment: int, *, n_threads: int = 0,
+                         check: bool = True):
+    """Windowed checkpoints: snapshots [L,B,W,E] for a step of n_tokens <= W tokens.
+
+    alignment 0: slot j holds the state after token j (slot = accept_len);
+    alignment 1: slot W-1 holds the state after the last token
+    (slot = W - n_tokens + accept_len). In place on `live`; returns the status.
+    """
+    lib = _load()
+    sn = _c(snapshots, np.float32)
+    al = _c(accept_len, np.int32)
+    assert live.dtype == np.float32 and live.flags.c_contiguous
+    L, B, W, E = sn.shape
+    assert live.shape == (L, B, E) and al.shape == (B,)
+    rc = lib.oracle_commit_state_aligned(_ptr(sn), _ptr(al), _ptr(live), L, B, W, E, int(n_tokens),
+                                         int(alignment), n_threads)
     if check and rc != 0:
         raise OracleError(rc)
     return rc

@@ -456,6 +456,40 @@ int oracle_accept(const float* target_logits, const int32_t* draft_tokens, const
  * and row; rows with accept_len outside [0,S-1] keep their live state and make
  * the call return ORACLE_ERR_ACCEPT_LEN.
  */
+/*
+ * Checkpoint windows of W >= n slots for a step of n tokens (onnxruntime-genai
+ * PR #2457: a checkpoint count plus a checkpoint alignment, because the conv
+ * writes slot j after local token j while GatedDeltaNet writes slot W-1 after
+ * the last token). With m = accept_len[b] drafts accepted the state to keep is
+ * the one after token m:
+ *   alignment 0 (token-indexed): slot m
+ *   alignment 1 (last at W-1):   slot W - n + m
+ * live[l,b,:] = snapshots[l,b,slot,:]; rows with m outside [0, n-1] are skipped
+ * and reported.
+ */
+int oracle_commit_state_aligned(const float* snapshots, const int32_t* accept_len, float* live, int L, int B,
+                                int W, int64_t E, int n, int alignment, int n_threads) {
+  if (!snapshots || !accept_len || !live || L < 0 || B < 0 || W < 1 || E < 0) return ORACLE_ERR_ARG;
+  if (n < 1 || n > W || (alignment != 0 && alignment != 1)) return ORACLE_ERR_ARG;
+  const int base = alignment == 0 ? 0 : W - n;
+  int status = ORACLE_OK;
+  for (int b = 0; b < B; ++b)
+    if (accept_len[b] < 0 || accept_len[b] >= n) status = ORACLE_ERR_ACCEPT_LEN;
+  set_threads(n_threads);
+  const int64_t n_units = (int64_t)L * B;
+#pragma omp parallel for schedule(static)
+  for (int64_t unit = 0; unit < n_units; ++unit) {
+    const int64_t l = unit / B;
+    const int b = (int)(unit % B);
+    const int m = accept_len[b];
+    if (m < 0 || m >= n) continue;
+    const float* src = snapshots + ((l * B + b) * W + base + m) * E;
+    float* dst = live + (l * B + b) * E;
+    memcpy(dst, src, sizeof(float) * (size_t)E);
+  }
+  return status;
+}
+
 int oracle_commit_state(const float* snapshots, const int32_t* accept_len, float* live, int L, int B,
                         int S, int64_t E, int n_threads) {
   if (!snapshots || !accept_len || !live || L < 0 || B < 0 || S < 1 || E < 0) return ORACLE_ERR_ARG;

@@ -513,6 +513,42 @@ def test_commit_picks_accepted_slot(oracle_mod):
     assert np.array_equal(live[:, 0], snaps[:, 0, 0])
 
 
+def test_commit_aligned_windows(oracle_mod):
+    """Token-indexed windows keep slot m, last-aligned windows slot W - n + m; with
+    W = n both are the plain commit, and a fully accepted step keeps slot W - 1 of a
+    last-aligned window (the state after its last token)."""
+    rng = np.random.default_rng(21)
+    L, B, W, E, n = 2, 6, 7, 5, 4
+    snaps = rng.standard_normal((L, B, W, E)).astype(np.float32)
+    # tag every slot with its index so the chosen slot can be read back
+    snaps[..., 0] = np.arange(W, dtype=np.float32)[None, None, :]
+    alen = np.array([0, 1, 2, 3, 3, 0], np.int32)
+    for alignment, base in ((0, 0), (1, W - n)):
+        live = np.zeros((L, B, E), np.float32)
+        assert oracle_mod.commit_state_aligned(snaps, alen, live, n, alignment) == 0
+        assert np.array_equal(live[..., 0], np.broadcast_to((base + alen).astype(np.float32), (L, B)))
+        for l in range(L):
+            for b in range(B):
+                assert np.array_equal(live[l, b], snaps[l, b, base + alen[b]])
+    live = np.zeros((L, B, E), np.float32)
+    oracle_mod.commit_state_aligned(snaps, np.full(B, n - 1, np.int32), live, n, 1)
+    assert np.all(live[..., 0] == W - 1)
+    # W = n: both alignments equal the plain commit
+    sq = snaps[:, :, :n].copy()
+    ref = np.zeros((L, B, E), np.float32)
+    oracle_mod.commit_state(sq, alen, ref)
+    for alignment in (0, 1):
+        live = np.zeros((L, B, E), np.float32)
+        oracle_mod.commit_state_aligned(sq, alen, live, n, alignment)
+        assert np.array_equal(live, ref)
+    # accept_len must lie in [0, n-1]; the row is skipped and reported
+    live = np.full((L, B, E), 9.0, np.float32)
+    bad = alen.copy()
+    bad[2] = n
+    rc = oracle_mod.commit_state_aligned(snaps, bad, live, n, 1, check=False)
+    assert rc != 0 and np.all(live[:, 2] == 9.0)
+
+
 def test_commit_skips_invalid_rows(oracle_mod):
     rng = np.random.default_rng(21)
     L, B, S, E = 2, 3, 4, 8
