@@ -67,7 +67,7 @@ typedef struct CUstream_st* spec_stream_t;
 #define SPEC_DEVERR_CTX_LEN 8      /* ctx_len < k+1 or > max_blocks_per_seq * bs */
 #define SPEC_DEVERR_TEMPERATURE 16 /* sampling row with temperature not > 0      */
 #define SPEC_DEVERR_TIMEOUT 32     /* an asynchronous copy did not arrive        */
-#define SPEC_DEVERR_MODE 64        /* mode not 0/1, or sampling row without probs */
+#define SPEC_DEVERR_MODE 64        /* mode not 0/1                               */
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* spec_status_string(int status);
@@ -205,8 +205,11 @@ size_t spec_verify_attention_noalloc_limit(void);
  *
  *  target_logits [B, k+1, V] fp32
  *  draft_tokens  [B, k] int32
- *  draft_probs   [B, k, V] fp32, each row a distribution; may be NULL only if
- *                every row is greedy
+ *  draft_probs   [B, k, V] fp32, each row a distribution; or NULL: the
+ *                drafts are then deterministic and q_j is one-hot at d_j, so
+ *                draft j is kept iff u_j < p_j(d_j) and a rejection draws from
+ *                p_m with d_m removed (the reject sampler of lmdeploy PR #3945
+ *                is called with draft_probs = None)
  *  mode          [B] int32 (SPEC_MODE_*); temperature [B] fp32 (ignored for
  *                greedy rows)
  *  out_tokens    [B, k+1] int32: d_0..d_{m-1}, final token, then -1 padding
@@ -216,8 +219,7 @@ size_t spec_verify_attention_noalloc_limit(void);
  * depend on the outcome.
  * Device errors: a row with a draft token outside [0, V) (SPEC_DEVERR_TOKEN),
  * a sampling row with temperature not > 0 (SPEC_DEVERR_TEMPERATURE), or a mode
- * other than 0/1 or a sampling row with draft_probs == NULL (SPEC_DEVERR_MODE)
- * gets out_tokens all -1 and accept_len -1.
+ * other than 0/1 (SPEC_DEVERR_MODE) gets out_tokens all -1 and accept_len -1.
  * Supported: k_draft <= 31; vocab <= 16 * 49152.
  */
 int spec_accept(const float* target_logits, const int32_t* draft_tokens,
@@ -247,6 +249,33 @@ int spec_commit_state(const float* snapshots, const int32_t* accept_len,
                       float* live_state, int32_t num_layers, int32_t batch,
                       int32_t num_slots, int64_t state_elems, int32_t* dev_err,
                       spec_stream_t stream);
+
+/* Checkpoint alignments of spec_commit_state_aligned. */
+#define SPEC_ALIGN_TOKEN 0 /* slot j holds the state after the step's token j      */
+#define SPEC_ALIGN_LAST 1  /* slot W-1 holds the state after the step's last token */
+
+/*
+ * Commit from a checkpoint window that may be wider than the step
+ * (onnxruntime-genai PR #2457: the window is described by a checkpoint count
+ * and an alignment, because the conv state writes slot j after local token j
+ * while GatedDeltaNet writes slot W-1 after the last token). A step of
+ * num_tokens = n tokens (k+1 for a verify step) fills a window of
+ * num_slots = W >= n slots; with m = accept_len[b] drafts accepted the kept
+ * state is the one after token m:
+ *
+ *   SPEC_ALIGN_TOKEN: live_state[l, b, :] = snapshots[l, b, m, :]
+ *   SPEC_ALIGN_LAST:  live_state[l, b, :] = snapshots[l, b, W - n + m, :]
+ *
+ * snapshots [L, B, W, state_elems] fp32; accept_len [B] int32; live_state
+ * [L, B, state_elems] fp32. With W = n both alignments equal spec_commit_state.
+ * A row with accept_len outside [0, n-1] keeps its live state and sets
+ * SPEC_DEVERR_ACCEPT_LEN. Returns SPEC_ERR_INVALID_ARG for n outside [1, W]
+ * or another alignment.
+ */
+int spec_commit_state_aligned(const float* snapshots, const int32_t* accept_len,
+                              float* live_state, int32_t num_layers, int32_t batch,
+                              int32_t num_slots, int64_t state_elems, int32_t num_tokens,
+                              int32_t alignment, int32_t* dev_err, spec_stream_t stream);
 
 #ifdef __cplusplus
 }

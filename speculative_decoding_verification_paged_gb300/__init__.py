@@ -94,6 +94,8 @@ def load_library():
         lib.spec_accept.restype = ctypes.c_int
         lib.spec_commit_state.argtypes = [P, P, P, i32, i32, i32, i64, P, P]
         lib.spec_commit_state.restype = ctypes.c_int
+        lib.spec_commit_state_aligned.argtypes = [P, P, P, i32, i32, i32, i64, i32, i32, P, P]
+        lib.spec_commit_state_aligned.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -242,4 +244,24 @@ def spec_commit_state(snapshots, accept_len, live_state, dev_err: Optional[torch
     rc = lib.spec_commit_state(_ptr(snapshots), _ptr(accept_len), _ptr(live_state), L, B, S, E,
                                _ptr(dev_err), _stream_handle(stream))
     _check("spec_commit_state", rc)
+    return live_state
+
+
+ALIGN_TOKEN, ALIGN_LAST = 0, 1
+
+
+def spec_commit_state_aligned(snapshots, accept_len, live_state, num_tokens: int, alignment: int,
+                              dev_err: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Commit from a checkpoint window [L, B, W, E] of a num_tokens-token step (see spec_verify.h):
+    slot accept_len[b] (ALIGN_TOKEN) or W - num_tokens + accept_len[b] (ALIGN_LAST)."""
+    lib = load_library()
+    _need(snapshots, "snapshots", torch.float32, 4)
+    _need(accept_len, "accept_len", torch.int32, 1)
+    _need(live_state, "live_state", torch.float32, 3)
+    L, B, W, E = snapshots.shape
+    if live_state.shape != (L, B, E) or accept_len.shape != (B,):
+        raise ValueError("inconsistent commit shapes")
+    rc = lib.spec_commit_state_aligned(_ptr(snapshots), _ptr(accept_len), _ptr(live_state), L, B, W, E,
+                                       int(num_tokens), int(alignment), _ptr(dev_err), _stream_handle(stream))
+    _check("spec_commit_state_aligned", rc)
     return live_state

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
 
   // ---- row validation (identical in every CTA of the cluster)
   const int md = p.mode[b];
-  bool valid = (md == SPEC_MODE_GREEDY) || (md == SPEC_MODE_SAMPLE && p.probs != nullptr);
+  bool valid = md == SPEC_MODE_GREEDY || md == SPEC_MODE_SAMPLE;
   int32_t err_bit = valid ? 0 : SPEC_DEVERR_MODE;
   for (int j = 0; j < k; ++j) {
     const int dj = d[j];
@@ -189,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
   // the values every decision needs are read once, up front, off the critical path
   if (!greedy && tid < k) {
     sh.l_draft[tid] = __ldg(p.logits + ((int64_t)b * R + tid) * V + d[tid]);
-    sh.q_draft[tid] = __ldg(p.probs + ((int64_t)b * k + tid) * V + d[tid]);
+    // without draft probabilities the draft distribution is one-hot at the drafted token
+    sh.q_draft[tid] = p.probs ? __ldg(p.probs + ((int64_t)b * k + tid) * V + d[tid]) : 1.f;
   }
   __syncthreads();
   uint32_t phase = 0;
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
         // (same 16-byte alignment rule as the bulk copy)
         if (p.prefetch && j < k) {
           bulk_prefetch_l2(row_ptr(j + 1), (uint32_t)n * 4u);
-          if (!greedy) bulk_prefetch_l2(p.probs + ((int64_t)b * k + j) * V + x0, (uint32_t)n * 4u);
+          if (!greedy && p.probs) bulk_prefetch_l2(p.probs + ((int64_t)b * k + j) * V + x0, (uint32_t)n * 4u);
         }
       }
       pending = true;
@@ -297,7 +298,10 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) qv[i][e] = 0.f;
         if (residual && off < n) {
-          if (vec) {
+          if (qrow == nullptr) {  // one-hot draft distribution at the rejected draft token
+#pragma unroll
+            for (int e = 0; e < 4; ++e) qv[i][e] = (x0 + off + e == d[pos]) ? 1.f : 0.f;
+          } else if (vec) {
             const float4 q4 = __ldg(reinterpret_cast<const float4*>(qrow + off));
             qv[i][0] = q4.x; qv[i][1] = q4.y; qv[i][2] = q4.z; qv[i][3] = q4.w;
           } else {
@@ -473,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
     }
     // ---- rejected at j: race over max(0, p_j - q_j), or over p_j if that is all zero
     const float f = fast_exp2((mx - M) * c2) / Z;  // e_x * f = p_j(x) on this slice
-    const float* qrow = p.probs + ((int64_t)b * k + j) * V + x0;
+    const float* qrow = p.probs ? p.probs + ((int64_t)b * k + j) * V + x0 : nullptr;
     if (!race(true, M, f, qrow, j, 0, j)) {
       // all-zero residual (rare): reload the logits over the overwritten slice and race over p_j
       __syncthreads();

@@ -20,19 +20,21 @@ constexpr int kThreads = 256;
 constexpr int kVecPerThread = 8;
 constexpr int kPiece = kThreads * kVecPerThread;  // float4 per CTA
 
+// The kept snapshot of row b is slot base + accept_len[b] of its `slots`-slot
+// window; accept_len must lie in [0, n_tokens).
 __global__ void __launch_bounds__(kThreads) commit_vec_kernel(const float4* __restrict__ snaps,
                                                               const int32_t* __restrict__ accept_len,
                                                               float4* __restrict__ live, int batch,
-                                                              int slots, int64_t vecs_per_state,
-                                                              int32_t* dev_err) {
+                                                              int slots, int base, int n_tokens,
+                                                              int64_t vecs_per_state, int32_t* dev_err) {
   const int64_t lb = blockIdx.y;  // layer * batch + row
   const int b = (int)(lb % batch);
   const int a = __ldg(accept_len + b);
-  if (a < 0 || a >= slots) {
+  if (a < 0 || a >= n_tokens) {
     if (blockIdx.x == 0 && lb == b && threadIdx.x == 0) raise_error(dev_err, SPEC_DEVERR_ACCEPT_LEN);
     return;
   }
-  const float4* src = snaps + (lb * slots + a) * vecs_per_state;
+  const float4* src = snaps + (lb * slots + base + a) * vecs_per_state;
   float4* dst = live + lb * vecs_per_state;
   const int64_t start = (int64_t)blockIdx.x * kPiece + threadIdx.x;
   float4 v[kVecPerThread];
@@ -52,15 +54,16 @@ __global__ void __launch_bounds__(kThreads) commit_vec_kernel(const float4* __re
 __global__ void __launch_bounds__(kThreads) commit_scalar_kernel(const float* __restrict__ snaps,
                                                                  const int32_t* __restrict__ accept_len,
                                                                  float* __restrict__ live, int batch, int slots,
-                                                                 int64_t elems, int32_t* dev_err) {
+                                                                 int base, int n_tokens, int64_t elems,
+                                                                 int32_t* dev_err) {
   const int64_t lb = blockIdx.y;
   const int b = (int)(lb % batch);
   const int a = __ldg(accept_len + b);
-  if (a < 0 || a >= slots) {
+  if (a < 0 || a >= n_tokens) {
     if (blockIdx.x == 0 && lb == b && threadIdx.x == 0) raise_error(dev_err, SPEC_DEVERR_ACCEPT_LEN);
     return;
   }
-  const float* src = snaps + (lb * slots + a) * elems;
+  const float* src = snaps + (lb * slots + base + a) * elems;
   float* dst = live + lb * elems;
   for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < elems; e += (int64_t)gridDim.x * kThreads)
     dst[e] = src[e];
@@ -71,33 +74,57 @@ __global__ void __launch_bounds__(kThreads) commit_scalar_kernel(const float* __
 
 using namespace specv;
 
-extern "C" int spec_commit_state(const float* snapshots, const int32_t* accept_len, float* live_state,
-                                 int32_t num_layers, int32_t batch, int32_t num_slots, int64_t state_elems,
-                                 int32_t* dev_err, spec_stream_t stream_) {
-  if (num_layers < 0 || batch < 0 || num_slots < 1 || state_elems < 0) return SPEC_ERR_INVALID_ARG;
+namespace specv {
+namespace cmt {
+
+static int launch(const float* snapshots, const int32_t* accept_len, float* live_state, int32_t num_layers,
+                  int32_t batch, int32_t num_slots, int64_t state_elems, int32_t base, int32_t n_tokens,
+                  int32_t* dev_err, cudaStream_t stream) {
   if (num_layers == 0 || batch == 0 || state_elems == 0) return SPEC_OK;
   if (!snapshots || !accept_len || !live_state) return SPEC_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)num_layers * batch;
   if (rows > 65535) return SPEC_ERR_UNSUPPORTED;
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   const bool vec = (state_elems % 4 == 0) && ((reinterpret_cast<uintptr_t>(snapshots) & 15) == 0) &&
                    ((reinterpret_cast<uintptr_t>(live_state) & 15) == 0);
   if (vec) {
     const int64_t vecs = state_elems / 4;
-    const int64_t pieces = (vecs + cmt::kPiece - 1) / cmt::kPiece;
+    const int64_t pieces = (vecs + kPiece - 1) / kPiece;
     if (pieces > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
     dim3 grid((unsigned)pieces, (unsigned)rows, 1);
-    cmt::commit_vec_kernel<<<grid, cmt::kThreads, 0, stream>>>(reinterpret_cast<const float4*>(snapshots),
-                                                               accept_len, reinterpret_cast<float4*>(live_state),
-                                                               batch, num_slots, vecs, dev_err);
+    commit_vec_kernel<<<grid, kThreads, 0, stream>>>(reinterpret_cast<const float4*>(snapshots), accept_len,
+                                                     reinterpret_cast<float4*>(live_state), batch, num_slots, base,
+                                                     n_tokens, vecs, dev_err);
   } else {
-    int64_t blocks = (state_elems + cmt::kThreads - 1) / cmt::kThreads;
+    int64_t blocks = (state_elems + kThreads - 1) / kThreads;
     if (blocks > 1024) blocks = 1024;
     dim3 grid((unsigned)blocks, (unsigned)rows, 1);
-    cmt::commit_scalar_kernel<<<grid, cmt::kThreads, 0, stream>>>(snapshots, accept_len, live_state, batch,
-                                                                  num_slots, state_elems, dev_err);
+    commit_scalar_kernel<<<grid, kThreads, 0, stream>>>(snapshots, accept_len, live_state, batch, num_slots, base,
+                                                        n_tokens, state_elems, dev_err);
   }
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
+}
+
+}  // namespace cmt
+}  // namespace specv
+
+extern "C" int spec_commit_state(const float* snapshots, const int32_t* accept_len, float* live_state,
+                                 int32_t num_layers, int32_t batch, int32_t num_slots, int64_t state_elems,
+                                 int32_t* dev_err, spec_stream_t stream_) {
+  if (num_layers < 0 || batch < 0 || num_slots < 1 || state_elems < 0) return SPEC_ERR_INVALID_ARG;
+  return cmt::launch(snapshots, accept_len, live_state, num_layers, batch, num_slots, state_elems, 0, num_slots,
+                     dev_err, reinterpret_cast<cudaStream_t>(stream_));
+}
+
+extern "C" int spec_commit_state_aligned(const float* snapshots, const int32_t* accept_len, float* live_state,
+                                         int32_t num_layers, int32_t batch, int32_t num_slots,
+                                         int64_t state_elems, int32_t num_tokens, int32_t alignment,
+                                         int32_t* dev_err, spec_stream_t stream_) {
+  if (num_layers < 0 || batch < 0 || num_slots < 1 || state_elems < 0) return SPEC_ERR_INVALID_ARG;
+  if (num_tokens < 1 || num_tokens > num_slots) return SPEC_ERR_INVALID_ARG;
+  if (alignment != SPEC_ALIGN_TOKEN && alignment != SPEC_ALIGN_LAST) return SPEC_ERR_INVALID_ARG;
+  const int32_t base = alignment == SPEC_ALIGN_TOKEN ? 0 : num_slots - num_tokens;
+  return cmt::launch(snapshots, accept_len, live_state, num_layers, batch, num_slots, state_elems, base, num_tokens,
+                     dev_err, reinterpret_cast<cudaStream_t>(stream_));
 }
 
 extern "C" const char* spec_status_string(int status) {

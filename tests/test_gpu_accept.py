@@ -67,6 +67,50 @@ def test_accept_greedy_without_draft_probs(sv, oracle_mod):
     assert err == 0 and np.array_equal(tok, rt) and np.array_equal(alen, ra)
 
 
+@pytest.mark.parametrize("name", ["tiny", "llama8b_eagle3", "serving128"])
+def test_accept_sampling_without_draft_probs(sv, oracle_mod, name):
+    """No draft distribution: one-hot q at the drafted token, same decisions as the oracle."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_accept_inputs(w, device=DEV)
+    tok, alen, err = run_accept(sv, inp, inp["mode"], probs=None)
+    assert err == 0
+    rt, ra, margin, gap, rc = oracle_accept(oracle_mod, inp, inp["mode"], probs=None)
+    assert rc == 0
+    bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
+    assert bad == 0, f"{bad} rows differ from the oracle"
+    # a rejected draft is never re-emitted as the correction token
+    d = inp["draft_tokens"].cpu().numpy()
+    samp = inp["mode"].cpu().numpy() == 1
+    for b in np.nonzero(samp & (alen < w.k_draft))[0]:
+        assert tok[b, alen[b]] != d[b, alen[b]]
+
+
+def test_accept_without_draft_probs_distribution(sv):
+    """Over 10^6 rows: a draft is kept with probability p(d); a rejection follows p
+    with d removed."""
+    B, k, V = 1_000_000, 1, 8
+    rng = np.random.default_rng(6)
+    l = rng.normal(0, 1.0, (k + 1, V)).astype(np.float32)
+    L = torch.tensor(l, device=DEV).expand(B, k + 1, V).contiguous()
+    d = torch.full((B, k), 3, dtype=torch.int32, device=DEV)
+    inp = {"target_logits": L, "draft_tokens": d, "draft_probs": None, "philox_seed": 99,
+           "temperature": torch.ones(B, device=DEV)}
+    tok, alen, err = run_accept(sv, inp, torch.ones(B, dtype=torch.int32, device=DEV), probs=None)
+    assert err == 0
+    p0 = np.exp(l[0].astype(np.float64))
+    p0 /= p0.sum()
+    acc = alen == 1
+    assert abs(acc.mean() - p0[3]) < 5 * np.sqrt(p0[3] * (1 - p0[3]) / B)
+    rej = tok[~acc, 0]
+    assert np.all(rej != 3)
+    resid = p0.copy()
+    resid[3] = 0.0
+    resid /= resid.sum()
+    counts = np.bincount(rej, minlength=V).astype(np.float64)
+    keep = resid > 0
+    assert stats.chisquare(counts[keep], resid[keep] * counts.sum()).pvalue > 1e-3
+
+
 def test_accept_greedy_is_sequential_greedy(sv):
     """Emitted tokens = argmax of each target row, cut after the first draft miss."""
     B, k, V = 512, 5, 4000

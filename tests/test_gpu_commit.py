@@ -58,3 +58,33 @@ def test_commit_unaligned_size_and_invalid_row(sv):
             assert torch.equal(live[:, b], snaps[:, b, alen[b]])
         else:
             assert torch.all(live[:, b] == 7.0)
+
+
+@pytest.mark.parametrize("alignment", [0, 1], ids=["token", "last"])
+@pytest.mark.parametrize("E", [4096, 1001], ids=["vec", "scalar"])
+def test_commit_aligned_window_matches_oracle(sv, oracle_mod, alignment, E):
+    """A checkpoint window wider than the step (W = 7 slots, n = 4 tokens), both
+    alignments, vectorised and element-wise copies; a bad accept_len is skipped."""
+    rng = np.random.default_rng(40 + alignment)
+    L, B, W, n = 3, 9, 7, 4
+    snaps = torch.tensor(rng.standard_normal((L, B, W, E)).astype(np.float32), device=DEV)
+    alen_np = rng.integers(0, n, B).astype(np.int32)
+    alen_np[0], alen_np[1], alen_np[2] = 0, n - 1, n  # both ends and one out of range
+    alen = torch.tensor(alen_np, device=DEV)
+    live = torch.full((L, B, E), 5.0, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sv.spec_commit_state_aligned(snaps, alen, live, n, alignment, dev_err=err)
+    torch.cuda.synchronize()
+    ref = np.full((L, B, E), 5.0, np.float32)
+    rc = oracle_mod.commit_state_aligned(snaps.cpu().numpy(), alen_np, ref, n, alignment, check=False)
+    assert rc != 0 and int(err.item()) & sv.DEVERR["accept_len"]
+    assert np.array_equal(live.cpu().numpy(), ref)
+
+
+def test_commit_aligned_rejects_bad_arguments(sv):
+    snaps = torch.zeros((1, 2, 3, 8), device=DEV)
+    live = torch.zeros((1, 2, 8), device=DEV)
+    alen = torch.zeros(2, dtype=torch.int32, device=DEV)
+    for n, alignment in ((4, 0), (0, 1), (2, 5)):
+        with pytest.raises(RuntimeError):
+            sv.spec_commit_state_aligned(snaps, alen, live, n, alignment)
