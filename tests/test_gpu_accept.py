@@ -111,6 +111,26 @@ def test_accept_without_draft_probs_distribution(sv):
     assert stats.chisquare(counts[keep], resid[keep] * counts.sum()).pvalue > 1e-3
 
 
+@pytest.mark.parametrize("mode", ["sample", "greedy"])
+def test_accept_longest_draft(sv, oracle_mod, mode):
+    """k = 31, the longest supported draft, with near-copy drafts so rows run deep."""
+    w = wl.WORKLOADS["tiny"].replace(batch=48, k_draft=31, vocab=3000, noise_sigma=0.2)
+    inp = wl.make_accept_inputs(w, device=DEV, mode=mode)
+    if mode == "greedy":
+        # row b copies the target's argmax for its first b % 32 positions
+        am = inp["target_logits"][:, :w.k_draft].argmax(-1).to(torch.int32)
+        depth = torch.arange(w.batch, device=DEV) % (w.k_draft + 1)
+        keep = torch.arange(w.k_draft, device=DEV)[None, :] < depth[:, None]
+        inp["draft_tokens"] = torch.where(keep, am, inp["draft_tokens"]).contiguous()
+    tok, alen, err = run_accept(sv, inp, inp["mode"])
+    assert err == 0
+    rt, ra, margin, gap, rc = oracle_accept(oracle_mod, inp, inp["mode"])
+    assert rc == 0
+    bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
+    assert bad == 0, f"{bad} rows differ from the oracle"
+    assert alen.max() >= 2  # some rows accept several drafts
+
+
 def test_accept_greedy_is_sequential_greedy(sv):
     """Emitted tokens = argmax of each target row, cut after the first draft miss."""
     B, k, V = 512, 5, 4000

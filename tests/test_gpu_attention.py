@@ -136,6 +136,37 @@ def test_attention_default_kernel_choice(sv, oracle_mod, monkeypatch, name):
     assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
 
 
+def _random_shape(rng):
+    D = int(rng.choice([64, 128, 256]))
+    bs = int(rng.choice([16, 32, 64, 128]))
+    while True:
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        G = int(rng.choice([1, 2, 3, 4, 6, 8, 16]))
+        k = int(rng.integers(1, 8))
+        if (k + 1) * G <= 64 and Hkv * G <= 64:
+            break
+    B = int(rng.integers(1, 9))
+    ctx = tuple(int(c) for c in rng.integers(k + 1, 2600, B))
+    return B, ctx, bs, Hkv * G, Hkv, D, k
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_attention_random_shapes(sv, oracle_mod, attn_kernel, seed):
+    """Seeded random shapes: every head dim, block size, GQA group and draft length
+    within the supported range, ragged contexts, both kernels where D = 128."""
+    rng = np.random.default_rng(1000 + seed)
+    B, ctx, bs, Hq, Hkv, D, k = _random_shape(rng)
+    if D != 128 and attn_kernel == "tc":
+        pytest.skip("one kernel for this head dim")
+    w = wl.Workload(name=f"rand{seed}", batch=B, ctx_lens=ctx, block_size=bs, num_q_heads=Hq,
+                    num_kv_heads=Hkv, head_dim=D, k_draft=k, seed=seed)
+    a = wl.make_attention_inputs(w, device=DEV)
+    out, err = run_attention(sv, a, w)
+    assert err == 0
+    mx, rel = attention_errors(out.cpu().numpy(), oracle_attention_for(oracle_mod, a))
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (w, mx, rel)
+
+
 def test_attention_is_deterministic_and_reuses_workspace(sv, attn_kernel):
     w = wl.WORKLOADS["llama8b_eagle3"].replace(batch=8, ctx_lens=(2048,) * 8)
     a = wl.make_attention_inputs(w, device=DEV)

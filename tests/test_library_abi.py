@@ -92,3 +92,10 @@ def test_accept_and_commit_host_validation(lib):
     assert com(snaps=None) == -1
     assert com(L=0) == 0
     assert com(L=1000, B=1000) == -2
+    al = lambda n=3, a=1, W=4, L=2, snaps=fake: lib.spec_commit_state_aligned(snaps, fake, fake, L, 2, W, 16, n, a,
+                                                                               None, None)
+    assert al(n=5) == -1      # step longer than the window
+    assert al(n=0) == -1
+    assert al(a=2) == -1      # unknown alignment
+    assert al(snaps=None) == -1
+    assert al(L=0) == 0
