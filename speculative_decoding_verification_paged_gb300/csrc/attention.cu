@@ -31,6 +31,12 @@
 //    independent accumulator chains per warp. P is split into a bf16 high part
 //    and a bf16 remainder and both are multiplied with V, so PV keeps ~16
 //    mantissa bits of P; softmax statistics and the output stay fp32.
+//  * At the end of a unit the warps that split a tile's keys write their
+//    partial outputs to the freed stage and all consumer threads merge them,
+//    one (row, 16-column) segment each.
+//  * Head dim 128 with 32 or more packed rows runs on a second kernel in this
+//    file, on 5th-generation tensor cores (tcgen05, tensor memory): see the
+//    comment before namespace tc. The host picks one per call.
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -765,14 +771,16 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, MT>::MIN_BLOCKS) verify_atten
 // The keys are the MMA's M dimension (128 per tile) and the packed query rows
 // are N (16, 32 or 64), so every M = 128 MMA is fully used for any row count:
 //   S^T[128 keys x N] = K[128 x 128] . Q^T            (K, Q K-major in smem)
-//   O^T[128 d x N]   += V^T[128 x 128 keys] . P^T     (V MN-major, P K-major)
-// with S^T and O^T in tensor memory. Warp 0 stages K/V/Q with TMA, warp 1
-// issues the MMAs (one thread), warps 2-5 run the softmax: each owns one
-// 32-lane quarter of tensor memory, i.e. 32 keys of S^T and 32 dims of O^T.
-// P is written to shared memory as a bf16 high part and a bf16 remainder and
-// both are multiplied with V. The running row max may lag by up to 8 (log2
-// units); a tile that exceeds it takes the slow path: exact row max, and the
-// accumulated O^T and row sums are rescaled in place.
+//   O^T[128 d x N]   += V^T[128 x 128 keys] . P^T     (V and P MN-major)
+// with S^T (two buffers) and O^T in tensor memory. Warp 0 stages K/V/Q with
+// TMA, warp 1 issues the MMAs (one thread; QK of tile i+1 before P.V of tile
+// i), warps 2-9 run the softmax in two warpgroups, each owning half of the
+// rows; a warp reads the 32-lane quarter of tensor memory that its index
+// selects, i.e. 32 keys of S^T and 32 dims of O^T. P is written to shared
+// memory as a bf16 high part and a bf16 remainder and both are multiplied with
+// V. The running row max may lag by up to 8 (log2 units); a tile that exceeds
+// it takes the slow path: exact row max, and the accumulated O^T and row sums
+// are rescaled in place.
 // ---------------------------------------------------------------------------
 namespace tc {
 
