@@ -15,7 +15,9 @@
 // Positions are processed in order and the row stops at the first rejection,
 // so logits past it are never read (early exit). For each position every CTA
 // pulls its slice into shared memory with one bulk asynchronous copy (TMA,
-// mbarrier completion) while the next position's slice is prefetched into L2,
+// mbarrier completion; position 0's copy is issued first thing, before the row
+// is validated), prefetches into L2 what comes next once the slice has landed
+// (the next position, and the draft probabilities a rejection would read),
 // reduces it (max / sum of exp / argmax) with warp shuffles, and publishes a
 // partial that every CTA of the cluster reads through distributed shared
 // memory, in rank order, so all CTAs reach bit-identical decisions without
@@ -74,6 +76,7 @@ struct Shared {
   float wf[kWarps];
   float wg[kWarps];
   int32_t wi[kWarps];
+  int32_t draft[kMaxK];  // the row's draft tokens
   float l_draft[kMaxK];  // target logit of each draft token, read once at start
   float q_draft[kMaxK];  // draft probability of each draft token
   uint64_t bar;
@@ -152,61 +155,17 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
   const int k = p.k, R = k + 1, V = p.vocab;
   const int x0 = rank * p.slice;
   const int n = min(p.slice, V - x0);  // >= 1 by construction of csize
-  const int32_t* d = p.drafts + (int64_t)b * k;
-
-  // ---- row validation (identical in every CTA of the cluster)
-  const int md = p.mode[b];
-  bool valid = md == SPEC_MODE_GREEDY || md == SPEC_MODE_SAMPLE;
-  int32_t err_bit = valid ? 0 : SPEC_DEVERR_MODE;
-  for (int j = 0; j < k; ++j) {
-    const int dj = d[j];
-    if (dj < 0 || dj >= V) { valid = false; err_bit |= SPEC_DEVERR_TOKEN; }
-  }
-  float T = 1.f;
-  if (valid && md == SPEC_MODE_SAMPLE) {
-    T = p.temperature[b];
-    if (!(T > 0.f) || !isfinite(T)) { valid = false; err_bit |= SPEC_DEVERR_TEMPERATURE; }
-  }
-  if (!valid) {
-    if (rank == 0 && tid == 0) {
-      raise_error(p.dev_err, err_bit);
-      for (int j = 0; j < R; ++j) p.out_tokens[(int64_t)b * R + j] = -1;
-      p.accept_len[b] = -1;
-    }
-    return;  // uniform across the cluster: no CTA touches another's shared memory
-  }
-  const bool greedy = md == SPEC_MODE_GREEDY;
-  const float c2 = (1.0f / T) * 1.4426950408889634f;  // logit -> log2 units of p
   const int lane = tid & 31;
   bool bulk = p.bulk != 0;
   const bool vec = bulk;  // 16-byte aligned slices
-
-  auto row_ptr = [&](int j) { return p.logits + ((int64_t)b * R + j) * V + x0; };
-  if (tid == 0) {
-    mbar_init(&sh.bar, 1);
-    fence_mbar_init();
-  }
-  // the values every decision needs are read once, up front, off the critical path
-  if (!greedy && tid < k) {
-    sh.l_draft[tid] = __ldg(p.logits + ((int64_t)b * R + tid) * V + d[tid]);
-    // without draft probabilities the draft distribution is one-hot at the drafted token
-    sh.q_draft[tid] = p.probs ? __ldg(p.probs + ((int64_t)b * k + tid) * V + d[tid]) : 1.f;
-  }
-  __syncthreads();
   uint32_t phase = 0;
   bool pending = false;  // a bulk copy was issued and not yet observed complete
-
+  auto row_ptr = [&](int j) { return p.logits + ((int64_t)b * R + j) * V + x0; };
   auto issue_row = [&](int j) {
     if (bulk) {
       if (tid == 0) {
         mbar_arrive_expect_tx(&sh.bar, (uint32_t)n * 4u);
         bulk_g2s(smem_u32(buf), row_ptr(j), (uint32_t)n * 4u, &sh.bar);
-        // the next position is likely needed: start pulling it into L2 now
-        // (same 16-byte alignment rule as the bulk copy)
-        if (p.prefetch && j < k) {
-          bulk_prefetch_l2(row_ptr(j + 1), (uint32_t)n * 4u);
-          if (!greedy && p.probs) bulk_prefetch_l2(p.probs + ((int64_t)b * k + j) * V + x0, (uint32_t)n * 4u);
-        }
       }
       pending = true;
     } else {
@@ -214,7 +173,57 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
       for (int x = tid; x < n; x += kThreads) buf[x] = src[x];
     }
   };
-  auto wait_row = [&]() {
+  // Position 0 is read whatever the row holds, so its copy starts before anything
+  // else (the barrier is initialised by the issuing thread; the others first wait
+  // on it after the block barrier below).
+  if (tid == 0) {
+    mbar_init(&sh.bar, 1);
+    fence_mbar_init();
+  }
+  if (bulk) issue_row(0);
+
+  // ---- row validation (identical in every CTA of the cluster): the mode, the
+  // temperature and the drafts (lane j holds d_j, k <= 31) are loaded together
+  const int md = p.mode[b];
+  const float t_row = p.temperature[b];
+  const int d_lane = lane < k ? p.drafts[(int64_t)b * k + lane] : 0;
+  const bool token_bad = __any_sync(0xffffffffu, lane < k && (d_lane < 0 || d_lane >= V));
+  bool valid = md == SPEC_MODE_GREEDY || md == SPEC_MODE_SAMPLE;
+  int32_t err_bit = valid ? 0 : SPEC_DEVERR_MODE;
+  if (token_bad) { valid = false; err_bit |= SPEC_DEVERR_TOKEN; }
+  float T = 1.f;
+  if (valid && md == SPEC_MODE_SAMPLE) {
+    T = t_row;
+    if (!(T > 0.f) || !isfinite(T)) { valid = false; err_bit |= SPEC_DEVERR_TEMPERATURE; }
+  }
+  if (tid < k) sh.draft[tid] = d_lane;
+  __syncthreads();
+  if (!valid) {
+    if (rank == 0 && tid == 0) {
+      raise_error(p.dev_err, err_bit);
+      for (int j = 0; j < R; ++j) p.out_tokens[(int64_t)b * R + j] = -1;
+      p.accept_len[b] = -1;
+    }
+    // the copy of position 0 must land before this CTA's shared memory goes away
+    if (pending && !mbar_wait_bounded(&sh.bar, phase) && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+    return;  // uniform across the cluster: no CTA touches another's shared memory
+  }
+  const int32_t* d = sh.draft;
+  const bool greedy = md == SPEC_MODE_GREEDY;
+  const float c2 = (1.0f / T) * 1.4426950408889634f;  // logit -> log2 units of p
+  // The target logit and draft probability of each draft token are first read
+  // after the block barriers of position 0's reductions: they load while the
+  // slice is in flight.
+  if (!greedy && tid < k) {
+    sh.l_draft[tid] = __ldg(p.logits + ((int64_t)b * R + tid) * V + d_lane);
+    // without draft probabilities the draft distribution is one-hot at the drafted token
+    sh.q_draft[tid] = p.probs ? __ldg(p.probs + ((int64_t)b * k + tid) * V + d_lane) : 1.f;
+  }
+
+  // Wait for position j's slice; once it has landed, pull what position j may
+  // need next into L2 (the next position, and the draft probabilities a
+  // rejection at j reads), so these prefetches never compete with the slice.
+  auto wait_row = [&](int j) {
     if (bulk && pending) {
       const bool ok = mbar_wait_bounded(&sh.bar, phase);
       phase ^= 1u;
@@ -223,6 +232,11 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
         if (tid == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
         bulk = false;  // stop issuing copies; later rows use plain loads
       }
+    }
+    // same 16-byte alignment rule as the bulk copy
+    if (bulk && p.prefetch && tid == 0 && j < k) {
+      bulk_prefetch_l2(row_ptr(j + 1), (uint32_t)n * 4u);
+      if (!greedy && p.probs) bulk_prefetch_l2(p.probs + ((int64_t)b * k + j) * V + x0, (uint32_t)n * 4u);
     }
     __syncthreads();
   };
@@ -408,9 +422,9 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
     return true;
   };
 
-  issue_row(0);
+  if (!bulk) issue_row(0);  // with bulk copies position 0 is already in flight
   for (int j = 0; j <= k; ++j) {
-    wait_row();
+    wait_row(j);
     if (greedy) {
       // ---- argmax of the slice, then of the cluster (ranks are in vocab order)
       float v = -INFINITY;
