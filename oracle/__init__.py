@@ -16,7 +16,9 @@ ctx - (k+1) + i; GQA groups are contiguous; softmax scale 1/sqrt(D); greedy
 ties go to the lowest index; acceptance compares u*q < p; the residual falls
 back to p when max(0, p-q) is all zero; without draft probabilities q is one-hot
 at the drafted token; the correction/bonus draw is an
-exponential race keyed by Philox words as documented in spec_verify.h.
+exponential race keyed by Philox words as documented in spec_verify.h; the
+zero-copy commit exchanges the live row with the chosen checkpoint row of a
+state pool.
 """
 
 from __future__ import annotations
@@ -92,6 +94,8 @@ def _load():
         lib.oracle_commit_state.restype = i32
         lib.oracle_commit_state_aligned.argtypes = [P, P, P, i32, i32, i32, i64, i32, i32, i32]
         lib.oracle_commit_state_aligned.restype = i32
+        lib.oracle_commit_select.argtypes = [P, P, P, i32, i32, i32, i32, i32]
+        lib.oracle_commit_select.restype = i32
         _lib = lib
         return lib
 
@@ -217,6 +221,26 @@ def commit_state_aligned(snapshots, accept_len, live, n_tokens: int, alignment: 
     assert live.shape == (L, B, E) and al.shape == (B,)
     rc = lib.oracle_commit_state_aligned(_ptr(sn), _ptr(al), _ptr(live), L, B, W, E, int(n_tokens),
                                          int(alignment), n_threads)
+    if check and rc != 0:
+        raise OracleError(rc)
+    return rc
+
+
+def commit_select(accept_len, live_row, ckpt_rows, n_tokens: int, alignment: int, *, check: bool = True):
+    """Commit by row selection in a state pool: live_row [L,B] and ckpt_rows [L,B,W]
+    int32 pool-row indices, updated in place.
+
+    The slot of the accepted prefix (as in commit_state_aligned) trades places
+    with the live row: live_row[l,b] <-> ckpt_rows[l,b,slot]. Returns the status.
+    """
+    lib = _load()
+    al = _c(accept_len, np.int32)
+    for t in (live_row, ckpt_rows):
+        assert t.dtype == np.int32 and t.flags.c_contiguous
+    L, B = live_row.shape
+    assert ckpt_rows.shape[:2] == (L, B) and al.shape == (B,)
+    W = ckpt_rows.shape[2]
+    rc = lib.oracle_commit_select(_ptr(al), _ptr(live_row), _ptr(ckpt_rows), L, B, W, int(n_tokens), int(alignment))
     if check and rc != 0:
         raise OracleError(rc)
     return rc

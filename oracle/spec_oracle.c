@@ -490,6 +490,41 @@ int oracle_commit_state_aligned(const float* snapshots, const int32_t* accept_le
   return status;
 }
 
+/*
+ * Commit by staging a different source row (onnxruntime-genai PR #2457,
+ * CommitPrefix note: rolling back a rejected draft only needs the state pool
+ * to stage another row, the checkpoint of the accepted prefix, instead of the
+ * step's final state). The states are rows of a pool; live_row[l,b] names the
+ * row holding the live state of (l, b) and ckpt_rows[l,b,:] the W rows of its
+ * checkpoint window. Committing slot s (picked exactly as in
+ * oracle_commit_state_aligned) exchanges live_row[l,b] and ckpt_rows[l,b,s]:
+ * the checkpoint row becomes the live row and the old live row becomes the
+ * window's free slot. No state is read or written; a row with accept_len
+ * outside [0, n-1] keeps both entries.
+ */
+int oracle_commit_select(const int32_t* accept_len, int32_t* live_row, int32_t* ckpt_rows, int L, int B, int W,
+                         int n, int alignment) {
+  if (!accept_len || !live_row || !ckpt_rows || L < 0 || B < 0 || W < 1) return ORACLE_ERR_ARG;
+  if (n < 1 || n > W || (alignment != 0 && alignment != 1)) return ORACLE_ERR_ARG;
+  const int base = alignment == 0 ? 0 : W - n;
+  int status = ORACLE_OK;
+  for (int l = 0; l < L; ++l) {
+    for (int b = 0; b < B; ++b) {
+      const int m = accept_len[b];
+      if (m < 0 || m >= n) {
+        status = ORACLE_ERR_ACCEPT_LEN;
+        continue;
+      }
+      const int64_t unit = (int64_t)l * B + b;
+      int32_t* slot = ckpt_rows + unit * W + base + m;
+      const int32_t chosen = *slot;
+      *slot = live_row[unit];
+      live_row[unit] = chosen;
+    }
+  }
+  return status;
+}
+
 int oracle_commit_state(const float* snapshots, const int32_t* accept_len, float* live, int L, int B,
                         int S, int64_t E, int n_threads) {
   if (!snapshots || !accept_len || !live || L < 0 || B < 0 || S < 1 || E < 0) return ORACLE_ERR_ARG;

@@ -549,6 +549,63 @@ def test_commit_aligned_windows(oracle_mod):
     assert rc != 0 and np.all(live[:, 2] == 9.0)
 
 
+def _pool_tables(rng, L, B, W):
+    """A pool of L*B*(W+1) rows dealt out at random: one live row and W window rows per (l, b)."""
+    perm = rng.permutation(L * B * (W + 1)).astype(np.int32)
+    return perm[:L * B].reshape(L, B).copy(), perm[L * B:].reshape(L, B, W).copy()
+
+
+def test_commit_select_stages_the_copied_state(oracle_mod):
+    """Selecting the checkpoint row leaves, as the live state of every (l, b), exactly
+    the state the copying commit writes; rows never move between (l, b) units, the
+    tables stay a permutation of the pool, and a row with an invalid accept_len
+    keeps both tables."""
+    rng = np.random.default_rng(5)
+    L, B, W, E, n = 3, 7, 6, 5, 4
+    pool = rng.standard_normal((L * B * (W + 1), E)).astype(np.float32)
+    for alignment in (0, 1):
+        live_row, ckpt_rows = _pool_tables(rng, L, B, W)
+        alen = rng.integers(0, n, B).astype(np.int32)
+        alen[2] = n  # out of range: skipped and reported
+        expect = pool[live_row].copy()
+        rc_copy = oracle_mod.commit_state_aligned(pool[ckpt_rows], alen, expect, n, alignment, check=False)
+        lr, cr = live_row.copy(), ckpt_rows.copy()
+        rc = oracle_mod.commit_select(alen, lr, cr, n, alignment, check=False)
+        assert rc == rc_copy != 0
+        assert np.array_equal(pool[lr], expect)
+        assert np.array_equal(lr[:, 2], live_row[:, 2]) and np.array_equal(cr[:, 2], ckpt_rows[:, 2])
+        for l in range(L):
+            for b in range(B):
+                before = np.sort(np.append(ckpt_rows[l, b], live_row[l, b]))
+                after = np.sort(np.append(cr[l, b], lr[l, b]))
+                assert np.array_equal(before, after)
+                assert lr[l, b] not in cr[l, b]
+
+
+def test_commit_select_follows_copying_commit_over_steps(oracle_mod):
+    """A run of verify steps: each writes its checkpoints into the window rows (a
+    function of the live state it starts from and fresh inputs) and commits. The
+    pool's live rows track, bit for bit, a second run that copies states, so no
+    step's checkpoint writes ever reach the live state it started from."""
+    rng = np.random.default_rng(8)
+    L, B, W, E, n = 2, 5, 5, 3, 4
+    pool = np.zeros((L * B * (W + 1), E), np.float32)
+    live_row, ckpt_rows = _pool_tables(rng, L, B, W)
+    live_copy = rng.standard_normal((L, B, E)).astype(np.float32)
+    pool[live_row] = live_copy
+    for step in range(6):
+        alignment = step % 2
+        inputs = rng.standard_normal((L, B, W, E)).astype(np.float32)
+        # checkpoints of this step: the starting state plus a running sum of inputs
+        snaps_copy = live_copy[:, :, None, :] + np.cumsum(inputs, axis=2)
+        pool[ckpt_rows] = pool[live_row][:, :, None, :] + np.cumsum(inputs, axis=2)
+        assert np.array_equal(pool[ckpt_rows], snaps_copy)
+        alen = rng.integers(0, n, B).astype(np.int32)
+        oracle_mod.commit_state_aligned(snaps_copy.astype(np.float32), alen, live_copy, n, alignment)
+        oracle_mod.commit_select(alen, live_row, ckpt_rows, n, alignment)
+        assert np.array_equal(pool[live_row], live_copy)
+
+
 def test_commit_skips_invalid_rows(oracle_mod):
     rng = np.random.default_rng(21)
     L, B, S, E = 2, 3, 4, 8
