@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--commit", default="copy", choices=["copy", "select"],
+                    help="recurrent-state commit: copy the kept checkpoint into the live state, or select it "
+                         "in place by exchanging state-pool row indices (zero-copy)")
     ap.add_argument("--gdn-layers", type=int, default=None,
                     help="override the workload's recurrent-state layer count (small profiler captures); "
                          "the line's config reports the count used")
@@ -119,8 +122,23 @@ def accept_bytes(w, modes, accept_len):
     return total
 
 
-def commit_bytes(w):
-    return 2 * w.gdn_layers * w.batch * w.state_elems * 4 if w.gdn_layers else 0
+def commit_bytes(w, commit="copy"):
+    if not w.gdn_layers:
+        return 0
+    if commit == "select":  # per (layer, row): accept_len, live_row and one window index read, two written
+        return w.gdn_layers * w.batch * 5 * 4
+    return 2 * w.gdn_layers * w.batch * w.state_elems * 4
+
+
+def select_tables(w, dev):
+    """State-pool index tables for the zero-copy commit: (layer, row) unit u owns pool
+    rows u*(W+1) (live) and u*(W+1)+1 .. u*(W+1)+W (its checkpoint window, W = k+1)."""
+    W = w.rows
+    units = torch.arange(w.gdn_layers * w.batch, dtype=torch.int32, device=dev) * (W + 1)
+    live_row = units.view(w.gdn_layers, w.batch).clone()
+    ckpt_rows = (units.view(-1, 1) + 1 + torch.arange(W, dtype=torch.int32, device=dev)).view(
+        w.gdn_layers, w.batch, W).contiguous()
+    return live_row, ckpt_rows
 
 
 # --------------------------------------------------------------------------
@@ -214,7 +232,9 @@ def run_native(args, world, rank, local):
     mode = args.mode or w.mode
     a = wl.make_attention_inputs(w, device=dev, seed=w.seed + 1000 * rank)
     acc_in = wl.make_accept_inputs(w, device=dev, seed=w.seed + 1000 * rank, mode=mode)
-    g = wl.make_gdn_inputs(w, device=dev, seed=w.seed + 1000 * rank) if w.gdn_layers else None
+    select = bool(w.gdn_layers) and args.commit == "select"
+    g = wl.make_gdn_inputs(w, device=dev, seed=w.seed + 1000 * rank) if w.gdn_layers and not select else None
+    tables = select_tables(w, dev) if select else None
     B, R = w.batch, w.rows
     out = torch.empty((B, R, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
     ws = sv.new_attention_workspace(
@@ -235,7 +255,9 @@ def run_native(args, world, rank, local):
                        acc_in["philox_seed"], acc_in["mode"], acc_in["temperature"], toks, alen, dev_err=err)
 
     def commit():
-        if g is not None:
+        if tables is not None:
+            sv.spec_commit_select(alen, tables[0], tables[1], w.rows, sv.ALIGN_TOKEN, dev_err=err)
+        elif g is not None:
             sv.spec_commit_state(g["snapshots"], alen, g["live_state"], dev_err=err)
 
     def step():
@@ -243,7 +265,7 @@ def run_native(args, world, rank, local):
         accept()
         commit()
 
-    launches_per_step = 1 + 1 + (1 if g is not None else 0)
+    launches_per_step = 1 + 1 + (1 if w.gdn_layers else 0)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -257,7 +279,7 @@ def run_native(args, world, rank, local):
     side.wait_stream(stream)
     with torch.cuda.stream(side):
         for name, fn in (("step", step), ("attention", attention), ("accept", accept), ("commit", commit)):
-            if name == "commit" and g is None:
+            if name == "commit" and not w.gdn_layers:
                 continue
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=side):
@@ -313,15 +335,16 @@ def run_native(args, world, rank, local):
     ctx = a["ctx_lens"].cpu().numpy()
     ab = attention_bytes(w, ctx)
     cb = accept_bytes(w, acc_in["mode"].cpu().numpy(), alen_h)
-    mb = commit_bytes(w)
+    mb = commit_bytes(w, "select" if select else "copy")
     ta, tc, tm = statistics.mean(t_attn), statistics.mean(t_acc), statistics.mean(t_cmt)
     kernels = {
         "attention": {"ms": ta, "bytes": ab, "GBps": ab / ta / 1e6, "frac": ab / ta / 1e6 / peak},
         "accept": {"ms": tc, "bytes": cb, "GBps": cb / tc / 1e6, "frac": cb / tc / 1e6 / peak,
                    "full_read_bytes": w.batch * 4 * w.vocab * (R + w.k_draft)},
     }
-    if g is not None:
-        kernels["commit"] = {"ms": tm, "bytes": mb, "GBps": mb / tm / 1e6, "frac": mb / tm / 1e6 / peak}
+    if w.gdn_layers:
+        kernels["commit"] = {"ms": tm, "bytes": mb, "GBps": mb / tm / 1e6, "frac": mb / tm / 1e6 / peak,
+                             "kind": "select" if select else "copy"}
     dominant = max(kernels, key=lambda k: kernels[k]["ms"])
     dk = kernels[dominant]
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["GBps"], "peak": peak, "unit": "GB/s",
@@ -330,7 +353,7 @@ def run_native(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(sv, w, a, acc_in, g, out, ws, toks, alen, err, dev, args, flush)
+        e2e = run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -340,6 +363,8 @@ def run_native(args, world, rank, local):
                    "ctx": list(w.ctx_range) if w.ctx_range else sorted(set(w.ctx_lens)),
                    "block_size": w.block_size, "heads": [w.num_q_heads, w.num_kv_heads], "head_dim": w.head_dim,
                    "vocab": w.vocab, "gdn_layers": w.gdn_layers, "parallelism": f"replicas x{world}",
+                   **({"commit": "select (zero-copy: pool-row index exchange)" if select else "copy"}
+                      if w.gdn_layers else {}),
                    "l2": "flushed between timed steps (512 MiB write, then 512 MiB read)",
                    "timing": "CUDA-graph replay of the step, CUDA events on the launching stream"},
         "verified_tokens_per_step": tokens_all, "mean_accept_len": float(np.mean(alen_h)),
@@ -349,7 +374,7 @@ def run_native(args, world, rank, local):
     return result
 
 
-def run_e2e(sv, w, a, acc_in, g, out, ws, toks, alen, err, dev, args, flush):
+def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush):
     """Same metric through the public API with the step's inputs in pinned host memory."""
     names = ["q", "k_cache", "v_cache", "block_table", "ctx_lens"]
     host = {n: a[n].cpu().pin_memory() for n in names}
@@ -371,8 +396,7 @@ def run_e2e(sv, w, a, acc_in, g, out, ws, toks, alen, err, dev, args, flush):
                                  devbuf["ctx_lens"], w.k_draft, out, workspace=ws, dev_err=err)
         sv.spec_accept(devbuf["target_logits"], devbuf["draft_tokens"], devbuf["draft_probs"],
                        acc_in["philox_seed"], devbuf["mode"], devbuf["temperature"], toks, alen, dev_err=err)
-        if g is not None:
-            sv.spec_commit_state(g["snapshots"], alen, g["live_state"], dev_err=err)
+        commit()
         out_h.copy_(out, non_blocking=True)
         toks_h.copy_(toks, non_blocking=True)
         alen_h.copy_(alen, non_blocking=True)
@@ -398,7 +422,7 @@ def run_e2e(sv, w, a, acc_in, g, out, ws, toks, alen, err, dev, args, flush):
 # --------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 # --------------------------------------------------------------------------
-def oracle_step_estimate(w, mode, budget_s, seed_offset=0):
+def oracle_step_estimate(w, mode, budget_s, seed_offset=0, commit="copy"):
     """Time the oracle on a bounded sample of one step; return (s per full step, tokens, sample text, threads)."""
     import oracle
     oracle.build()
@@ -426,7 +450,12 @@ def oracle_step_estimate(w, mode, budget_s, seed_offset=0):
                                        acc_in["mode"].numpy(), acc_in["temperature"].numpy())
     t_acc = time.perf_counter() - t1
     t_cmt = 0.0
-    if w.gdn_layers:
+    if w.gdn_layers and commit == "select":
+        live_row, ckpt_rows = (t.numpy() for t in select_tables(w, "cpu"))
+        t2 = time.perf_counter()
+        oracle.commit_select(alen, live_row, ckpt_rows, w.rows, 0)
+        t_cmt = time.perf_counter() - t2
+    elif w.gdn_layers:
         g = wl.make_gdn_inputs(w.replace(gdn_layers=1), device="cpu", seed=w.seed + seed_offset)
         live = g["live_state"].numpy()
         t2 = time.perf_counter()
@@ -435,7 +464,8 @@ def oracle_step_estimate(w, mode, budget_s, seed_offset=0):
     tokens = float(np.sum(alen + 1))
     sample = (f"attention over {done}/{w.batch} sequences ({done_ctx} of {int(ctx.sum())} context tokens, "
               f"scaled by tokens) + acceptance of all {w.batch} rows"
-              + (f" + commit of 1/{w.gdn_layers} layers (scaled)" if w.gdn_layers else ""))
+              + ((" + zero-copy commit of all layers" if commit == "select" else
+                  f" + commit of 1/{w.gdn_layers} layers (scaled)") if w.gdn_layers else ""))
     return t_attn + t_acc + t_cmt, tokens, sample, threads
 
 
@@ -445,7 +475,7 @@ def run_reference(args, world, rank):
     per_step_budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     times, tokens, sample, threads = [], 0.0, "", 1
     for i in range(args.warmup + args.steps):
-        s, tokens, sample, threads = oracle_step_estimate(w, mode, per_step_budget)
+        s, tokens, sample, threads = oracle_step_estimate(w, mode, per_step_budget, commit=args.commit)
         if i >= args.warmup:
             times.append(s)
     ms = statistics.mean(times) * 1e3
@@ -455,7 +485,7 @@ def run_reference(args, world, rank):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "batch_per_gpu": w.batch, "k_draft": w.k_draft, "mode": mode,
-                   "parallelism": "host cores (OpenMP)"},
+                   "parallelism": "host cores (OpenMP)", **({"commit": args.commit} if w.gdn_layers else {})},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -475,7 +505,8 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline:
             w = workload_for(args)
-            s, tokens, sample, threads = oracle_step_estimate(w, args.mode or w.mode, args.cpu_seconds)
+            s, tokens, sample, threads = oracle_step_estimate(w, args.mode or w.mode, args.cpu_seconds,
+                                                              commit=args.commit)
             result["cpu_baseline"] = {"value": tokens / s, "unit": UNIT, "cores": threads, "kind": "oracle",
                                       "sample": sample}
         print(json.dumps(result), flush=True)

@@ -277,6 +277,39 @@ int spec_commit_state_aligned(const float* snapshots, const int32_t* accept_len,
                               int32_t num_slots, int64_t state_elems, int32_t num_tokens,
                               int32_t alignment, int32_t* dev_err, spec_stream_t stream);
 
+/*
+ * Zero-copy commit: stage a different source row instead of copying state
+ * (onnxruntime-genai PR #2457, CommitPrefix note: rolling back a rejected
+ * draft only needs the state pool to stage another row, the checkpoint of the
+ * accepted prefix, instead of the step's final state).
+ *
+ * The states are rows of a pool that the caller owns and that this call never
+ * touches; two int32 tables of pool-row indices, updated in place, say where
+ * each (layer l, row b) keeps its state:
+ *
+ *  live_row  [L, B]    int32: the row holding the live state of (l, b)
+ *  ckpt_rows [L, B, W] int32: the W rows the verify step writes its
+ *                      checkpoints to (slot s in ckpt_rows[l, b, s])
+ *  accept_len [B] int32 (as written by spec_accept)
+ *
+ * With m = accept_len[b] and the slot s picked as in spec_commit_state_aligned
+ * (s = m for SPEC_ALIGN_TOKEN, W - n + m for SPEC_ALIGN_LAST, n = num_tokens),
+ * the call exchanges live_row[l, b] and ckpt_rows[l, b, s]: the chosen
+ * checkpoint becomes the live state where it lies, and the former live row
+ * becomes the window's free slot for the next step. Afterwards
+ * pool[live_row[l, b]] holds exactly what spec_commit_state_aligned would have
+ * copied, and each (l, b) still owns the same W + 1 rows. Cost: 16 bytes of
+ * index traffic per (l, b) instead of two state copies.
+ *
+ * A row with accept_len outside [0, n-1] keeps both tables and sets
+ * SPEC_DEVERR_ACCEPT_LEN. Returns SPEC_ERR_INVALID_ARG for n outside [1, W],
+ * another alignment, negative sizes or a missing table.
+ */
+int spec_commit_select(const int32_t* accept_len, int32_t* live_row, int32_t* ckpt_rows,
+                       int32_t num_layers, int32_t batch, int32_t num_slots,
+                       int32_t num_tokens, int32_t alignment, int32_t* dev_err,
+                       spec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,8 +26,8 @@ from . import buildlib as _build_mod
 __all__ = [
     "SpecError", "build", "library_path", "load_library", "spec_verify_attention",
     "spec_verify_attention_workspace", "new_attention_workspace", "spec_verify_attention_noalloc",
-    "spec_accept", "spec_commit_state", "status_string",
-    "DEVERR", "MODE_GREEDY", "MODE_SAMPLE",
+    "spec_accept", "spec_commit_state", "spec_commit_state_aligned", "spec_commit_select", "status_string",
+    "DEVERR", "MODE_GREEDY", "MODE_SAMPLE", "ALIGN_TOKEN", "ALIGN_LAST",
 ]
 
 MODE_GREEDY = 0
@@ -96,6 +96,8 @@ def load_library():
         lib.spec_commit_state.restype = ctypes.c_int
         lib.spec_commit_state_aligned.argtypes = [P, P, P, i32, i32, i32, i64, i32, i32, P, P]
         lib.spec_commit_state_aligned.restype = ctypes.c_int
+        lib.spec_commit_select.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P]
+        lib.spec_commit_select.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -265,3 +267,21 @@ def spec_commit_state_aligned(snapshots, accept_len, live_state, num_tokens: int
                                        int(num_tokens), int(alignment), _ptr(dev_err), _stream_handle(stream))
     _check("spec_commit_state_aligned", rc)
     return live_state
+
+
+def spec_commit_select(accept_len, live_row, ckpt_rows, num_tokens: int, alignment: int,
+                       dev_err: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Zero-copy commit over a state pool (see spec_verify.h): exchange live_row[l, b] [L, B] with
+    the window slot ckpt_rows[l, b, s] [L, B, W] of the accepted prefix, in place; no state moves."""
+    lib = load_library()
+    _need(accept_len, "accept_len", torch.int32, 1)
+    _need(live_row, "live_row", torch.int32, 2)
+    _need(ckpt_rows, "ckpt_rows", torch.int32, 3)
+    L, B = live_row.shape
+    W = ckpt_rows.shape[2]
+    if ckpt_rows.shape[:2] != (L, B) or accept_len.shape != (B,):
+        raise ValueError("inconsistent commit shapes")
+    rc = lib.spec_commit_select(_ptr(accept_len), _ptr(live_row), _ptr(ckpt_rows), L, B, W, int(num_tokens),
+                                int(alignment), _ptr(dev_err), _stream_handle(stream))
+    _check("spec_commit_select", rc)
+    return live_row, ckpt_rows

@@ -11,6 +11,11 @@
 // piece of one (layer, row) state with 16-byte loads, 8 in flight per thread
 // before the first store, reading accept_len once; the grid is
 // (pieces per state) x (layers * rows), so no division sits in the copy loop.
+//
+// The same PR notes that a rollback only needs the state pool to stage a
+// different source row: spec_commit_select moves no state at all and instead
+// exchanges two int32 pool-row indices per (layer, row), the live row and the
+// window slot of the accepted prefix.
 #include "common.cuh"
 
 namespace specv {
@@ -69,6 +74,44 @@ __global__ void __launch_bounds__(kThreads) commit_scalar_kernel(const float* __
     dst[e] = src[e];
 }
 
+// Zero-copy commit: thread i owns unit i = layer * batch + row and exchanges
+// its live-row index with the window slot of the accepted prefix. Units are
+// disjoint, so the exchanges need no atomics. For windows of up to
+// kWindowRegs slots every entry is loaded together with accept_len, so the
+// exchange waits for one round trip to memory instead of two.
+constexpr int kWindowRegs = 8;
+
+__global__ void __launch_bounds__(kThreads) commit_select_kernel(const int32_t* __restrict__ accept_len,
+                                                                 int32_t* __restrict__ live_row,
+                                                                 int32_t* __restrict__ ckpt_rows, int64_t units,
+                                                                 int batch, int slots, int base, int n_tokens,
+                                                                 int32_t* dev_err) {
+  const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  if (i >= units) return;
+  const int b = (int)(i % batch);
+  const int a = __ldg(accept_len + b);
+  const int32_t live = live_row[i];
+  int32_t* win = ckpt_rows + i * slots;
+  int32_t entry[kWindowRegs];
+#pragma unroll
+  for (int s = 0; s < kWindowRegs; ++s) entry[s] = s < slots ? win[s] : 0;
+  if (a < 0 || a >= n_tokens) {
+    if (i == b) raise_error(dev_err, SPEC_DEVERR_ACCEPT_LEN);  // once per row, from layer 0
+    return;
+  }
+  const int s_keep = base + a;
+  int32_t chosen = 0;
+  if (slots <= kWindowRegs) {
+#pragma unroll
+    for (int s = 0; s < kWindowRegs; ++s)
+      if (s == s_keep) chosen = entry[s];
+  } else {
+    chosen = win[s_keep];
+  }
+  win[s_keep] = live;
+  live_row[i] = chosen;
+}
+
 }  // namespace cmt
 }  // namespace specv
 
@@ -125,6 +168,23 @@ extern "C" int spec_commit_state_aligned(const float* snapshots, const int32_t* 
   const int32_t base = alignment == SPEC_ALIGN_TOKEN ? 0 : num_slots - num_tokens;
   return cmt::launch(snapshots, accept_len, live_state, num_layers, batch, num_slots, state_elems, base, num_tokens,
                      dev_err, reinterpret_cast<cudaStream_t>(stream_));
+}
+
+extern "C" int spec_commit_select(const int32_t* accept_len, int32_t* live_row, int32_t* ckpt_rows,
+                                  int32_t num_layers, int32_t batch, int32_t num_slots, int32_t num_tokens,
+                                  int32_t alignment, int32_t* dev_err, spec_stream_t stream_) {
+  if (num_layers < 0 || batch < 0 || num_slots < 1) return SPEC_ERR_INVALID_ARG;
+  if (num_tokens < 1 || num_tokens > num_slots) return SPEC_ERR_INVALID_ARG;
+  if (alignment != SPEC_ALIGN_TOKEN && alignment != SPEC_ALIGN_LAST) return SPEC_ERR_INVALID_ARG;
+  const int64_t units = (int64_t)num_layers * batch;
+  if (units == 0) return SPEC_OK;
+  if (!accept_len || !live_row || !ckpt_rows) return SPEC_ERR_INVALID_ARG;
+  const int64_t blocks = (units + cmt::kThreads - 1) / cmt::kThreads;
+  if (blocks > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
+  const int32_t base = alignment == SPEC_ALIGN_TOKEN ? 0 : num_slots - num_tokens;
+  cmt::commit_select_kernel<<<(unsigned)blocks, cmt::kThreads, 0, reinterpret_cast<cudaStream_t>(stream_)>>>(
+      accept_len, live_row, ckpt_rows, units, batch, num_slots, base, num_tokens, dev_err);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
 extern "C" const char* spec_status_string(int status) {

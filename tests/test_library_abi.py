@@ -99,3 +99,13 @@ def test_accept_and_commit_host_validation(lib):
     assert al(a=2) == -1      # unknown alignment
     assert al(snaps=None) == -1
     assert al(L=0) == 0
+    sel = lambda n=3, a=1, W=4, L=2, B=2, live=fake: lib.spec_commit_select(fake, live, fake, L, B, W, n, a, None,
+                                                                              None)
+    assert sel(n=5) == -1     # step longer than the window
+    assert sel(n=0) == -1
+    assert sel(W=0) == -1
+    assert sel(a=2) == -1     # unknown alignment
+    assert sel(L=-1) == -1
+    assert sel(live=None) == -1
+    assert sel(L=0) == 0      # nothing to do: no launch
+    assert sel(B=0, live=None) == 0
