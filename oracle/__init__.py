@@ -18,7 +18,10 @@ back to p when max(0, p-q) is all zero; without draft probabilities q is one-hot
 at the drafted token; the correction/bonus draw is an
 exponential race keyed by Philox words as documented in spec_verify.h; the
 zero-copy commit exchanges the live row with the chosen checkpoint row of a
-state pool.
+state pool; the gated delta rule (from the published Gated DeltaNet method,
+which the pages name but do not state) takes log-decay gates g and write
+strengths beta as inputs, keeps a V-major dv x dk state and scales q by the
+given factor.
 """
 
 from __future__ import annotations
@@ -96,6 +99,9 @@ def _load():
         lib.oracle_commit_state_aligned.restype = i32
         lib.oracle_commit_select.argtypes = [P, P, P, i32, i32, i32, i32, i32]
         lib.oracle_commit_select.restype = i32
+        lib.oracle_gdn_verify.argtypes = [P, P, P, P, P, ctypes.c_double, P, P, P, i32, i32, i32, i32, i32, i32,
+                                          i32, i32]
+        lib.oracle_gdn_verify.restype = i32
         _lib = lib
         return lib
 
@@ -244,3 +250,29 @@ def commit_select(accept_len, live_row, ckpt_rows, n_tokens: int, alignment: int
     if check and rc != 0:
         raise OracleError(rc)
     return rc
+
+
+def gdn_verify(q, k, v, g, beta, state_in, *, scale: float, num_slots: int = 0, alignment: int = 0,
+               n_threads: int = 0, check: bool = True):
+    """Gated delta rule over a verify chain (double precision).
+
+    q, k [B,R,H,dk]; v [B,R,H,dv]; g (log decay), beta [B,R,H]; state_in [B,H,dv,dk]
+    (V-major). Token t: S = exp(g) S + beta (v - exp(g) S k) k^T, o = S (scale q).
+    Returns (snapshots [B,W,H,dv,dk] with slot base+t = state after token t, out
+    [B,R,H,dv], status); W = num_slots (default R), base 0 (alignment 0) or W - R.
+    Slots outside the written range are zero.
+    """
+    lib = _load()
+    q, k, v, g, beta, s0 = (_c(x, np.float32) for x in (q, k, v, g, beta, state_in))
+    B, R, H, dk = q.shape
+    dv = v.shape[3]
+    assert k.shape == q.shape and v.shape == (B, R, H, dv) and g.shape == (B, R, H) and beta.shape == (B, R, H)
+    assert s0.shape == (B, H, dv, dk)
+    W = int(num_slots) if num_slots else R
+    snaps = np.zeros((B, W, H, dv, dk), np.float32)
+    out = np.zeros((B, R, H, dv), np.float32)
+    rc = lib.oracle_gdn_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(s0), _ptr(snaps),
+                               _ptr(out), B, R, H, dk, dv, W, int(alignment), n_threads)
+    if check and rc != 0:
+        raise OracleError(rc)
+    return snaps, out, rc

@@ -31,6 +31,10 @@
  *    token and the commit picks the slot of the accepted prefix
  *    (onnxruntime-genai PR #2457, per-token state checkpoint and CommitPrefix
  *    notes; lmdeploy PR #5019, fix 2, CommitAcceptedRecurrentStateKernel).
+ *  - gated delta rule over the verify chain (the checkpoints' producer): the
+ *    pages name the GatedDeltaNet operator, its V-major float32 state and its
+ *    checkpoint window but not the update, which follows Yang, Kautz,
+ *    Hatamizadeh, "Gated Delta Networks: Improving Mamba2 with Delta Rule".
  */
 #include <math.h>
 #include <stdint.h>
@@ -544,4 +548,87 @@ int oracle_commit_state(const float* snapshots, const int32_t* accept_len, float
     memcpy(dst, src, sizeof(float) * (size_t)E);
   }
   return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Gated delta rule over the verify chain                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * The hybrid models interleave attention with GatedDeltaNet layers whose
+ * operators publish the recurrent state after every token of the step
+ * (onnxruntime-genai PR #2457: GatedDeltaNet.checkpoints; V-major float32
+ * state; a window of W slots written either at slot j after token j or with
+ * slot W-1 after the last token; lmdeploy PR #5019: GDR verify kernels). The
+ * pages do not state the recurrence; it is taken from the published method
+ * (Yang, Kautz, Hatamizadeh, "Gated Delta Networks: Improving Mamba2 with
+ * Delta Rule", ICLR 2025). Per (row b, head h) the state S is dv x dk, V-major
+ * (S[i][c], value index i, key index c), and token t updates it by
+ *
+ *   alpha_t = exp(g_t)                          (g_t <= 0: log decay)
+ *   S_t     = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T
+ *   o_t     = S_t (scale q_t)
+ *
+ * which is S_{t-1} alpha_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T written
+ * out. S_0 is the live state; slot base + t of the window receives S_{t+1}
+ * (the state after input t), base = 0 (token alignment) or W - R (last).
+ * Everything is computed in double; the snapshots and outputs are rounded to
+ * float when stored, the running state stays in double.
+ *
+ * Layouts: q, k [B,R,H,dk]; v [B,R,H,dv]; g, beta [B,R,H]; state_in
+ * [B,H,dv,dk]; snapshots [B,W,H,dv,dk]; out [B,R,H,dv]. All float.
+ */
+int oracle_gdn_verify(const float* q, const float* k, const float* v, const float* g, const float* beta,
+                      double scale, const float* state_in, float* snapshots, float* out, int B, int R, int H,
+                      int dk, int dv, int W, int alignment, int n_threads) {
+  if (!q || !k || !v || !g || !beta || !state_in || !snapshots || !out) return ORACLE_ERR_ARG;
+  if (B < 0 || R < 1 || H < 1 || dk < 1 || dv < 1 || W < R || (alignment != 0 && alignment != 1))
+    return ORACLE_ERR_ARG;
+  const int base = alignment == 0 ? 0 : W - R;
+  const int64_t E = (int64_t)dv * dk;
+  int err = ORACLE_OK;
+  set_threads(n_threads);
+#pragma omp parallel
+  {
+    double* S = (double*)malloc(sizeof(double) * (size_t)E);
+    double* Sk = (double*)malloc(sizeof(double) * (size_t)dv);
+    if (!S || !Sk) {
+#pragma omp critical
+      err = ORACLE_ERR_NOMEM;
+    }
+#pragma omp for schedule(dynamic)
+    for (int64_t unit = 0; unit < (int64_t)B * H; ++unit) {
+      if (!S || !Sk) continue;
+      const int64_t b = unit / H, h = unit % H;
+      const float* s0 = state_in + unit * E;
+      for (int64_t e = 0; e < E; ++e) S[e] = s0[e];
+      for (int t = 0; t < R; ++t) {
+        const int64_t tok = (b * R + t) * H + h;
+        const float* kt = k + tok * dk;
+        const float* qt = q + tok * dk;
+        const float* vt = v + tok * dv;
+        const double alpha = exp((double)g[tok]);
+        const double bt = beta[tok];
+        for (int i = 0; i < dv; ++i) {  /* S_{t-1} k_t */
+          double acc = 0.0;
+          for (int c = 0; c < dk; ++c) acc += S[(int64_t)i * dk + c] * (double)kt[c];
+          Sk[i] = acc;
+        }
+        for (int i = 0; i < dv; ++i) {
+          const double u = (double)vt[i] - alpha * Sk[i];
+          for (int c = 0; c < dk; ++c) S[(int64_t)i * dk + c] = alpha * S[(int64_t)i * dk + c] + bt * u * (double)kt[c];
+        }
+        float* o = out + tok * dv;
+        for (int i = 0; i < dv; ++i) {  /* o_t = S_t (scale q_t) */
+          double acc = 0.0;
+          for (int c = 0; c < dk; ++c) acc += S[(int64_t)i * dk + c] * (scale * (double)qt[c]);
+          o[i] = (float)acc;
+        }
+        float* snap = snapshots + ((b * W + base + t) * H + h) * E;
+        for (int64_t e = 0; e < E; ++e) snap[e] = (float)S[e];
+      }
+    }
+    free(S);
+    free(Sk);
+  }
+  return err;
 }

@@ -615,3 +615,94 @@ def test_commit_skips_invalid_rows(oracle_mod):
     assert rc == -7
     assert np.array_equal(live[:, 0], snaps[:, 0, 1])
     assert np.all(live[:, 1:] == 7.0)
+
+
+# ---------------------------------------------------------------------------
+# gated delta rule over the verify chain
+# ---------------------------------------------------------------------------
+def _gdn_inputs(rng, B, R, H, dk, dv, unit_keys=True):
+    q = rng.standard_normal((B, R, H, dk)).astype(np.float32)
+    k = rng.standard_normal((B, R, H, dk))
+    if unit_keys:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, R, H, dv)).astype(np.float32)
+    g = -rng.uniform(0.0, 1.0, (B, R, H)).astype(np.float32)
+    beta = rng.uniform(0.05, 1.0, (B, R, H)).astype(np.float32)
+    s0 = rng.standard_normal((B, H, dv, dk)).astype(np.float32)
+    return q, k.astype(np.float32), v, g, beta, s0
+
+
+def test_gdn_pure_decay_closed_form(oracle_mod):
+    """beta = 0: the state only decays, S_t = exp(g_0 + ... + g_t) S_0, and o_t = S_t (scale q_t)."""
+    rng = np.random.default_rng(70)
+    B, R, H, dk, dv = 2, 4, 3, 8, 5
+    q, k, v, g, beta, s0 = _gdn_inputs(rng, B, R, H, dk, dv)
+    beta[:] = 0
+    snaps, out, _ = oracle_mod.gdn_verify(q, k, v, g, beta, s0, scale=0.25)
+    decay = np.exp(np.cumsum(g.astype(np.float64), axis=1))  # [B,R,H]
+    expect = decay[:, :, :, None, None] * s0.astype(np.float64)[:, None]
+    np.testing.assert_allclose(snaps, expect, rtol=1e-6, atol=1e-7)
+    o = np.einsum("brhij,brhj->brhi", expect, 0.25 * q.astype(np.float64))
+    np.testing.assert_allclose(out, o, rtol=1e-5, atol=1e-6)
+
+
+def test_gdn_delta_rule_on_the_key_direction(oracle_mod):
+    """With unit keys the update moves S k_t to (1 - beta) alpha S_{t-1} k_t + beta v_t
+    and only decays every direction orthogonal to k_t (the rule's rank-one form)."""
+    rng = np.random.default_rng(71)
+    B, R, H, dk, dv = 3, 5, 2, 16, 12
+    q, k, v, g, beta, s0 = _gdn_inputs(rng, B, R, H, dk, dv)
+    snaps, _, _ = oracle_mod.gdn_verify(q, k, v, g, beta, s0, scale=1.0)
+    for b in range(B):
+        for h in range(H):
+            prev = s0[b, h].astype(np.float64)
+            for t in range(R):
+                kt = k[b, t, h].astype(np.float64)
+                a, bt = np.exp(float(g[b, t, h])), float(beta[b, t, h])
+                cur = snaps[b, t, h].astype(np.float64)
+                np.testing.assert_allclose(cur @ kt, (1 - bt) * a * (prev @ kt) + bt * v[b, t, h], rtol=1e-5,
+                                           atol=1e-5)
+                w = rng.standard_normal(dk)
+                w -= (w @ kt) * kt  # orthogonal to k_t
+                np.testing.assert_allclose(cur @ w, a * (prev @ w), rtol=1e-5, atol=1e-5)
+                prev = cur
+
+
+def test_gdn_orthonormal_keys_store_outer_products(oracle_mod):
+    """From S_0 = 0 with alpha = beta = 1 and orthonormal keys the state is the sum of
+    v_t k_t^T, so querying with k_j / scale returns v_j for every j <= t."""
+    rng = np.random.default_rng(72)
+    B, R, H, dk, dv = 1, 4, 2, 8, 6
+    _, _, v, g, beta, s0 = _gdn_inputs(rng, B, R, H, dk, dv)
+    basis = np.linalg.qr(rng.standard_normal((H, dk, dk)))[0]  # orthonormal columns per head
+    k = np.transpose(basis[:, :, :R], (2, 0, 1))[None].astype(np.float32)  # [1,R,H,dk]
+    g[:], beta[:], s0[:] = 0, 1, 0
+    scale = 0.5
+    q = (k[:, :1].repeat(R, axis=1) / scale).astype(np.float32)  # every token queries k_0
+    snaps, out, _ = oracle_mod.gdn_verify(q, k, v, g, beta, s0, scale=scale)
+    full = sum(np.einsum("hi,hc->hic", v[0, t].astype(np.float64), k[0, t].astype(np.float64)) for t in range(R))
+    np.testing.assert_allclose(snaps[0, R - 1], full, atol=1e-6)
+    np.testing.assert_allclose(out[0], np.broadcast_to(v[0, 0], (R, H, dv)), atol=1e-5)
+
+
+def test_gdn_chain_splits_and_windows(oracle_mod):
+    """One call over R tokens equals R one-token calls carrying the state; a window
+    wider than the chain holds the same states at slots t (token alignment) or
+    W - R + t (last alignment) and leaves its other slots untouched."""
+    rng = np.random.default_rng(73)
+    B, R, H, dk, dv = 2, 4, 2, 8, 8
+    q, k, v, g, beta, s0 = _gdn_inputs(rng, B, R, H, dk, dv, unit_keys=False)
+    snaps, out, _ = oracle_mod.gdn_verify(q, k, v, g, beta, s0, scale=0.3)
+    state = s0
+    for t in range(R):
+        sl = slice(t, t + 1)
+        s1, o1, _ = oracle_mod.gdn_verify(q[:, sl], k[:, sl], v[:, sl], g[:, sl], beta[:, sl], state, scale=0.3)
+        np.testing.assert_allclose(s1[:, 0], snaps[:, t], rtol=1e-5, atol=1e-5)
+        np.testing.assert_allclose(o1[:, 0], out[:, t], rtol=1e-5, atol=1e-5)
+        state = s1[:, 0]
+    W = R + 3
+    for alignment, base in ((0, 0), (1, W - R)):
+        sw, ow, _ = oracle_mod.gdn_verify(q, k, v, g, beta, s0, scale=0.3, num_slots=W, alignment=alignment)
+        assert np.array_equal(sw[:, base:base + R], snaps) and np.array_equal(ow, out)
+        rest = np.delete(sw, np.arange(base, base + R), axis=1)
+        assert not rest.any()
