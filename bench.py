@@ -53,6 +53,9 @@ def parse():
     ap.add_argument("--commit", default="copy", choices=["copy", "select"],
                     help="recurrent-state commit: copy the kept checkpoint into the live state, or select it "
                          "in place by exchanging state-pool row indices (zero-copy)")
+    ap.add_argument("--gdn-verify", action="store_true",
+                    help="add one gated-delta-net layer's recurrence over the verify chain to the step "
+                         "(workloads with recurrent state; pooled when --commit select)")
     ap.add_argument("--gdn-layers", type=int, default=None,
                     help="override the workload's recurrent-state layer count (small profiler captures); "
                          "the line's config reports the count used")
@@ -128,6 +131,14 @@ def commit_bytes(w, commit="copy"):
     if commit == "select":  # per (layer, row): accept_len, live_row and one window index read, two written
         return w.gdn_layers * w.batch * 5 * 4
     return 2 * w.gdn_layers * w.batch * w.state_elems * 4
+
+
+def gdn_verify_bytes(w):
+    """One layer: read each (row, head) state once, write R checkpoints; q, k, v, out; g, beta."""
+    states = w.batch * w.gdn_heads
+    state_bytes = w.gdn_dv * w.gdn_dk * 4
+    return (states * state_bytes * (1 + w.rows) + w.batch * w.rows * w.gdn_heads * (2 * w.gdn_dk + 2 * w.gdn_dv) * 4
+            + w.batch * w.rows * w.gdn_heads * 8)
 
 
 def select_tables(w, dev):
@@ -235,6 +246,14 @@ def run_native(args, world, rank, local):
     select = bool(w.gdn_layers) and args.commit == "select"
     g = wl.make_gdn_inputs(w, device=dev, seed=w.seed + 1000 * rank) if w.gdn_layers and not select else None
     tables = select_tables(w, dev) if select else None
+    gv = None
+    if args.gdn_verify and w.gdn_layers:
+        gv = wl.make_gdn_verify_inputs(w, device=dev, seed=w.seed + 1000 * rank, layers=1)
+        gv = {n: (t[0] if torch.is_tensor(t) else t) for n, t in gv.items()}
+        gv["out"] = torch.empty((w.batch, w.rows, w.gdn_heads, w.gdn_dv), device=dev)
+        if select:  # layer 0's rows of the pool: unit b owns rows b*(W+1) .. b*(W+1)+W
+            gv["pool"] = torch.zeros((w.batch * (w.rows + 1), w.state_elems), device=dev)
+            gv["pool"][tables[0][0].long()] = gv["state"].view(w.batch, -1)
     B, R = w.batch, w.rows
     out = torch.empty((B, R, w.num_q_heads, w.head_dim), dtype=torch.float32, device=dev)
     ws = sv.new_attention_workspace(
@@ -260,12 +279,24 @@ def run_native(args, world, rank, local):
         elif g is not None:
             sv.spec_commit_state(g["snapshots"], alen, g["live_state"], dev_err=err)
 
+    def gdn_verify():
+        qkv = [gv[n] for n in ("q", "k", "v", "g", "beta")]
+        if tables is not None:
+            sv.spec_gdn_verify_pooled(*qkv, gv["pool"], tables[0][0], tables[1][0], gv["out"], gv["scale"],
+                                      dev_err=err)
+        else:
+            sv.spec_gdn_verify(*qkv, g["live_state"][0].view(w.batch, w.gdn_heads, w.gdn_dv, w.gdn_dk),
+                               g["snapshots"][0].view(w.batch, w.rows, w.gdn_heads, w.gdn_dv, w.gdn_dk),
+                               gv["out"], gv["scale"], dev_err=err)
+
     def step():
         attention()
+        if gv is not None:
+            gdn_verify()
         accept()
         commit()
 
-    launches_per_step = 1 + 1 + (1 if w.gdn_layers else 0)
+    launches_per_step = 1 + 1 + (1 if w.gdn_layers else 0) + (1 if gv is not None else 0)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -278,8 +309,11 @@ def run_native(args, world, rank, local):
     side = torch.cuda.Stream()
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        for name, fn in (("step", step), ("attention", attention), ("accept", accept), ("commit", commit)):
+        for name, fn in (("step", step), ("attention", attention), ("accept", accept), ("commit", commit),
+                         ("gdn_verify", gdn_verify)):
             if name == "commit" and not w.gdn_layers:
+                continue
+            if name == "gdn_verify" and gv is None:
                 continue
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph, stream=side):
@@ -321,6 +355,7 @@ def run_native(args, world, rank, local):
     t_attn = timed(graphs["attention"], args.steps)
     t_acc = timed(graphs["accept"], args.steps)
     t_cmt = timed(graphs["commit"], args.steps) if "commit" in graphs else [0.0]
+    t_gdn = timed(graphs["gdn_verify"], args.steps) if "gdn_verify" in graphs else None
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
 
@@ -345,6 +380,10 @@ def run_native(args, world, rank, local):
     if w.gdn_layers:
         kernels["commit"] = {"ms": tm, "bytes": mb, "GBps": mb / tm / 1e6, "frac": mb / tm / 1e6 / peak,
                              "kind": "select" if select else "copy"}
+    if t_gdn is not None:
+        tg, gb = statistics.mean(t_gdn), gdn_verify_bytes(w)
+        kernels["gdn_verify"] = {"ms": tg, "bytes": gb, "GBps": gb / tg / 1e6, "frac": gb / tg / 1e6 / peak,
+                                 "layers": 1}
     dominant = max(kernels, key=lambda k: kernels[k]["ms"])
     dk = kernels[dominant]
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["GBps"], "peak": peak, "unit": "GB/s",
@@ -353,7 +392,7 @@ def run_native(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush)
+        e2e = run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush, gv, gdn_verify)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -365,6 +404,8 @@ def run_native(args, world, rank, local):
                    "vocab": w.vocab, "gdn_layers": w.gdn_layers, "parallelism": f"replicas x{world}",
                    **({"commit": "select (zero-copy: pool-row index exchange)" if select else "copy"}
                       if w.gdn_layers else {}),
+                   **({"gdn_verify": f"one layer: {w.gdn_heads} heads, {w.gdn_dv}x{w.gdn_dk} fp32 state, "
+                                     f"{w.rows} tokens"} if gv is not None else {}),
                    "l2": "flushed between timed steps (512 MiB write, then 512 MiB read)",
                    "timing": "CUDA-graph replay of the step, CUDA events on the launching stream"},
         "verified_tokens_per_step": tokens_all, "mean_accept_len": float(np.mean(alen_h)),
@@ -374,17 +415,21 @@ def run_native(args, world, rank, local):
     return result
 
 
-def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush):
-    """Same metric through the public API with the step's inputs in pinned host memory."""
+def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush, gv=None, gdn_verify=None):
+    """Same metric through the public API with the step's inputs in pinned host memory (the recurrent
+    state, like the model weights, stays resident; the step's activations are copied in)."""
     names = ["q", "k_cache", "v_cache", "block_table", "ctx_lens"]
     host = {n: a[n].cpu().pin_memory() for n in names}
     for n in ["target_logits", "draft_tokens", "draft_probs", "mode", "temperature"]:
         host[n] = acc_in[n].cpu().pin_memory()
+    gdn_host = {}
+    if gv is not None:
+        gdn_host = {n: gv[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
     devbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     toks_h = torch.empty(toks.shape, dtype=toks.dtype).pin_memory()
     alen_h = torch.empty(alen.shape, dtype=alen.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(gdn_host.values()))
     d2h = out_h.numel() * 4 + toks_h.numel() * 4 + alen_h.numel() * 4
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -394,6 +439,10 @@ def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush
             devbuf[n].copy_(t, non_blocking=True)
         sv.spec_verify_attention(devbuf["q"], devbuf["k_cache"], devbuf["v_cache"], devbuf["block_table"],
                                  devbuf["ctx_lens"], w.k_draft, out, workspace=ws, dev_err=err)
+        if gv is not None:
+            for n, t in gdn_host.items():  # the step's activations into the buffers the recurrence reads
+                gv[n].copy_(t, non_blocking=True)
+            gdn_verify()
         sv.spec_accept(devbuf["target_logits"], devbuf["draft_tokens"], devbuf["draft_probs"],
                        acc_in["philox_seed"], devbuf["mode"], devbuf["temperature"], toks, alen, dev_err=err)
         commit()
@@ -422,7 +471,7 @@ def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush
 # --------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 # --------------------------------------------------------------------------
-def oracle_step_estimate(w, mode, budget_s, seed_offset=0, commit="copy"):
+def oracle_step_estimate(w, mode, budget_s, seed_offset=0, commit="copy", gdn_verify=False):
     """Time the oracle on a bounded sample of one step; return (s per full step, tokens, sample text, threads)."""
     import oracle
     oracle.build()
@@ -461,12 +510,21 @@ def oracle_step_estimate(w, mode, budget_s, seed_offset=0, commit="copy"):
         t2 = time.perf_counter()
         oracle.commit_state(g["snapshots"].numpy(), alen, live)
         t_cmt = (time.perf_counter() - t2) * w.gdn_layers
+    t_gdn, gdn_rows = 0.0, 0
+    if gdn_verify and w.gdn_layers:  # one layer; a few rows (all heads), scaled to the batch
+        gdn_rows = min(4, w.batch)
+        x = wl.make_gdn_verify_inputs(w.replace(batch=gdn_rows), device="cpu", seed=w.seed + seed_offset)
+        arrays = [x[n][0].numpy() for n in ("q", "k", "v", "g", "beta")]
+        t3 = time.perf_counter()
+        oracle.gdn_verify(*arrays, x["state"][0].numpy(), scale=x["scale"])
+        t_gdn = (time.perf_counter() - t3) * w.batch / gdn_rows
     tokens = float(np.sum(alen + 1))
     sample = (f"attention over {done}/{w.batch} sequences ({done_ctx} of {int(ctx.sum())} context tokens, "
               f"scaled by tokens) + acceptance of all {w.batch} rows"
               + ((" + zero-copy commit of all layers" if commit == "select" else
-                  f" + commit of 1/{w.gdn_layers} layers (scaled)") if w.gdn_layers else ""))
-    return t_attn + t_acc + t_cmt, tokens, sample, threads
+                  f" + commit of 1/{w.gdn_layers} layers (scaled)") if w.gdn_layers else "")
+              + (f" + one gated-delta-net layer over {gdn_rows}/{w.batch} rows (scaled)" if gdn_rows else ""))
+    return t_attn + t_acc + t_cmt + t_gdn, tokens, sample, threads
 
 
 def run_reference(args, world, rank):
@@ -475,7 +533,8 @@ def run_reference(args, world, rank):
     per_step_budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
     times, tokens, sample, threads = [], 0.0, "", 1
     for i in range(args.warmup + args.steps):
-        s, tokens, sample, threads = oracle_step_estimate(w, mode, per_step_budget, commit=args.commit)
+        s, tokens, sample, threads = oracle_step_estimate(w, mode, per_step_budget, commit=args.commit,
+                                                          gdn_verify=args.gdn_verify)
         if i >= args.warmup:
             times.append(s)
     ms = statistics.mean(times) * 1e3
@@ -506,7 +565,7 @@ def main():
         if not args.no_cpu_baseline:
             w = workload_for(args)
             s, tokens, sample, threads = oracle_step_estimate(w, args.mode or w.mode, args.cpu_seconds,
-                                                              commit=args.commit)
+                                                              commit=args.commit, gdn_verify=args.gdn_verify)
             result["cpu_baseline"] = {"value": tokens / s, "unit": UNIT, "cores": threads, "kind": "oracle",
                                       "sample": sample}
         print(json.dumps(result), flush=True)

@@ -68,6 +68,7 @@ typedef struct CUstream_st* spec_stream_t;
 #define SPEC_DEVERR_TEMPERATURE 16 /* sampling row with temperature not > 0      */
 #define SPEC_DEVERR_TIMEOUT 32     /* an asynchronous copy did not arrive        */
 #define SPEC_DEVERR_MODE 64        /* mode not 0/1                               */
+#define SPEC_DEVERR_POOL_ROW 128   /* state-pool row index outside the pool      */
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* spec_status_string(int status);
@@ -309,6 +310,63 @@ int spec_commit_select(const int32_t* accept_len, int32_t* live_row, int32_t* ck
                        int32_t num_layers, int32_t batch, int32_t num_slots,
                        int32_t num_tokens, int32_t alignment, int32_t* dev_err,
                        spec_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* 4. Gated delta rule over the verify chain (checkpoint producer)            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The GatedDeltaNet layers of a hybrid model publish their recurrent state
+ * after every token of the speculative step (onnxruntime-genai PR #2457:
+ * GatedDeltaNet.checkpoints, V-major float32 state, checkpoint windows;
+ * lmdeploy PR #5019: GDR verify kernels); these calls compute that series for
+ * one layer. The pages name the operator but not its update, which follows the
+ * published Gated DeltaNet rule (Yang, Kautz, Hatamizadeh, "Gated Delta
+ * Networks"). Per row b, head h and token t (R = num_tokens tokens, k+1 for a
+ * verify step), with the state S V-major (S[i][c]: value i, key c):
+ *
+ *   a_t = exp(g_t)
+ *   S_t = a_t S_{t-1} + beta_t (v_t - a_t S_{t-1} k_t) k_t^T
+ *   o_t = S_t (scale q_t)
+ *
+ * S_0 is the live state; checkpoint slot base + t of a W-slot window
+ * (W = num_slots >= R) receives S_{t+1}, the state after input t, with
+ * base = 0 for SPEC_ALIGN_TOKEN and W - R for SPEC_ALIGN_LAST; other slots are
+ * not written. The gates arrive computed (g is the log decay, typically <= 0);
+ * q and k are used as given (any normalisation happens upstream).
+ *
+ *  q, k   [B, R, H, dk] fp32      v    [B, R, H, dv] fp32
+ *  g, beta [B, R, H] fp32         out  [B, R, H, dv] fp32 (o_t)
+ *  state_in  [B, H, dv, dk] fp32  (one row of E = H*dv*dk floats per b)
+ *  snapshots [B, W, H, dv, dk] fp32
+ *
+ * Arithmetic is fp32 (the state stays fp32 between tokens). dk = dv = 128
+ * runs the register-resident kernel (16-byte aligned states); other sizes run
+ * a shared-memory kernel while dv*dk + R*(2dk+dv) + 3dv floats fit in 200 KB.
+ * Returns SPEC_ERR_INVALID_ARG for R outside [1, 32], W < R, an unknown
+ * alignment, non-positive sizes or missing pointers; SPEC_ERR_UNSUPPORTED for
+ * a state too large for either kernel.
+ */
+int spec_gdn_verify(const float* q, const float* k, const float* v, const float* g,
+                    const float* beta, float scale, const float* state_in, float* snapshots,
+                    float* out, int32_t batch, int32_t num_tokens, int32_t num_heads,
+                    int32_t dk, int32_t dv, int32_t num_slots, int32_t alignment,
+                    int32_t* dev_err, spec_stream_t stream);
+
+/*
+ * The same step over a state pool, the companion of spec_commit_select: row b
+ * reads its live state from pool row live_row[b] and writes checkpoint slot s
+ * to pool row ckpt_rows[b, s]; a pool row holds E = H*dv*dk floats (all heads
+ * of one (layer, row)). Pass the tables of one layer (live_row + l*B,
+ * ckpt_rows + l*B*W). A row naming an index outside [0, pool_rows) writes
+ * zeros to its out rows, touches no state and sets SPEC_DEVERR_POOL_ROW.
+ */
+int spec_gdn_verify_pooled(const float* q, const float* k, const float* v, const float* g,
+                           const float* beta, float scale, float* pool, int64_t pool_rows,
+                           const int32_t* live_row, const int32_t* ckpt_rows, float* out,
+                           int32_t batch, int32_t num_tokens, int32_t num_heads, int32_t dk,
+                           int32_t dv, int32_t num_slots, int32_t alignment, int32_t* dev_err,
+                           spec_stream_t stream);
 
 #ifdef __cplusplus
 }

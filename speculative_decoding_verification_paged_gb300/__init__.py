@@ -26,7 +26,8 @@ from . import buildlib as _build_mod
 __all__ = [
     "SpecError", "build", "library_path", "load_library", "spec_verify_attention",
     "spec_verify_attention_workspace", "new_attention_workspace", "spec_verify_attention_noalloc",
-    "spec_accept", "spec_commit_state", "spec_commit_state_aligned", "spec_commit_select", "status_string",
+    "spec_accept", "spec_commit_state", "spec_commit_state_aligned", "spec_commit_select", "spec_gdn_verify",
+    "spec_gdn_verify_pooled", "status_string",
     "DEVERR", "MODE_GREEDY", "MODE_SAMPLE", "ALIGN_TOKEN", "ALIGN_LAST",
 ]
 
@@ -34,7 +35,7 @@ MODE_GREEDY = 0
 MODE_SAMPLE = 1
 DEVERR = {
     "block_id": 1, "token": 2, "accept_len": 4, "ctx_len": 8, "temperature": 16,
-    "timeout": 32, "mode": 64,
+    "timeout": 32, "mode": 64, "pool_row": 128,
 }
 
 _lock = threading.Lock()
@@ -98,6 +99,12 @@ def load_library():
         lib.spec_commit_state_aligned.restype = ctypes.c_int
         lib.spec_commit_select.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P]
         lib.spec_commit_select.restype = ctypes.c_int
+        lib.spec_gdn_verify.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                         P, P]
+        lib.spec_gdn_verify.restype = ctypes.c_int
+        lib.spec_gdn_verify_pooled.argtypes = [P, P, P, P, P, ctypes.c_float, P, i64, P, P, P, i32, i32, i32, i32,
+                                                i32, i32, i32, P, P]
+        lib.spec_gdn_verify_pooled.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -285,3 +292,56 @@ def spec_commit_select(accept_len, live_row, ckpt_rows, num_tokens: int, alignme
                                 int(alignment), _ptr(dev_err), _stream_handle(stream))
     _check("spec_commit_select", rc)
     return live_row, ckpt_rows
+
+
+def _gdn_shapes(q, k, v, g, beta, out):
+    _need(q, "q", torch.float32, 4)
+    _need(k, "k", torch.float32, 4)
+    _need(v, "v", torch.float32, 4)
+    _need(g, "g", torch.float32, 3)
+    _need(beta, "beta", torch.float32, 3)
+    _need(out, "out", torch.float32, 4)
+    B, R, H, dk = q.shape
+    dv = v.shape[3]
+    if k.shape != q.shape or v.shape != (B, R, H, dv) or g.shape != (B, R, H) or beta.shape != (B, R, H) \
+            or out.shape != (B, R, H, dv):
+        raise ValueError("inconsistent gated-delta-rule shapes")
+    return B, R, H, dk, dv
+
+
+def spec_gdn_verify(q, k, v, g, beta, state_in, snapshots, out, scale: float, alignment: int = ALIGN_TOKEN,
+                    dev_err: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Gated delta rule over the verify chain for one layer (see spec_verify.h): state_in [B,H,dv,dk],
+    snapshots [B,W,H,dv,dk] (slot base+t = state after token t), out [B,R,H,dv]."""
+    lib = load_library()
+    B, R, H, dk, dv = _gdn_shapes(q, k, v, g, beta, out)
+    _need(state_in, "state_in", torch.float32, 4)
+    _need(snapshots, "snapshots", torch.float32, 5)
+    W = snapshots.shape[1]
+    if state_in.shape != (B, H, dv, dk) or snapshots.shape != (B, W, H, dv, dk):
+        raise ValueError("inconsistent state shapes")
+    rc = lib.spec_gdn_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state_in),
+                             _ptr(snapshots), _ptr(out), B, R, H, dk, dv, W, int(alignment), _ptr(dev_err),
+                             _stream_handle(stream))
+    _check("spec_gdn_verify", rc)
+    return snapshots, out
+
+
+def spec_gdn_verify_pooled(q, k, v, g, beta, pool, live_row, ckpt_rows, out, scale: float,
+                           alignment: int = ALIGN_TOKEN, dev_err: Optional[torch.Tensor] = None,
+                           stream: Optional[torch.cuda.Stream] = None):
+    """The same step over a state pool [P, H*dv*dk]: reads pool[live_row[b]], writes checkpoint slot s to
+    pool[ckpt_rows[b, s]] (the tables of one layer: live_row [B], ckpt_rows [B, W])."""
+    lib = load_library()
+    B, R, H, dk, dv = _gdn_shapes(q, k, v, g, beta, out)
+    _need(pool, "pool", torch.float32, 2)
+    _need(live_row, "live_row", torch.int32, 1)
+    _need(ckpt_rows, "ckpt_rows", torch.int32, 2)
+    W = ckpt_rows.shape[1]
+    if pool.shape[1] != H * dv * dk or live_row.shape != (B,) or ckpt_rows.shape != (B, W):
+        raise ValueError("inconsistent pool shapes")
+    rc = lib.spec_gdn_verify_pooled(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(pool),
+                                    pool.shape[0], _ptr(live_row), _ptr(ckpt_rows), _ptr(out), B, R, H, dk, dv, W,
+                                    int(alignment), _ptr(dev_err), _stream_handle(stream))
+    _check("spec_gdn_verify_pooled", rc)
+    return out

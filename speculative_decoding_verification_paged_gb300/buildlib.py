@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libspecverify.so")
-SOURCES = ["attention.cu", "accept.cu", "commit.cu"]
+SOURCES = ["attention.cu", "accept.cu", "commit.cu", "gdn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

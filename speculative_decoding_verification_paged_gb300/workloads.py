@@ -195,6 +195,31 @@ def make_gdn_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
     return {"snapshots": snaps, "live_state": live}
 
 
+def make_gdn_verify_inputs(w: Workload, device="cpu", seed: Optional[int] = None, layers: int = 1,
+                           generator: Optional[torch.Generator] = None) -> dict:
+    """Inputs of the gated delta rule over the verify chain, for `layers` layers.
+
+    q, k [layers, B, R, H, dk] are L2-normalised per head (the GatedDeltaNet layer
+    normalises them before the recurrence); v ~ N(0, 1); g = log sigmoid(N(0,1) + 3)
+    (decay factors near 0.95); beta = sigmoid(N(0, 1)); the live state
+    [layers, B, H, dv, dk] ~ N(0, 1). scale = 1/sqrt(dk).
+    """
+    g = generator if generator is not None else _gen(device, (w.seed if seed is None else seed) + 15485863)
+    L, B, R, H, dk, dv = layers, w.batch, w.rows, w.gdn_heads, w.gdn_dk, w.gdn_dv
+    q = torch.randn((L, B, R, H, dk), generator=g, device=device)
+    k = torch.randn((L, B, R, H, dk), generator=g, device=device)
+    q = q / q.norm(dim=-1, keepdim=True)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn((L, B, R, H, dv), generator=g, device=device)
+    gate = torch.nn.functional.logsigmoid(torch.randn((L, B, R, H), generator=g, device=device) + 3.0)
+    beta = torch.sigmoid(torch.randn((L, B, R, H), generator=g, device=device))
+    state = torch.empty((L, B, H, dv, dk), dtype=torch.float32, device=device)
+    for l in range(L):
+        state[l] = torch.randn((B, H, dv, dk), generator=g, device=device)
+    return {"q": q.contiguous(), "k": k.contiguous(), "v": v.contiguous(), "g": gate.contiguous(),
+            "beta": beta.contiguous(), "state": state, "scale": 1.0 / float(dk) ** 0.5}
+
+
 def kv_bytes(ctx_lens, num_kv_heads: int, head_dim: int) -> int:
     """Bytes of K and V (bf16) that the visible tokens occupy."""
     return int(sum(int(c) for c in ctx_lens)) * num_kv_heads * head_dim * 2 * 2

@@ -109,3 +109,25 @@ def test_accept_and_commit_host_validation(lib):
     assert sel(live=None) == -1
     assert sel(L=0) == 0      # nothing to do: no launch
     assert sel(B=0, live=None) == 0
+
+
+def test_gdn_host_validation(lib):
+    fake = ctypes.c_void_p(256)
+    gv = lambda B=2, R=4, H=2, dk=16, dv=16, W=4, a=0, state=fake: lib.spec_gdn_verify(
+        fake, fake, fake, fake, fake, ctypes.c_float(0.25), state, fake, fake, B, R, H, dk, dv, W, a, None, None)
+    assert gv(R=0) == -1
+    assert gv(R=33) == -1     # longer than a verify chain can be
+    assert gv(W=3) == -1      # window shorter than the chain
+    assert gv(a=2) == -1
+    assert gv(H=0) == -1
+    assert gv(dk=0) == -1
+    assert gv(state=None) == -1
+    assert gv(B=0) == 0       # nothing to do: no launch
+    assert gv(dk=512, dv=512) == -2  # state too large for either kernel
+    gp = lambda B=2, rows=10, live=fake, a=0: lib.spec_gdn_verify_pooled(
+        fake, fake, fake, fake, fake, ctypes.c_float(0.25), fake, rows, live, fake, fake, B, 4, 2, 16, 16, 4, a,
+        None, None)
+    assert gp(rows=0) == -1
+    assert gp(live=None) == -1
+    assert gp(a=5) == -1
+    assert gp(B=0) == 0
