@@ -218,8 +218,9 @@ def workload_for(args):
 
 
 def recorded_traffic(workload):
-    """DRAM bytes per attention call from an ncu capture, if taken on the current source."""
-    if not os.path.exists(TRAFFIC_FILE):
+    """DRAM bytes per attention call from an ncu capture, if taken on the current source with the
+    kernel the library picks by itself (a SPEC_ATTN_KERNEL override runs another kernel)."""
+    if not os.path.exists(TRAFFIC_FILE) or os.environ.get("SPEC_ATTN_KERNEL"):
         return None
     with open(TRAFFIC_FILE) as f:
         rec = json.load(f)
