@@ -125,6 +125,14 @@ def accept_bytes(w, modes, accept_len):
     return total
 
 
+def acceptance_rate(alen, k):
+    """Per-position acceptance rate: accepted drafts over decided drafts (a row that
+    stops at m < k decided m + 1 drafts, a fully accepted row k)."""
+    alen = np.asarray(alen, dtype=np.int64)
+    decided = np.where(alen < k, alen + 1, k).sum()
+    return float(alen.sum() / decided) if decided else None
+
+
 def commit_bytes(w, commit="copy"):
     if not w.gdn_layers:
         return 0
@@ -410,6 +418,7 @@ def run_native(args, world, rank, local):
                    "l2": "flushed between timed steps (512 MiB write, then 512 MiB read)",
                    "timing": "CUDA-graph replay of the step, CUDA events on the launching stream"},
         "verified_tokens_per_step": tokens_all, "mean_accept_len": float(np.mean(alen_h)),
+        "acceptance_rate": acceptance_rate(alen_h, w.k_draft),
         "kernels": kernels, "roofline": roofline, "clocks": clk, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
     }

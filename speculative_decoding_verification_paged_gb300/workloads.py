@@ -92,6 +92,13 @@ WORKLOADS = {
         name="llama8b_eagle3", batch=32, ctx_lens=(2048,) * 32, block_size=64, num_q_heads=32,
         num_kv_heads=8, head_dim=128, k_draft=3, vocab=128256, logit_sigma=3.0,
         noise_sigma=1.5, mode="sample", temperature=(1.0, 1.0), seed=1),
+    # The same step with the draft noise calibrated so that about 70% of drafts
+    # are accepted, the rate the MTP validation runs report (the literal noise
+    # of 1.5 gives about 46%).
+    "llama8b_eagle3_cal": Workload(
+        name="llama8b_eagle3_cal", batch=32, ctx_lens=(2048,) * 32, block_size=64, num_q_heads=32,
+        num_kv_heads=8, head_dim=128, k_draft=3, vocab=128256, logit_sigma=3.0,
+        noise_sigma=0.75, mode="sample", temperature=(1.0, 1.0), seed=1),
     # A full serving batch (max_batch_size 128) with ragged contexts and mixed rows.
     "serving128": Workload(
         name="serving128", batch=128, ctx_range=(512, 8192), block_size=64, num_q_heads=32,

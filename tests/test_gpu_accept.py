@@ -40,6 +40,7 @@ def oracle_accept(oracle_mod, inp, modes, probs="given"):
 
 CASES = [
     ("tiny", "sample"), ("tiny", "greedy"), ("llama8b_eagle3", "sample"), ("llama8b_eagle3", "greedy"),
+    ("llama8b_eagle3_cal", "sample"),
     ("serving128", "mixed"), ("hybrid_gdn", "sample"), ("hybrid_gdn", "greedy"), ("longctx", "sample"),
 ]
 
