@@ -1,7 +1,7 @@
 """Pins of the CPU oracle to facts outside itself (CPU only).
 
-Each test ties one oracle function to something it does not compute: published
-known-answer vectors, closed forms, library routines (numpy argmax, scipy's
+Each test ties one oracle function to something it does not compute: closed
+forms, library routines (a library Philox run on the CPU, numpy argmax, scipy's
 logistic function and chi-square test), invariances of the definition, or the
 output layout printed on the pages. A plausible slip in the oracle (a dropped
 scale, a wrong slot or block index, a transposed head mapping, a sign error in
@@ -32,14 +32,57 @@ def bits_to_f64(b: np.ndarray) -> np.ndarray:
 # Philox and the uniform map
 # --------------------------------------------------------------------------
 
-def test_philox_known_answer_vectors(oracle_mod):
-    rows = [l.split() for l in open(os.path.join(GOLDEN, "philox4x32_10_kat.txt"))
-            if l.strip() and not l.startswith("#")]
-    assert len(rows) == 3
-    for r in rows:
-        vals = [int(v, 16) for v in r]
-        out = oracle_mod.philox4x32_10(vals[0:4], vals[4:6])
-        assert [int(v) for v in out] == vals[6:10]
+_TRITON_PHILOX = r"""
+import json, sys
+import torch, triton, triton.language as tl
+
+@triton.jit
+def philox_kernel(c0p, c1p, c2p, c3p, o0p, o1p, o2p, o3p, seed, N: tl.constexpr):
+    offs = tl.arange(0, N)
+    r0, r1, r2, r3 = tl.philox(seed, tl.load(c0p + offs), tl.load(c1p + offs), tl.load(c2p + offs),
+                               tl.load(c3p + offs), 10)
+    tl.store(o0p + offs, r0)
+    tl.store(o1p + offs, r1)
+    tl.store(o2p + offs, r2)
+    tl.store(o3p + offs, r3)
+
+cases = json.loads(sys.stdin.read())
+result = []
+for seed, ctrs in cases:
+    n = len(ctrs)
+    c = [torch.tensor([x[j] for x in ctrs], dtype=torch.int64).to(torch.uint32) for j in range(4)]
+    o = [torch.zeros(n, dtype=torch.uint32) for _ in range(4)]
+    philox_kernel[(1,)](*c, *o, seed, N=n)
+    result.append([[int(o[j][i].to(torch.int64)) & 0xFFFFFFFF for j in range(4)] for i in range(n)])
+print(json.dumps(result))
+"""
+
+
+def test_philox_matches_library_reference(oracle_mod):
+    """Philox4x32-10 against a library implementation run on the CPU (Triton's
+    tl.philox under its interpreter: the Salmon et al. round function with the
+    same constants, key = seed split into its low and high words), over a sweep
+    of counters and keys that includes the all-zero and all-ones corners."""
+    import json
+    import subprocess
+    import sys
+
+    pytest.importorskip("triton")
+    rng = np.random.default_rng(2011)
+    cases = []
+    for seed in (0, 0xFFFFFFFFFFFFFFFF, 0x299F31D0A4093822, int(rng.integers(0, 2**63))):
+        ctrs = [[0, 0, 0, 0], [0xFFFFFFFF] * 4, [1, 0, 0, 0], [0, 0, 0, 1]]
+        ctrs += rng.integers(0, 2**32, size=(12, 4), dtype=np.uint64).tolist()
+        cases.append([seed, [[int(v) for v in c] for c in ctrs]])
+    env = dict(os.environ, TRITON_INTERPRET="1")
+    proc = subprocess.run([sys.executable, "-c", _TRITON_PHILOX], input=json.dumps(cases), env=env,
+                          capture_output=True, text=True, timeout=600, cwd=os.path.dirname(GOLDEN))
+    assert proc.returncode == 0, proc.stderr[-2000:]
+    ref = json.loads(proc.stdout.strip().splitlines()[-1])
+    for (seed, ctrs), want in zip(cases, ref):
+        key = [seed & 0xFFFFFFFF, seed >> 32]
+        for c, w in zip(ctrs, want):
+            assert [int(x) for x in oracle_mod.philox4x32_10(c, key)] == w, (seed, c)
 
 
 def test_uniform_map_endpoints(oracle_mod):
