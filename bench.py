@@ -216,6 +216,35 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def live_ceilings(dev):
+    """Same-run context for the roofline: a 1 GiB device-to-device copy (read + write
+    bytes) and a 2 GiB read-only reduction, best of 5, CUDA events; taken after the
+    timed region."""
+    src = torch.ones(1 << 28, dtype=torch.float32, device=dev)
+    dst = torch.empty_like(src)
+    big = torch.ones(1 << 29, dtype=torch.float32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def best(fn, nbytes):
+        fn()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(5):
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1))
+        return nbytes / (min(t) / 1e3) / 1e9
+
+    out = {"copy_gbs": best(lambda: dst.copy_(src), 2 * src.numel() * 4),
+           "read_gbs": best(lambda: big.sum(), big.numel() * 4),
+           "how": "1 GiB copy_ (read+write bytes) and a 2 GiB sum, best of 5, after the timed region"}
+    del src, dst, big
+    torch.cuda.empty_cache()
+    return out
+
+
 def workload_for(args):
     w = wl.WORKLOADS[args.config]
     if args.gdn_layers is not None:
@@ -397,7 +426,8 @@ def run_native(args, world, rank, local):
     dk = kernels[dominant]
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["GBps"], "peak": peak, "unit": "GB/s",
                 "frac": dk["frac"], "peak_source": peak_kind,
-                "traffic": recorded_traffic(args.config) if dominant == "attention" else None}
+                "traffic": recorded_traffic(args.config) if dominant == "attention" else None,
+                "same_run_ceilings": live_ceilings(dev)}
 
     e2e = None
     if not args.no_e2e:
