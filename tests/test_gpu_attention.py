@@ -124,6 +124,30 @@ def test_attention_large_batch_plans(sv, oracle_mod, attn_kernel, B, Hq, k):
     assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
 
 
+@pytest.mark.parametrize("B", [8, 16, 40, 48])
+@pytest.mark.parametrize("bad_row", [False, True], ids=["uniform", "one_unusable"])
+def test_attention_uniform_context_split_plans(sv, oracle_mod, attn_kernel, B, bad_row):
+    """Equal context lengths, so every (sequence, kv head) unit has the same tile
+    count: 8 kv heads x B sequences = 64 / 128 / 320 / 384 units take, on the
+    mma.sync kernel's 304-CTA grid, the even stream-K split, one whole unit per
+    CTA, the stream-K split again (whole units would load 1.9x) and two whole
+    units per CTA; the tcgen05 kernel's 152-CTA grid gives other cases of the
+    same rule. An unusable sequence (context shorter than the chain) must not
+    change the plan of the others."""
+    w = wl.WORKLOADS["llama8b_eagle3"].replace(batch=B, ctx_lens=(1024,) * B, seed=B + 7 * bad_row)
+    a = wl.make_attention_inputs(w, device=DEV)
+    if bad_row:
+        a["ctx_lens"][B // 3] = 2  # < k + 1: zero rows and an error bit, excluded from the unit lengths
+    out, err = run_attention(sv, a, w)
+    assert err == (sv.DEVERR["ctx_len"] if bad_row else 0)
+    picks = sorted({0, B // 2, B - 1} - ({B // 3} if bad_row else set()))
+    ref = oracle_attention_for(oracle_mod, a, seqs=np.array(picks, np.int32))
+    mx, rel = attention_errors(out[picks].cpu().numpy(), ref)
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+    if bad_row:
+        assert torch.all(out[B // 3] == 0)
+
+
 @pytest.mark.parametrize("name", ["longctx", "llama8b_eagle3"])
 def test_attention_default_kernel_choice(sv, oracle_mod, monkeypatch, name):
     """No override: the library picks the kernel (tcgen05 for 64 rows, mma.sync for 16)."""
