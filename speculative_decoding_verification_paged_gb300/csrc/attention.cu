@@ -90,7 +90,12 @@ struct Cfg {
   static constexpr int TILE_BYTES = TK * D * 2;   // one K (or V) tile
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int Q_BYTES = ROWS * D * 2;
-  static constexpr int S = (3 * (STAGE_BYTES + Q_BYTES) <= kSmemBudget) ? 3 : 2;  // pipeline depth
+  // Pipeline depth: three stages when they fit; a kernel that runs one CTA per
+  // SM anyway takes a fourth when it fits too, for more bytes in flight per SM
+  // (the per-slot tables hold up to four stages).
+  static constexpr int S3 = (3 * (STAGE_BYTES + Q_BYTES) <= kSmemBudget) ? 3 : 2;
+  static constexpr bool ONE_CTA_PER_SM = 2 * (1024 + S3 * (STAGE_BYTES + Q_BYTES) + 2048 + 1024) > 228 * 1024;
+  static constexpr int S = (ONE_CTA_PER_SM && S3 == 3 && 4 * (STAGE_BYTES + Q_BYTES) <= kSmemBudget) ? 4 : S3;
   static constexpr int RING_BYTES = S * STAGE_BYTES;
   static constexpr int SCRATCH_BYTES = (WN - 1) * MT * 16 * D * 4;  // cross-warp merge
   // Two CTAs per SM when their shared memory fits (228 KB per SM, 1 KB reserved per CTA);
@@ -102,6 +107,7 @@ struct Cfg {
   static_assert(KW % 16 == 0, "each warp needs whole 16-key steps");
   static_assert(WN * MT == kWarps, "warp layout");
   static_assert(SCRATCH_BYTES <= STAGE_BYTES, "merge scratch reuses one ring stage");
+  static_assert(S <= 4, "per-slot tables (bad-block flags) hold four stages");
 };
 
 template <int D, int MT>
