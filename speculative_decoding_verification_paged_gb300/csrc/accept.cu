@@ -564,56 +564,57 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
   p.prefetch = 1;
 
   auto kern = acc::accept_kernel;
+  const int dev = current_device();
+  if (dev < 0) return SPEC_ERR_LAUNCH;
+  // The cluster plan (size, slice, groups per CTA) depends only on the device and
+  // the vocabulary: it is worked out once per (device, vocabulary), together with
+  // the kernel attributes, under a lock shared by all host threads.
+  static LaunchMemo memo;
+  static int plan_vocab[kMaxDevices], plan_csize[kMaxDevices], plan_slice[kMaxDevices], plan_gpc[kMaxDevices];
+  static bool nonportable[kMaxDevices];
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-  // Function attributes and the cluster-size probe depend only on (device, slice):
-  // remember the last answer so steady-state calls make no extra runtime queries.
-  static int cached_dev = -1, cached_vocab = -1, cached_csize = 0, cached_slice = 0, cached_gpc = 0;
-  static size_t cached_smem = 0;
-  const bool cached = dev == cached_dev && vocab == cached_vocab;
-  if (cached) {
-    p.csize = cached_csize;
-    p.slice = cached_slice;
-    p.gpc = cached_gpc;
-  }
-  // Clusters larger than 8 CTAs are not guaranteed to fit a GPC; if the device
-  // cannot hold one, use 8 CTAs with larger slices.
-  for (int attempt = 0; attempt < 2; ++attempt) {
-    const size_t smem = (size_t)p.slice * sizeof(float);
-    if (!cached || smem > cached_smem) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return SPEC_ERR_LAUNCH;
-      if (p.csize > 8 &&
-          cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-        return SPEC_ERR_LAUNCH;
-      cached_smem = smem > cached_smem ? smem : cached_smem;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(acc::kThreads, 1, 1);
+  cfg.stream = stream;
+  {
+    std::lock_guard<std::mutex> lock(memo.mu);
+    if (plan_vocab[dev] != vocab) {  // vocab >= 1, so 0 marks "no plan yet"
+      // Clusters larger than 8 CTAs are not guaranteed to fit a GPC; if the
+      // device cannot hold one, use 8 CTAs with larger slices.
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        if (!grant_smem_locked(memo, (const void*)kern, dev, (size_t)p.slice * sizeof(float))) return SPEC_ERR_LAUNCH;
+        if (p.csize <= 8) break;
+        if (!nonportable[dev]) {
+          if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            return SPEC_ERR_LAUNCH;
+          nonportable[dev] = true;
+        }
+        cfg.gridDim = dim3((unsigned)p.csize, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)p.slice * sizeof(float);
+        attr[0].val.clusterDim.x = (unsigned)p.csize;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0) break;
+        (void)cudaGetLastError();
+        p.csize = acc::pick_cluster(vocab, 8, p.slice, p.gpc);
+        if (p.gpc > acc::kMaxGroupsPerCta) return SPEC_ERR_UNSUPPORTED;
+      }
+      plan_csize[dev] = p.csize;
+      plan_slice[dev] = p.slice;
+      plan_gpc[dev] = p.gpc;
+      plan_vocab[dev] = vocab;
     }
-    cfg.gridDim = dim3((unsigned)(batch * p.csize), 1, 1);
-    cfg.blockDim = dim3(acc::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cached || p.csize <= 8) break;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0) break;
-    (void)cudaGetLastError();
-    p.csize = acc::pick_cluster(vocab, 8, p.slice, p.gpc);
-    if (p.gpc > acc::kMaxGroupsPerCta) return SPEC_ERR_UNSUPPORTED;
+    p.csize = plan_csize[dev];
+    p.slice = plan_slice[dev];
+    p.gpc = plan_gpc[dev];
   }
-  if (!cached) {
-    cached_dev = dev;
-    cached_vocab = vocab;
-    cached_csize = p.csize;
-    cached_slice = p.slice;
-    cached_gpc = p.gpc;
-  }
+  cfg.gridDim = dim3((unsigned)(batch * p.csize), 1, 1);
+  cfg.dynamicSmemBytes = (size_t)p.slice * sizeof(float);
+  attr[0].val.clusterDim.x = (unsigned)p.csize;
   if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return SPEC_ERR_LAUNCH;
   return SPEC_OK;
 }

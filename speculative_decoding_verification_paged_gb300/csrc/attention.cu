@@ -1585,23 +1585,25 @@ static int launch_main(const Params& p, const CUtensorMap& tq, const CUtensorMap
                        cudaStream_t stream) {
   auto kern = verify_attention_kernel<D, MT>;
   const size_t smem = smem_bytes<D, MT>(p.batch);
-  static int cached_dev = -1, cached_grid = 0;
-  static size_t cached_smem = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-  if (dev != cached_dev || smem != cached_smem) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return SPEC_ERR_LAUNCH;
-    int sms = 0, per_sm = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
-      return SPEC_ERR_LAUNCH;
-    if (per_sm < 1) return SPEC_ERR_UNSUPPORTED;
-    cached_grid = sms * per_sm > kMaxGrid ? kMaxGrid : sms * per_sm;
-    cached_dev = dev;
-    cached_smem = smem;
+  static LaunchMemo memo;
+  const int dev = current_device();
+  if (dev < 0) return SPEC_ERR_LAUNCH;
+  int grid = 0;
+  {
+    std::lock_guard<std::mutex> lock(memo.mu);
+    if (memo.grid_smem[dev] != smem) {
+      if (!grant_smem_locked(memo, (const void*)kern, dev, smem)) return SPEC_ERR_LAUNCH;
+      int sms = 0, per_sm = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+        return SPEC_ERR_LAUNCH;
+      if (per_sm < 1) return SPEC_ERR_UNSUPPORTED;
+      memo.grid[dev] = sms * per_sm > kMaxGrid ? kMaxGrid : sms * per_sm;
+      memo.grid_smem[dev] = smem;
+    }
+    grid = memo.grid[dev];
   }
-  kern<<<cached_grid, kThreads, smem, stream>>>(p, tq, tk, tv);
+  kern<<<grid, kThreads, smem, stream>>>(p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
@@ -1621,20 +1623,22 @@ static int launch_tc(const Params& p, const CUtensorMap& tq, const CUtensorMap& 
                      cudaStream_t stream) {
   auto kern = tc::verify_attention_tc_kernel<MT, S, NP>;
   const size_t smem = tc::smem_bytes<MT, S, NP>(p.batch);
-  static int cached_dev = -1, cached_grid = 0;
-  static size_t cached_smem = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-  if (dev != cached_dev || smem != cached_smem) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return SPEC_ERR_LAUNCH;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-    cached_grid = sms > kMaxGrid ? kMaxGrid : sms;
-    cached_dev = dev;
-    cached_smem = smem;
+  static LaunchMemo memo;
+  const int dev = current_device();
+  if (dev < 0) return SPEC_ERR_LAUNCH;
+  int grid = 0;
+  {
+    std::lock_guard<std::mutex> lock(memo.mu);
+    if (memo.grid_smem[dev] != smem) {
+      if (!grant_smem_locked(memo, (const void*)kern, dev, smem)) return SPEC_ERR_LAUNCH;
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+      memo.grid[dev] = sms > kMaxGrid ? kMaxGrid : sms;
+      memo.grid_smem[dev] = smem;
+    }
+    grid = memo.grid[dev];
   }
-  kern<<<cached_grid, tc::kThreads, smem, stream>>>(p, tq, tk, tv);
+  kern<<<grid, tc::kThreads, smem, stream>>>(p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 

@@ -280,23 +280,22 @@ static int launch(Params& p, cudaStream_t stream) {
   const bool aligned = ((reinterpret_cast<uintptr_t>(state_base) | reinterpret_cast<uintptr_t>(snap_base)) & 15) == 0;
   if (p.dk == kFastDim && p.dv == kFastDim && aligned) {
     const size_t smem = (size_t)3 * p.tokens * kFastDim * sizeof(float);
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-      if (cudaFuncSetAttribute(gdn_verify_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess)
-        return SPEC_ERR_LAUNCH;
-      configured = smem;
+    static LaunchMemo memo;
+    if (smem > 48 * 1024) {
+      const int dev = current_device();
+      std::lock_guard<std::mutex> lock(memo.mu);
+      if (dev < 0 || !grant_smem_locked(memo, (const void*)gdn_verify_fast_kernel, dev, smem)) return SPEC_ERR_LAUNCH;
     }
     gdn_verify_fast_kernel<<<(unsigned)units, kThreads, smem, stream>>>(p);
   } else {
     const size_t smem = sizeof(float) * ((size_t)p.dv * p.dk + (size_t)p.tokens * (2 * p.dk + p.dv) + 3 * (size_t)p.dv);
     if (smem > 200 * 1024) return SPEC_ERR_UNSUPPORTED;
-    static size_t configured = 0;
-    if (smem > 48 * 1024 && smem > configured) {
-      if (cudaFuncSetAttribute(gdn_verify_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess)
+    static LaunchMemo memo;
+    if (smem > 48 * 1024) {
+      const int dev = current_device();
+      std::lock_guard<std::mutex> lock(memo.mu);
+      if (dev < 0 || !grant_smem_locked(memo, (const void*)gdn_verify_generic_kernel, dev, smem))
         return SPEC_ERR_LAUNCH;
-      configured = smem;
     }
     gdn_verify_generic_kernel<<<(unsigned)units, kThreads, smem, stream>>>(p);
   }
