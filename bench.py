@@ -602,7 +602,9 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     result = run_native(args, world, rank, local)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if args.no_cpu_baseline or world > 1:  # the oracle baseline is an N = 1 measurement
+            result["cpu_baseline"] = None
+        else:
             w = workload_for(args)
             s, tokens, sample, threads = oracle_step_estimate(w, args.mode or w.mode, args.cpu_seconds,
                                                               commit=args.commit, gdn_verify=args.gdn_verify)
