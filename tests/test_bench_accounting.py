@@ -1,0 +1,52 @@
+"""The algorithmic byte counts behind every roofline fraction bench.py reports,
+checked on small cases worked out by hand (CPU only)."""
+
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from speculative_decoding_verification_paged_gb300 import workloads as wl  # noqa: E402
+
+
+def test_attention_bytes_by_hand():
+    # 2 sequences of 5 and 70 tokens, 2 kv heads x 8 dims, 4 q heads, 3 drafts, blocks of 16
+    w = wl.Workload(name="t", batch=2, ctx_lens=(5, 70), block_size=16, num_q_heads=4, num_kv_heads=2,
+                    head_dim=8, k_draft=3)
+    kv = 75 * 2 * 8 * 2 * 2        # visible tokens x kv heads x dims x bf16 x (K, V)
+    qo = 2 * 4 * 4 * 8 * (2 + 4)   # rows x q heads x dims x (bf16 q in + fp32 out)
+    table = (1 + 5) * 4 + 2 * 4    # block ids used (1 + 5 blocks) + ctx_lens
+    assert bench.attention_bytes(w, [5, 70]) == kv + qo + table == 6368
+
+
+def test_accept_bytes_by_hand():
+    # V = 1000, k = 3; a greedy row that stops at 0, a sampling row that keeps all three
+    # drafts and a sampling row that stops at 1; an invalid row reads nothing but the fixed part
+    w = wl.Workload(name="t", batch=4, ctx_lens=(8,) * 4, vocab=1000, k_draft=3)
+    greedy_0 = 1 * 4000                                # logit row 0
+    sample_3 = 4 * 4000 + 0 + 3 * 32                   # rows 0..3, no residual row, q(d_j) sectors
+    sample_1 = 2 * 4000 + 4000 + 1 * 32                # rows 0..1, draft row 1 of the race, q(d_0)
+    fixed = 4 * (3 * 4 + 4 + 4 + 4 * 4 + 4)            # drafts, mode, temperature, out_tokens, accept_len
+    got = bench.accept_bytes(w, [0, 1, 1, 1], [0, 3, 1, -1])
+    assert got == greedy_0 + sample_3 + sample_1 + fixed == 32288
+
+
+def test_acceptance_rate_by_hand():
+    # accepted 0 + 3 + 1 drafts; decided 1 + 3 + 2 (a full row decided k drafts)
+    assert bench.acceptance_rate([0, 3, 1], 3) == pytest.approx(4 / 6)
+    assert bench.acceptance_rate([], 3) is None
+
+
+def test_commit_and_gdn_bytes_by_hand():
+    w = wl.Workload(name="t", batch=3, ctx_lens=(8,) * 3, k_draft=1, gdn_layers=2, gdn_heads=1, gdn_dk=5, gdn_dv=2)
+    assert bench.commit_bytes(w) == 2 * 2 * 3 * 10 * 4           # read the kept slot, write the live state
+    assert bench.commit_bytes(w, "select") == 2 * 3 * 20          # five int32 per (layer, row)
+    g = wl.Workload(name="t", batch=2, ctx_lens=(8,) * 2, k_draft=1, gdn_layers=1, gdn_heads=3, gdn_dk=4, gdn_dv=4)
+    states = 2 * 3 * (4 * 4 * 4) * (1 + 2)                       # read once, write one checkpoint per token
+    acts = 2 * 2 * 3 * (2 * 4 + 2 * 4) * 4                       # q, k, v, out per token and head
+    gates = 2 * 2 * 3 * 8                                        # g and beta
+    assert bench.gdn_verify_bytes(g) == states + acts + gates == 2016
