@@ -119,8 +119,11 @@ size_t spec_verify_attention_workspace(const spec_attn_desc* d, int32_t k_draft)
  *
  * The key tiles of all (sequence, kv head) units are split evenly over the
  * CTAs (split-KV); a unit held by several CTAs is merged by its log-sum-exp
- * inside the same launch. The split is chosen on the device from ctx_lens, so
- * no host synchronisation is needed.
+ * inside the same launch. When all units have the same length, CTAs take
+ * whole units instead as long as the load stays close to even. The split is
+ * chosen on the device from ctx_lens, so no host synchronisation is needed.
+ * Calls may come from several host threads at once (each with its own
+ * workspace and stream).
  * Kernels: D = 128 with (k_draft+1)*G >= 17 packed query rows runs on the
  * 5th-generation tensor cores (tcgen05, 128-key tiles, accumulators in tensor
  * memory) when that kernel's shared-memory plan fits the batch; other shapes

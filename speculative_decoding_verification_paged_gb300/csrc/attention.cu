@@ -1552,17 +1552,18 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// Resolved once per process (a function-local static is initialised exactly
+// once even when several host threads arrive together).
 static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
       return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
   return fn;
 }
 
@@ -1820,13 +1821,19 @@ extern "C" int spec_verify_attention_noalloc(const void* q, const void* k_cache,
   // Set-up, once per device, with that device current: the device address of
   // the scratch array (host code cannot use the symbol itself).
   static void* scratch_addr[attn::kNoAllocMaxDevices] = {};
+  static std::mutex scratch_mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= attn::kNoAllocMaxDevices) return SPEC_ERR_LAUNCH;
-  if (scratch_addr[dev] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, attn::g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
-      return SPEC_ERR_LAUNCH;
-    scratch_addr[dev] = ptr;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(scratch_mu);
+    if (scratch_addr[dev] == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, attn::g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+        return SPEC_ERR_LAUNCH;
+      scratch_addr[dev] = ptr;
+    }
+    scratch = scratch_addr[dev];
   }
 
   const int R = k_draft + 1, G = d->num_q_heads / d->num_kv_heads, D = d->head_dim;
@@ -1848,7 +1855,7 @@ extern "C" int spec_verify_attention_noalloc(const void* q, const void* k_cache,
   const size_t total = opart_off + attn::align256((size_t)(slots * n_rows * D * 4));
   if (total > attn::kNoAllocScratchBytes) return SPEC_ERR_SCRATCH_LIMIT;
 
-  uint8_t* ws = static_cast<uint8_t*>(scratch_addr[dev]);
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
   // The counters must start at zero; every call shares the array, so clear them here.
   if (cudaMemsetAsync(ws, 0, counters_bytes, stream) != cudaSuccess) return SPEC_ERR_LAUNCH;
 
