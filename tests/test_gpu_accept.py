@@ -221,3 +221,33 @@ def test_accept_invalid_rows_flagged(sv):
     tok, alen, err = run_accept(sv, inp, modes)
     assert alen[0] == k and np.all(alen[1:] == -1) and np.all(tok[1:] == -1)
     assert err & sv.DEVERR["token"] and err & sv.DEVERR["temperature"] and err & sv.DEVERR["mode"]
+
+
+@pytest.mark.parametrize("vocab", [1000, 1001], ids=["aligned", "unaligned"])
+def test_accept_many_waves(sv, oracle_mod, vocab):
+    """1400 rows of a 1000-word vocabulary (one CTA per row) run in several waves
+    of resident CTAs; aligned rows (bulk copies) and unaligned ones (plain loads)."""
+    w = wl.WORKLOADS["tiny"].replace(vocab=vocab, batch=1400, mode="mixed")
+    inp = wl.make_accept_inputs(w, device=DEV)
+    tok, alen, err = run_accept(sv, inp, inp["mode"])
+    rt, ra, margin, gap, rc = oracle_accept(oracle_mod, inp, inp["mode"])
+    assert err == 0 and rc == 0
+    bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
+    assert bad == 0
+
+
+@pytest.mark.parametrize("batch", [64, 1400], ids=["one_wave", "many_waves"])
+def test_accept_all_zero_residual_races_over_p(sv, oracle_mod, batch):
+    """Draft probabilities at twice the target's make max(0, p - q) zero everywhere
+    while drafts are still rejected (whenever u >= 1/2): the correction token is
+    then drawn from p itself (the slice is reloaded over the residual weights)."""
+    w = wl.WORKLOADS["tiny"].replace(vocab=1000, batch=batch, mode="sample")
+    inp = wl.make_accept_inputs(w, device=DEV)
+    T = inp["temperature"].view(-1, 1, 1)
+    inp["draft_probs"] = (2.0 * torch.softmax(inp["target_logits"][:, :w.k_draft] / T, dim=-1)).contiguous()
+    tok, alen, err = run_accept(sv, inp, inp["mode"])
+    rt, ra, margin, gap, rc = oracle_accept(oracle_mod, inp, inp["mode"])
+    assert err == 0 and rc == 0
+    assert (ra < w.k_draft).sum() > batch // 4  # rejections happen (u >= 1/2 at some position)
+    bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
+    assert bad == 0
