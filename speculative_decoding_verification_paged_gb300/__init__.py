@@ -119,7 +119,11 @@ def _check(fn: str, rc: int):
 
 
 def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    """The stream to launch on; it must belong to the current device (the one the
+    library launches on)."""
     s = torch.cuda.current_stream() if stream is None else stream
+    if s.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream is on {s.device}, the current device is cuda:{torch.cuda.current_device()}")
     return int(s.cuda_stream)
 
 
@@ -128,6 +132,9 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, the call runs on the current device "
+                         f"cuda:{torch.cuda.current_device()}")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != ndim:
@@ -138,6 +145,18 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
 
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _err_ptr(dev_err: Optional[torch.Tensor]):
+    """The optional device error word: an int32 CUDA tensor of at least one element."""
+    if dev_err is None:
+        return None
+    if not isinstance(dev_err, torch.Tensor) or not dev_err.is_cuda or dev_err.dtype != torch.int32 \
+            or dev_err.numel() < 1:
+        raise ValueError("dev_err must be an int32 CUDA tensor with at least one element")
+    if dev_err.device.index != torch.cuda.current_device():
+        raise ValueError(f"dev_err is on {dev_err.device}, the call runs on cuda:{torch.cuda.current_device()}")
+    return ctypes.c_void_p(dev_err.data_ptr())
 
 
 def _attn_desc(q, k_cache, block_table) -> _AttnDesc:
@@ -183,7 +202,7 @@ def spec_verify_attention(q, k_cache, v_cache, block_table, ctx_lens, k_draft: i
     _need(workspace, "workspace", torch.uint8, 1)
     rc = lib.spec_verify_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens),
                                    int(k_draft), _ptr(out), ctypes.byref(d), _ptr(workspace),
-                                   workspace.numel(), _ptr(dev_err), _stream_handle(stream))
+                                   workspace.numel(), _err_ptr(dev_err), _stream_handle(stream))
     _check("spec_verify_attention", rc)
     return out
 
@@ -208,7 +227,7 @@ def spec_verify_attention_noalloc(q, k_cache, v_cache, block_table, ctx_lens, k_
     d = _attn_desc(q, k_cache, block_table)
     rc = lib.spec_verify_attention_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
                                            _ptr(ctx_lens), int(k_draft), _ptr(out), ctypes.byref(d),
-                                           _ptr(dev_err), _stream_handle(stream))
+                                           _err_ptr(dev_err), _stream_handle(stream))
     _check("spec_verify_attention_noalloc", rc)
     return out
 
@@ -235,7 +254,7 @@ def spec_accept(target_logits, draft_tokens, draft_probs, philox_seed: int, mode
         raise ValueError("draft_probs must be [B, k, V]")
     rc = lib.spec_accept(_ptr(target_logits), _ptr(draft_tokens), _ptr(draft_probs),
                          int(philox_seed) & 0xFFFFFFFFFFFFFFFF, _ptr(mode), _ptr(temperature),
-                         _ptr(out_tokens), _ptr(accept_len), B, k, V, _ptr(dev_err), _stream_handle(stream))
+                         _ptr(out_tokens), _ptr(accept_len), B, k, V, _err_ptr(dev_err), _stream_handle(stream))
     _check("spec_accept", rc)
     return out_tokens, accept_len
 
@@ -251,7 +270,7 @@ def spec_commit_state(snapshots, accept_len, live_state, dev_err: Optional[torch
     if live_state.shape != (L, B, E) or accept_len.shape != (B,):
         raise ValueError("inconsistent commit shapes")
     rc = lib.spec_commit_state(_ptr(snapshots), _ptr(accept_len), _ptr(live_state), L, B, S, E,
-                               _ptr(dev_err), _stream_handle(stream))
+                               _err_ptr(dev_err), _stream_handle(stream))
     _check("spec_commit_state", rc)
     return live_state
 
@@ -271,7 +290,7 @@ def spec_commit_state_aligned(snapshots, accept_len, live_state, num_tokens: int
     if live_state.shape != (L, B, E) or accept_len.shape != (B,):
         raise ValueError("inconsistent commit shapes")
     rc = lib.spec_commit_state_aligned(_ptr(snapshots), _ptr(accept_len), _ptr(live_state), L, B, W, E,
-                                       int(num_tokens), int(alignment), _ptr(dev_err), _stream_handle(stream))
+                                       int(num_tokens), int(alignment), _err_ptr(dev_err), _stream_handle(stream))
     _check("spec_commit_state_aligned", rc)
     return live_state
 
@@ -289,7 +308,7 @@ def spec_commit_select(accept_len, live_row, ckpt_rows, num_tokens: int, alignme
     if ckpt_rows.shape[:2] != (L, B) or accept_len.shape != (B,):
         raise ValueError("inconsistent commit shapes")
     rc = lib.spec_commit_select(_ptr(accept_len), _ptr(live_row), _ptr(ckpt_rows), L, B, W, int(num_tokens),
-                                int(alignment), _ptr(dev_err), _stream_handle(stream))
+                                int(alignment), _err_ptr(dev_err), _stream_handle(stream))
     _check("spec_commit_select", rc)
     return live_row, ckpt_rows
 
@@ -321,7 +340,7 @@ def spec_gdn_verify(q, k, v, g, beta, state_in, snapshots, out, scale: float, al
     if state_in.shape != (B, H, dv, dk) or snapshots.shape != (B, W, H, dv, dk):
         raise ValueError("inconsistent state shapes")
     rc = lib.spec_gdn_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(state_in),
-                             _ptr(snapshots), _ptr(out), B, R, H, dk, dv, W, int(alignment), _ptr(dev_err),
+                             _ptr(snapshots), _ptr(out), B, R, H, dk, dv, W, int(alignment), _err_ptr(dev_err),
                              _stream_handle(stream))
     _check("spec_gdn_verify", rc)
     return snapshots, out
@@ -342,6 +361,6 @@ def spec_gdn_verify_pooled(q, k, v, g, beta, pool, live_row, ckpt_rows, out, sca
         raise ValueError("inconsistent pool shapes")
     rc = lib.spec_gdn_verify_pooled(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(pool),
                                     pool.shape[0], _ptr(live_row), _ptr(ckpt_rows), _ptr(out), B, R, H, dk, dv, W,
-                                    int(alignment), _ptr(dev_err), _stream_handle(stream))
+                                    int(alignment), _err_ptr(dev_err), _stream_handle(stream))
     _check("spec_gdn_verify_pooled", rc)
     return out

@@ -251,3 +251,29 @@ def test_accept_all_zero_residual_races_over_p(sv, oracle_mod, batch):
     assert (ra < w.k_draft).sum() > batch // 4  # rejections happen (u >= 1/2 at some position)
     bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
     assert bad == 0
+
+
+def test_binding_rejects_tensors_the_kernels_cannot_use(sv):
+    """Host tensors, a malformed error word and tensors on another device are
+    refused before anything is launched."""
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.make_accept_inputs(w, device=DEV)
+    B, R, V = inp["target_logits"].shape
+    toks = torch.empty((B, R), dtype=torch.int32, device=DEV)
+    alen = torch.empty((B,), dtype=torch.int32, device=DEV)
+    args = [inp["target_logits"], inp["draft_tokens"], inp["draft_probs"], inp["philox_seed"], inp["mode"],
+            inp["temperature"], toks, alen]
+    host = list(args)
+    host[0] = inp["target_logits"].cpu()
+    with pytest.raises(ValueError):
+        sv.spec_accept(*host)
+    for bad in (torch.zeros(1, dtype=torch.float32, device=DEV), torch.zeros(1, dtype=torch.int32),
+                torch.zeros(0, dtype=torch.int32, device=DEV)):
+        with pytest.raises(ValueError):
+            sv.spec_accept(*args, dev_err=bad)
+    if torch.cuda.device_count() > 1:
+        other = torch.cuda.Stream(device=1)
+        with pytest.raises(ValueError):
+            sv.spec_accept(*args, stream=other)
+    sv.spec_accept(*args, dev_err=torch.zeros(1, dtype=torch.int32, device=DEV))  # the valid call still works
+    torch.cuda.synchronize()
