@@ -11,7 +11,9 @@
 // in the reject sampler's expected output of lmdeploy PR #3945.
 //
 // Design (GB300): one thread-block cluster per batch row, its CTAs splitting
-// the vocabulary into contiguous slices of at most 16K logits (<= 16 CTAs).
+// the vocabulary into contiguous slices of whole 8192-logit groups (one to
+// six groups per CTA; at most 16 CTAs, 8 where the device cannot schedule a
+// 16-CTA cluster).
 // Positions are processed in order and the row stops at the first rejection,
 // so logits past it are never read (early exit). For each position every CTA
 // pulls its slice into shared memory with one bulk asynchronous copy (TMA,

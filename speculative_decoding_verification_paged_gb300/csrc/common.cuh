@@ -1,4 +1,8 @@
-// Device helpers shared by the verify-step kernels (sm_103a).
+// Helpers shared by the verify-step kernels (sm_103a): the device error word,
+// shared-memory addressing, mbarriers, bulk and TMA copies, thread-block
+// cluster and distributed-shared-memory access, mma.sync fragments, tcgen05
+// MMA / tensor-memory / descriptor helpers, Philox4x32-10 and the uniform map,
+// and the host-side per-device launch settings.
 #pragma once
 
 #include <cuda_runtime.h>
