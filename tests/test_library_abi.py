@@ -131,3 +131,24 @@ def test_gdn_host_validation(lib):
     assert gp(live=None) == -1
     assert gp(a=5) == -1
     assert gp(B=0) == 0
+
+
+def test_plain_c_program_uses_the_boundary(lib, tmp_path):
+    """A C program built with gcc against the header alone links the library and
+    exercises its host-side paths (no GPU needed)."""
+    import shutil
+    import subprocess
+
+    import speculative_decoding_verification_paged_gb300 as sv
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    libdir = os.path.dirname(sv.library_path())
+    exe = str(tmp_path / "c_abi_host_checks")
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c_abi_host_checks.c"), "-L", libdir, "-lspecverify",
+                        "-Wl,-rpath," + libdir, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-3000:]
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", run.stdout + run.stderr
