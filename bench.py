@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--gdn-verify", action="store_true",
                     help="add one gated-delta-net layer's recurrence over the verify chain to the step "
                          "(workloads with recurrent state; pooled when --commit select)")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="draw the synthetic inputs from this seed instead of the workload's own")
     ap.add_argument("--gdn-layers", type=int, default=None,
                     help="override the workload's recurrent-state layer count (small profiler captures); "
                          "the line's config reports the count used")
@@ -247,6 +249,8 @@ def live_ceilings(dev):
 
 def workload_for(args):
     w = wl.WORKLOADS[args.config]
+    if args.seed is not None:
+        w = w.replace(seed=args.seed)
     if args.gdn_layers is not None:
         if not w.gdn_layers or args.gdn_layers < 1:
             raise SystemExit(f"--gdn-layers needs a workload with recurrent state and a count >= 1 ({w.name})")
@@ -335,9 +339,12 @@ def run_native(args, world, rank, local):
         commit()
 
     launches_per_step = 1 + 1 + (1 if w.gdn_layers else 0) + (1 if gv is not None else 0)
+    nvtx = torch.cuda.nvtx  # phase markers for timeline profilers
+    nvtx.range_push("warm-up")
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    nvtx.range_pop()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
 
@@ -386,14 +393,18 @@ def run_native(args, world, rank, local):
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)  # let the sampler start
+    nvtx.range_push("timed steps")
     per_step = timed(graphs["step"], args.steps)
     torch.cuda.synchronize()
+    nvtx.range_pop()
     barrier(world)
     clk = clocks.stop()
+    nvtx.range_push("per-kernel timing")
     t_attn = timed(graphs["attention"], args.steps)
     t_acc = timed(graphs["accept"], args.steps)
     t_cmt = timed(graphs["commit"], args.steps) if "commit" in graphs else [0.0]
     t_gdn = timed(graphs["gdn_verify"], args.steps) if "gdn_verify" in graphs else None
+    nvtx.range_pop()
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())}")
 
@@ -431,13 +442,15 @@ def run_native(args, world, rank, local):
 
     e2e = None
     if not args.no_e2e:
+        nvtx.range_push("end to end")
         e2e = run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush, gv, gdn_verify)
+        nvtx.range_pop()
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "batch_per_gpu": w.batch, "k_draft": w.k_draft, "mode": mode,
+        "config": {"workload": w.name, "batch_per_gpu": w.batch, "k_draft": w.k_draft, "mode": mode, "seed": w.seed,
                    "ctx": list(w.ctx_range) if w.ctx_range else sorted(set(w.ctx_lens)),
                    "block_size": w.block_size, "heads": [w.num_q_heads, w.num_kv_heads], "head_dim": w.head_dim,
                    "vocab": w.vocab, "gdn_layers": w.gdn_layers, "parallelism": f"replicas x{world}",
@@ -583,7 +596,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "batch_per_gpu": w.batch, "k_draft": w.k_draft, "mode": mode,
+        "config": {"workload": w.name, "batch_per_gpu": w.batch, "k_draft": w.k_draft, "mode": mode, "seed": w.seed,
                    "parallelism": "host cores (OpenMP)", **({"commit": args.commit} if w.gdn_layers else {})},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
