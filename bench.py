@@ -36,7 +36,13 @@ UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "llama8b_eagle3"
 L2_FLUSH_BYTES = 512 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-ATTN_SOURCE = os.path.join(ROOT, "speculative_decoding_verification_paged_gb300", "csrc", "attention.cu")
+# The device code of each verify-attention kernel: a recorded ncu traffic figure
+# stays valid while these files hash to the recorded value (host launch code may change).
+_CSRC = "speculative_decoding_verification_paged_gb300/csrc/"
+ATTN_KERNEL_SOURCES = {
+    "mma": [_CSRC + "common.cuh", _CSRC + "attention_device.cuh", _CSRC + "attention_mma.cuh"],
+    "tc": [_CSRC + "common.cuh", _CSRC + "attention_device.cuh", _CSRC + "attention_tc.cuh"],
+}
 
 
 def parse():
@@ -258,16 +264,27 @@ def workload_for(args):
     return w
 
 
-def recorded_traffic(workload):
-    """DRAM bytes per attention call from an ncu capture, if taken on the current source with the
-    kernel the library picks by itself (a SPEC_ATTN_KERNEL override runs another kernel)."""
-    if not os.path.exists(TRAFFIC_FILE) or os.environ.get("SPEC_ATTN_KERNEL"):
+def kernel_sources_sha256(paths):
+    """sha256 over the repo-relative path and the bytes of each file, in order."""
+    h = hashlib.sha256()
+    for rel in paths:
+        h.update(rel.encode() + b"\0")
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload, plan):
+    """DRAM bytes per attention call from an ncu capture, if the capture ran the kernel instance
+    the library plans for this call (`plan`, from spec_verify_attention_plan) and that kernel's
+    device sources are unchanged since."""
+    if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
-        rec = json.load(f)
-    src = hashlib.sha256(open(ATTN_SOURCE, "rb").read()).hexdigest()
-    entry = rec.get(workload)
-    if not entry or entry.get("attention_source_sha256") != src:
+        entry = json.load(f).get(workload)
+    if not entry or entry.get("plan") != plan:
+        return None
+    if entry.get("kernel_sources_sha256") != kernel_sources_sha256(ATTN_KERNEL_SOURCES[plan["kernel"]]):
         return None
     return entry.get("dram_bytes_per_call")
 
@@ -421,8 +438,9 @@ def run_native(args, world, rank, local):
     cb = accept_bytes(w, acc_in["mode"].cpu().numpy(), alen_h)
     mb = commit_bytes(w, "select" if select else "copy")
     ta, tc, tm = statistics.mean(t_attn), statistics.mean(t_acc), statistics.mean(t_cmt)
+    plan = sv.spec_verify_attention_plan(a["q"], a["k_cache"], a["block_table"], w.k_draft)
     kernels = {
-        "attention": {"ms": ta, "bytes": ab, "GBps": ab / ta / 1e6, "frac": ab / ta / 1e6 / peak},
+        "attention": {"ms": ta, "bytes": ab, "GBps": ab / ta / 1e6, "frac": ab / ta / 1e6 / peak, "plan": plan},
         "accept": {"ms": tc, "bytes": cb, "GBps": cb / tc / 1e6, "frac": cb / tc / 1e6 / peak,
                    "full_read_bytes": w.batch * 4 * w.vocab * (R + w.k_draft)},
     }
@@ -437,7 +455,7 @@ def run_native(args, world, rank, local):
     dk = kernels[dominant]
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["GBps"], "peak": peak, "unit": "GB/s",
                 "frac": dk["frac"], "peak_source": peak_kind,
-                "traffic": recorded_traffic(args.config) if dominant == "attention" else None,
+                "traffic": recorded_traffic(args.config, plan) if dominant == "attention" else None,
                 "same_run_ceilings": live_ceilings(dev)}
 
     e2e = None

@@ -172,6 +172,35 @@ int spec_verify_attention_noalloc(const void* q, const void* k_cache, const void
 /* Bytes of the fixed scratch array used by spec_verify_attention_noalloc. */
 size_t spec_verify_attention_noalloc_limit(void);
 
+/*
+ * Which kernel spec_verify_attention (and its allocation-free form) launches
+ * for `d` and `k_draft` on the current device, with the tile settings it is
+ * built with (a convenience of this library, for callers that report
+ * per-kernel figures). The choice follows the rule stated above
+ * spec_verify_attention, SPEC_ATTN_KERNEL included.
+ *
+ *  plan   written on SPEC_OK; host memory owned by the caller.
+ *
+ * Returns SPEC_ERR_INVALID_ARG for an invalid descriptor or a null plan,
+ * SPEC_ERR_UNSUPPORTED for a shape spec_verify_attention rejects the same way,
+ * and SPEC_ERR_LAUNCH when a device query it needs fails (D = 128 with 17 or
+ * more packed rows reads the current device's shared-memory limit; other
+ * shapes need no device). Launches nothing and touches no device memory.
+ */
+#define SPEC_ATTN_KERNEL_MMA 1 /* mma.sync m16n8k16 tiles                    */
+#define SPEC_ATTN_KERNEL_TC 2  /* tcgen05 MMAs, accumulators in tensor memory */
+
+typedef struct spec_attn_plan {
+  int32_t kernel;        /* SPEC_ATTN_KERNEL_*                                   */
+  int32_t m_tiles;       /* (k_draft+1)*G packed rows padded to 16*m_tiles: 1, 2, 4 */
+  int32_t keys_per_tile; /* keys per K/V pipeline stage                          */
+  int32_t stages;        /* K/V pipeline stages in shared memory                 */
+  int32_t p_buffers;     /* tcgen05: shared-memory buffers of P; 0 for mma.sync  */
+  int32_t ctas_per_sm;   /* resident CTAs per SM the kernel is compiled for      */
+} spec_attn_plan;
+
+int spec_verify_attention_plan(const spec_attn_desc* d, int32_t k_draft, spec_attn_plan* plan);
+
 /* ------------------------------------------------------------------------ */
 /* 2. Acceptance: greedy prefix match or speculative sampling                  */
 /* ------------------------------------------------------------------------ */

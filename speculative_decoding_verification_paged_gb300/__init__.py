@@ -26,6 +26,7 @@ from . import buildlib as _build_mod
 __all__ = [
     "SpecError", "build", "library_path", "load_library", "spec_verify_attention",
     "spec_verify_attention_workspace", "new_attention_workspace", "spec_verify_attention_noalloc",
+    "spec_verify_attention_plan",
     "spec_accept", "spec_commit_state", "spec_commit_state_aligned", "spec_commit_select", "spec_gdn_verify",
     "spec_gdn_verify_pooled", "status_string",
     "DEVERR", "MODE_GREEDY", "MODE_SAMPLE", "ALIGN_TOKEN", "ALIGN_LAST",
@@ -46,6 +47,14 @@ class SpecError(RuntimeError):
     def __init__(self, fn: str, code: int):
         super().__init__(f"{fn} returned {code} ({status_string(code)})")
         self.code = code
+
+
+class _AttnPlan(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int32) for name in
+                ("kernel", "m_tiles", "keys_per_tile", "stages", "p_buffers", "ctas_per_sm")]
+
+
+_ATTN_KERNELS = {1: "mma", 2: "tc"}
 
 
 class _AttnDesc(ctypes.Structure):
@@ -91,6 +100,8 @@ def load_library():
         lib.spec_verify_attention_noalloc.restype = ctypes.c_int
         lib.spec_verify_attention_noalloc_limit.argtypes = []
         lib.spec_verify_attention_noalloc_limit.restype = sz
+        lib.spec_verify_attention_plan.argtypes = [ctypes.POINTER(_AttnDesc), i32, ctypes.POINTER(_AttnPlan)]
+        lib.spec_verify_attention_plan.restype = ctypes.c_int
         lib.spec_accept.argtypes = [P, P, P, u64, P, P, P, P, i32, i32, i32, P, P]
         lib.spec_accept.restype = ctypes.c_int
         lib.spec_commit_state.argtypes = [P, P, P, i32, i32, i32, i64, P, P]
@@ -172,6 +183,20 @@ def spec_verify_attention_workspace(q: torch.Tensor, k_cache: torch.Tensor, bloc
     """Workspace bytes spec_verify_attention needs for these shapes."""
     d = _attn_desc(q, k_cache, block_table)
     return int(load_library().spec_verify_attention_workspace(ctypes.byref(d), int(k_draft)))
+
+
+def spec_verify_attention_plan(q: torch.Tensor, k_cache: torch.Tensor, block_table: torch.Tensor,
+                               k_draft: int) -> dict:
+    """Which kernel spec_verify_attention launches for these shapes on the current
+    device, and its tile settings. Only the tensors' shapes are read (meta tensors
+    do); D = 128 with 17 or more packed rows queries the current device."""
+    d = _attn_desc(q, k_cache, block_table)
+    plan = _AttnPlan()
+    _check("spec_verify_attention_plan",
+           load_library().spec_verify_attention_plan(ctypes.byref(d), int(k_draft), ctypes.byref(plan)))
+    out = {name: int(getattr(plan, name)) for name, _ in _AttnPlan._fields_}
+    out["kernel"] = _ATTN_KERNELS[out["kernel"]]
+    return out
 
 
 def new_attention_workspace(nbytes: int, device) -> torch.Tensor:

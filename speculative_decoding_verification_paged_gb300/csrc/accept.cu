@@ -33,6 +33,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "launch_memo.h"
 
 namespace specv {
 namespace acc {

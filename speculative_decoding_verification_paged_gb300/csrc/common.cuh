@@ -1,15 +1,13 @@
 // Helpers shared by the verify-step kernels (sm_103a): the device error word,
 // shared-memory addressing, mbarriers, bulk and TMA copies, thread-block
 // cluster and distributed-shared-memory access, mma.sync fragments, tcgen05
-// MMA / tensor-memory / descriptor helpers, Philox4x32-10 and the uniform map,
-// and the host-side per-device launch settings.
+// MMA / tensor-memory / descriptor helpers, Philox4x32-10 and the uniform map.
+// Device code only; the host launch settings are in launch_memo.h.
 #pragma once
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
-
-#include <mutex>
 
 #include "spec_verify.h"
 
@@ -122,37 +120,6 @@ SPEC_DEVICE bool named_sync_or(int id, int count, bool pred) {
 // Hint: pull a byte range into L2 (no completion tracking).
 SPEC_DEVICE void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// --------------------------------------------------------------------------
-// Host: per-device launch settings, shared by every host thread. A launch site
-// keeps one LaunchMemo and reads or updates it under its mutex only; the
-// launch itself happens outside the lock. A kernel's dynamic shared-memory
-// limit is only ever raised, so a concurrent launch never sees it lowered.
-// --------------------------------------------------------------------------
-constexpr int kMaxDevices = 64;
-
-struct LaunchMemo {
-  std::mutex mu;
-  size_t granted[kMaxDevices] = {};    // dynamic shared memory granted so far
-  size_t grid_smem[kMaxDevices] = {};  // shared-memory size `grid` was computed for
-  int grid[kMaxDevices] = {};
-};
-
-// The current device, or -1 when it cannot be read or is out of range.
-static inline int current_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
-  return dev;
-}
-
-// Caller holds m.mu: raise `kern`'s dynamic shared-memory limit on `dev` to `smem`.
-static inline bool grant_smem_locked(LaunchMemo& m, const void* kern, int dev, size_t smem) {
-  if (smem <= m.granted[dev]) return true;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return false;
-  m.granted[dev] = smem;
-  return true;
 }
 
 // --------------------------------------------------------------------------

@@ -43,6 +43,14 @@ int main(void) {
   spec_attn_desc odd = d; /* a valid descriptor this build has no kernel for */
   odd.head_dim = 96;
 
+  /* kernel plan: 16 packed rows at D = 128 run on mma.sync tiles (no device query) */
+  spec_attn_plan plan;
+  memset(&plan, 0, sizeof plan);
+  CHECK(spec_verify_attention_plan(&d, 3, &plan) == SPEC_OK);
+  CHECK(plan.kernel == SPEC_ATTN_KERNEL_MMA && plan.m_tiles == 1 && plan.stages >= 2 && plan.p_buffers == 0);
+  CHECK(spec_verify_attention_plan(&d, 3, NULL) == SPEC_ERR_INVALID_ARG);
+  CHECK(spec_verify_attention_plan(&odd, 3, &plan) == SPEC_ERR_UNSUPPORTED);
+
   /* argument validation returns before anything reaches the device */
   void* fake = (void*)(uintptr_t)256; /* never dereferenced on these paths */
   int32_t dummy = 0;

@@ -50,3 +50,47 @@ def test_commit_and_gdn_bytes_by_hand():
     acts = 2 * 2 * 3 * (2 * 4 + 2 * 4) * 4                       # q, k, v, out per token and head
     gates = 2 * 2 * 3 * 8                                        # g and beta
     assert bench.gdn_verify_bytes(g) == states + acts + gates == 2016
+
+
+def test_recorded_traffic_follows_plan_and_kernel_sources(tmp_path, monkeypatch):
+    """A recorded ncu DRAM figure is reported only for the kernel instance it was
+    captured on and only while that kernel's device sources are unchanged."""
+    import json
+    src = tmp_path / "k.cuh"
+    src.write_text("// kernel v1\n")
+    plan = dict(kernel="mma", m_tiles=1, keys_per_tile=64, stages=3, p_buffers=0, ctas_per_sm=2)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "ATTN_KERNEL_SOURCES", {"mma": ["k.cuh"], "tc": ["other.cuh"]})
+    record = {"w": {"plan": plan, "kernel_sources_sha256": bench.kernel_sources_sha256(["k.cuh"]),
+                    "dram_bytes_per_call": 1234}}
+    traffic = tmp_path / "traffic.json"
+    traffic.write_text(json.dumps(record))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(traffic))
+    assert bench.recorded_traffic("w", plan) == 1234
+    assert bench.recorded_traffic("unrecorded", plan) is None
+    assert bench.recorded_traffic("w", dict(plan, stages=4)) is None       # another instance runs
+    assert bench.recorded_traffic("w", dict(plan, kernel="tc")) is None    # another kernel runs
+    src.write_text("// kernel v2\n")                                      # the kernel changed
+    assert bench.recorded_traffic("w", plan) is None
+
+
+def test_kernel_sources_hash_covers_names_and_bytes(tmp_path, monkeypatch):
+    (tmp_path / "a").write_text("x")
+    (tmp_path / "b").write_text("x")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    ha, hb = bench.kernel_sources_sha256(["a"]), bench.kernel_sources_sha256(["b"])
+    assert ha != hb and len(ha) == 64
+    assert bench.kernel_sources_sha256(["a", "b"]) != bench.kernel_sources_sha256(["b", "a"])
+
+
+def test_committed_traffic_records_name_their_kernel_sources():
+    """Every committed record lists exactly the device sources bench.py hashes for its kernel."""
+    import json
+    with open(bench.TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    assert rec
+    for name, entry in rec.items():
+        assert entry["kernel_sources"] == bench.ATTN_KERNEL_SOURCES[entry["plan"]["kernel"]], name
+        assert entry["dram_bytes_per_call"] > 0
+        for rel in entry["kernel_sources"]:
+            assert os.path.exists(os.path.join(ROOT, rel)), rel

@@ -160,6 +160,36 @@ def test_attention_default_kernel_choice(sv, oracle_mod, monkeypatch, name):
     assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
 
 
+def _launched_kernel_names(fn):
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    return [e.name for e in prof.events() if "verify_attention" in e.name]
+
+
+@pytest.mark.parametrize("name,kind", [("longctx", "tc"), ("llama8b_eagle3", "mma"), ("hybrid_gdn", "mma")])
+def test_attention_plan_names_the_launched_kernel(sv, monkeypatch, name, kind):
+    """spec_verify_attention_plan reports the kernel instance the call launches
+    (read back from the profiler's kernel names, demangled or not)."""
+    monkeypatch.delenv("SPEC_ATTN_KERNEL", raising=False)
+    w = wl.WORKLOADS[name].replace(batch=3, ctx_lens=(129, 3000, 9), ctx_range=None)
+    a = wl.make_attention_inputs(w, device=DEV)
+    plan = sv.spec_verify_attention_plan(a["q"], a["k_cache"], a["block_table"], w.k_draft)
+    assert plan["kernel"] == kind
+    names = _launched_kernel_names(lambda: run_attention(sv, a, w))
+    assert len(names) == 1, names
+    if kind == "tc":
+        args = (plan["m_tiles"], plan["stages"], plan["p_buffers"])
+        demangled, mangled = "verify_attention_tc_kernel<%d, %d, %d>" % args, "verify_attention_tc_kernelILi%dELi%dELi%dE" % args
+        assert plan["keys_per_tile"] == 128 and plan["ctas_per_sm"] == 1
+    else:
+        args = (w.head_dim, plan["m_tiles"])
+        demangled, mangled = "verify_attention_kernel<%d, %d>" % args, "verify_attention_kernelILi%dELi%dE" % args
+        assert plan["p_buffers"] == 0
+    assert demangled in names[0] or mangled in names[0], (names[0], plan)
+
+
 def _random_shape(rng):
     D = int(rng.choice([64, 128, 256]))
     bs = int(rng.choice([16, 32, 64, 128]))

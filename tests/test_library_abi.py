@@ -78,6 +78,40 @@ def test_attention_host_validation(lib):
     assert call(_desc(batch=0)) == 0
 
 
+def _plan(lib, kd=3, **kw):
+    import speculative_decoding_verification_paged_gb300 as sv
+    plan = sv._AttnPlan()
+    rc = lib.spec_verify_attention_plan(ctypes.byref(_desc(**kw)), kd, ctypes.byref(plan))
+    return rc, {name: getattr(plan, name) for name, _ in sv._AttnPlan._fields_}
+
+
+def test_attention_plan_without_a_device(lib, monkeypatch):
+    """Plans that need no device query: the mma.sync instances, whose tile settings
+    follow from the shared-memory arithmetic of their configuration (16 rows at
+    D = 128: 64-key stages of 32 KB, three stages, two CTAs per SM; 32 rows at
+    D = 256: 32-key stages, one CTA per SM, so a fourth stage)."""
+    monkeypatch.delenv("SPEC_ATTN_KERNEL", raising=False)
+    rc, p = _plan(lib, num_q_heads=32, num_kv_heads=8)  # (3+1) * 4 = 16 rows
+    assert rc == 0
+    assert p == dict(kernel=1, m_tiles=1, keys_per_tile=64, stages=3, p_buffers=0, ctas_per_sm=2)
+    rc, p = _plan(lib, num_q_heads=24, num_kv_heads=4, head_dim=256)  # 24 rows
+    assert rc == 0
+    assert p == dict(kernel=1, m_tiles=2, keys_per_tile=32, stages=4, p_buffers=0, ctas_per_sm=1)
+    rc, p = _plan(lib, num_q_heads=4, num_kv_heads=1, head_dim=64)
+    assert rc == 0 and p["kernel"] == 1 and p["m_tiles"] == 1 and p["keys_per_tile"] == 64
+    # D = 128 with 17+ rows asks the device for its shared-memory limit: no device here
+    assert _plan(lib, kd=7, num_q_heads=64, num_kv_heads=8)[0] == -3
+    monkeypatch.setenv("SPEC_ATTN_KERNEL", "mma")
+    rc, p = _plan(lib, kd=7, num_q_heads=64, num_kv_heads=8)  # 64 rows, forced onto mma.sync
+    assert rc == 0 and p["kernel"] == 1 and p["m_tiles"] == 4
+    monkeypatch.delenv("SPEC_ATTN_KERNEL")
+    assert lib.spec_verify_attention_plan(ctypes.byref(_desc()), 3, None) == -1
+    assert _plan(lib, num_q_heads=7)[0] == -1
+    assert _plan(lib, kd=0)[0] == -1
+    assert _plan(lib, head_dim=96)[0] == -2
+    assert _plan(lib, num_q_heads=36, num_kv_heads=2)[0] == -2
+
+
 def test_accept_and_commit_host_validation(lib):
     fake = ctypes.c_void_p(256)
     acc = lambda B=2, k=3, V=100, logits=fake: lib.spec_accept(logits, fake, fake, 1, fake, fake, fake, fake,
@@ -150,5 +184,6 @@ def test_plain_c_program_uses_the_boundary(lib, tmp_path):
                         os.path.join(ROOT, "tests", "c_abi_host_checks.c"), "-L", libdir, "-lspecverify",
                         "-Wl,-rpath," + libdir, "-o", exe], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr[-3000:]
-    run = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    env = {k: v for k, v in os.environ.items() if k != "SPEC_ATTN_KERNEL"}  # the default kernel choice
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=120, env=env)
     assert run.returncode == 0 and run.stdout.strip() == "ok", run.stdout + run.stderr
