@@ -160,34 +160,36 @@ def test_attention_default_kernel_choice(sv, oracle_mod, monkeypatch, name):
     assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
 
 
-def _launched_kernel_names(fn):
-    from torch.profiler import ProfilerActivity, profile
-    with profile(activities=[ProfilerActivity.CUDA]) as prof:
-        fn()
-        torch.cuda.synchronize()
-    return [e.name for e in prof.events() if "verify_attention" in e.name]
-
-
 @pytest.mark.parametrize("name,kind", [("longctx", "tc"), ("llama8b_eagle3", "mma"), ("hybrid_gdn", "mma")])
-def test_attention_plan_names_the_launched_kernel(sv, monkeypatch, name, kind):
-    """spec_verify_attention_plan reports the kernel instance the call launches
-    (read back from the profiler's kernel names, demangled or not)."""
+def test_attention_plan_names_the_kernel_that_runs(sv, monkeypatch, name, kind):
+    """spec_verify_attention_plan names the kernel the call runs. The two head-dim-128
+    kernels round differently, so the default call's output equals, bit for bit,
+    that of the kernel the plan names when SPEC_ATTN_KERNEL forces it, and differs
+    from the other's; head dim 256 has the mma.sync kernel only."""
     monkeypatch.delenv("SPEC_ATTN_KERNEL", raising=False)
     w = wl.WORKLOADS[name].replace(batch=3, ctx_lens=(129, 3000, 9), ctx_range=None)
     a = wl.make_attention_inputs(w, device=DEV)
-    plan = sv.spec_verify_attention_plan(a["q"], a["k_cache"], a["block_table"], w.k_draft)
+    plan_of = lambda: sv.spec_verify_attention_plan(a["q"], a["k_cache"], a["block_table"], w.k_draft)
+    plan = plan_of()
     assert plan["kernel"] == kind
-    names = _launched_kernel_names(lambda: run_attention(sv, a, w))
-    assert len(names) == 1, names
+    assert plan["stages"] >= 2
     if kind == "tc":
-        args = (plan["m_tiles"], plan["stages"], plan["p_buffers"])
-        demangled, mangled = "verify_attention_tc_kernel<%d, %d, %d>" % args, "verify_attention_tc_kernelILi%dELi%dELi%dE" % args
-        assert plan["keys_per_tile"] == 128 and plan["ctas_per_sm"] == 1
+        assert plan["keys_per_tile"] == 128 and plan["p_buffers"] >= 1 and plan["ctas_per_sm"] == 1
     else:
-        args = (w.head_dim, plan["m_tiles"])
-        demangled, mangled = "verify_attention_kernel<%d, %d>" % args, "verify_attention_kernelILi%dELi%dE" % args
         assert plan["p_buffers"] == 0
-    assert demangled in names[0] or mangled in names[0], (names[0], plan)
+    default, err = run_attention(sv, a, w)
+    assert err == 0
+    if w.head_dim != 128:
+        return
+    forced = {}
+    for k in ("tc", "mma"):
+        monkeypatch.setenv("SPEC_ATTN_KERNEL", k)
+        assert plan_of()["kernel"] == k
+        forced[k], err = run_attention(sv, a, w)
+        assert err == 0
+    other = "mma" if kind == "tc" else "tc"
+    assert torch.equal(default, forced[kind])
+    assert not torch.equal(default, forced[other])
 
 
 def _random_shape(rng):
