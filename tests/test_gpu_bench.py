@@ -38,6 +38,9 @@ def test_bench_line_fields(sv, extra):
     assert d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] > 0
     kernels = d["kernels"]
     assert {"attention", "accept", "commit"} <= set(kernels)
+    plan = kernels["attention"]["plan"]  # the kernel instance the attention call ran
+    assert set(plan) == {"kernel", "m_tiles", "keys_per_tile", "stages", "p_buffers", "ctas_per_sm"}
+    assert plan["kernel"] == "mma" and plan["m_tiles"] == 1  # tiny: head dim 64, 16 packed rows
     launches_per_step = 3
     if extra:
         assert kernels["commit"]["kind"] == "select" and "gdn_verify" in kernels
