@@ -23,8 +23,9 @@
  *    lmdeploy PR #3945 review of spec_decode/reject_sampler.py, whose fixture
  *    pads the emitted tokens with -1), i.e. the rule of Leviathan et al. 2023
  *    and Chen et al. 2023: accept a draft d with probability min(1, p(d)/q(d)),
- *    otherwise draw from max(0, p - q) normalised; the draw is a three-level
- *    exponential race (an exact sampler of w / sum(w)).
+ *    otherwise draw from max(0, p - q) normalised; the draw is an exponential
+ *    race (an exact sampler of w / sum(w)) with one uniform per vocabulary
+ *    entry.
  *  - Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
  *    easy as 1, 2, 3", SC'11.
  *  - state commit: the operators publish the recurrent state after every verify
@@ -252,91 +253,39 @@ static void softmax_stats(const float* row, int V, double T, double* mx, double*
 }
 
 /*
- * Three-level exponential race over weights w (length V), an exact sampler
- * of w / sum(w): a group of 8192 consecutive entries is raced by its weight
- * sum, then one of the group's 256 chunks by its sum, then one entry of the
- * chunk by its weight. Chunk c of group g holds the entries
- * 8192 g + 1024 i + 4 c + e (i < 8, e < 4). Each race is argmax of
- * weight / E with E = -ln U and U from a Philox word: groups use word g mod 4
- * of counter (g/4, m, b, 2); chunks word c mod 4 of counter
- * ((256 g + c)/4, m, b, 3); entries word x mod 4 of counter (x/4, m, b, 1).
- * Ties go to the lowest index. *gap receives the smallest relative gap
- * between the two largest keys over the three races (+inf where a race has a
- * single candidate).
+ * Exponential race over the weights w (length V), an exact sampler of
+ * w / sum(w) that needs no normalisation: every entry x with w_x > 0 gets the
+ * key w_x / E_x, E_x = -ln U_x with U_x from word (x mod 4) of Philox counter
+ * (x / 4, m, b, 1), and the entry with the largest key wins (ties go to the
+ * lowest index). Since E_x is exponential with rate 1, w_x / E_x exceeds every
+ * other key with probability w_x / sum(w). *gap receives the relative gap
+ * between the two largest keys (+inf when fewer than two entries have a key).
+ * The four words of one counter serve four consecutive entries, so each
+ * Philox block is computed once.
  */
-#define RACE_GROUP 8192
-#define RACE_CHUNKS 256
-
-static double race_e(uint64_t seed, uint32_t index, int m, int b, uint32_t level) {
-  return -log(oracle_uniform(philox_word(seed, index / 4u, (uint32_t)m, (uint32_t)b, level, (int)(index % 4u))));
-}
-
-/* argmax of weight[i] / e(i) over n candidates; returns the winner, updates *gap */
-static int race_level(const double* weight, int n, uint64_t seed, int m, int b, uint32_t level,
-                      uint32_t index_base, double* gap) {
+static int exponential_race(const double* w, int V, uint64_t seed, int m, int b, double* gap) {
+  const uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
   int best = -1;
   double best_key = -1.0, second_key = -1.0;
-  for (int i = 0; i < n; ++i) {
-    double key = 0.0;
-    if (weight[i] > 0.0) key = weight[i] / race_e(seed, index_base + (uint32_t)i, m, b, level);
-    if (key > best_key) {
-      second_key = best_key;
-      best_key = key;
-      best = i;
-    } else if (key > second_key) {
-      second_key = key;
-    }
-  }
-  if (best_key > 0.0 && second_key > 0.0) {
-    double g = (best_key - second_key) / best_key;
-    if (g < *gap) *gap = g;
-  }
-  return best;
-}
-
-static int exponential_race(const double* w, int V, uint64_t seed, int m, int b, double* gap) {
-  const int n_groups = (V + RACE_GROUP - 1) / RACE_GROUP;
-  double* gw = (double*)calloc((size_t)n_groups, sizeof(double));
-  double cw[RACE_CHUNKS];
-  double ew[32];
-  int ex[32];
-  *gap = INFINITY;
-  if (!gw) return 0;
-  for (int x = 0; x < V; ++x) gw[x / RACE_GROUP] += w[x];
-  const int g = race_level(gw, n_groups, seed, m, b, 2u, 0u, gap);
-  free(gw);
-  for (int c = 0; c < RACE_CHUNKS; ++c) cw[c] = 0.0;
-  for (int x = g * RACE_GROUP; x < V && x < (g + 1) * RACE_GROUP; ++x) cw[((x % RACE_GROUP) % 1024) / 4] += w[x];
-  const int c = race_level(cw, RACE_CHUNKS, seed, m, b, 3u, (uint32_t)(g * RACE_CHUNKS), gap);
-  int n = 0;
-  for (int i = 0; i < 8; ++i)
-    for (int e = 0; e < 4; ++e) {
-      const int x = g * RACE_GROUP + 1024 * i + 4 * c + e;
-      if (x < V) {
-        ew[n] = w[x];
-        ex[n] = x;
-        ++n;
+  for (int x0 = 0; x0 < V; x0 += 4) {
+    const uint32_t ctr[4] = {(uint32_t)(x0 / 4), (uint32_t)m, (uint32_t)b, 1u};
+    uint32_t words[4];
+    oracle_philox4x32_10(ctr, key, words);
+    for (int e = 0; e < 4 && x0 + e < V; ++e) {
+      const int x = x0 + e;
+      if (!(w[x] > 0.0)) continue;
+      const double k = w[x] / -log(oracle_uniform(words[e]));
+      if (k > best_key) {
+        second_key = best_key;
+        best_key = k;
+        best = x;
+      } else if (k > second_key) {
+        second_key = k;
       }
     }
-  /* entries of a chunk are raced with their own counters (x/4, m, b, 1) */
-  int best = -1;
-  double best_key = -1.0, second_key = -1.0;
-  for (int i = 0; i < n; ++i) {
-    double key = 0.0;
-    if (ew[i] > 0.0) key = ew[i] / race_e(seed, (uint32_t)ex[i], m, b, 1u);
-    if (key > best_key) {
-      second_key = best_key;
-      best_key = key;
-      best = i;
-    } else if (key > second_key) {
-      second_key = key;
-    }
   }
-  if (best_key > 0.0 && second_key > 0.0) {
-    double gg = (best_key - second_key) / best_key;
-    if (gg < *gap) *gap = gg;
-  }
-  return ex[best];
+  *gap = (best_key > 0.0 && second_key > 0.0) ? (best_key - second_key) / best_key : INFINITY;
+  return best;
 }
 
 /* Draft probability q_j(x). Without a draft distribution (draft_probs NULL) the
@@ -352,8 +301,8 @@ static double draft_q(const float* Q, const int32_t* d, int j, int V, int x) {
  * temperature [B]. Outputs out_tokens [B,k+1], accept_len [B], and for the
  * parity bookkeeping accept_margin [B] = min over the drafts that were tested
  * of |u - p/q| (+inf for greedy rows or when every q was 0) and race_gap [B] =
- * smallest relative gap between the two largest keys of any race level (+inf
- * for greedy rows).
+ * relative gap between the two largest keys of the race (+inf for greedy
+ * rows).
  * Invalid rows (draft token out of range, sampling temperature not > 0) get
  * out_tokens -1 and accept_len -1; the call then returns an error code but
  * still computes every other row.

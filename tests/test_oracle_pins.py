@@ -368,8 +368,9 @@ def test_sampling_bonus_token_follows_last_target_row(oracle_mod):
     assert _chi2_ok(tok[:, k], _softmax(lk.astype(np.float64))) > 1e-3
 
 
-def test_race_across_groups_and_chunks_follows_target(oracle_mod):
-    """The bonus token follows p_k when its mass spans several 8192-entry groups and chunks."""
+def test_race_with_mass_spread_over_the_vocabulary_follows_target(oracle_mod):
+    """The bonus token follows p_k when its mass sits on a few entries far apart in the
+    vocabulary (both ends, and both sides of multiples of 4, 1024 and 8192)."""
     B, k, V = 20000, 1, 20000
     support = np.array([5, 4100, 8191, 8192, 12000, 19999])
     lk = np.full(V, -1e30, np.float32)
@@ -471,45 +472,55 @@ def test_sampling_uniform_uses_documented_counter(oracle_mod):
         assert (alen[b] >= 1) == (u0 < 0.5)
 
 
-@pytest.mark.parametrize("V", [16, 20000])
-def test_final_draw_follows_documented_three_level_race(oracle_mod, V):
-    """With every draft accepted (q = p) the bonus token comes from the documented race:
-    8192-entry groups raced by their sums (Philox counter (g/4, k, b, 2)), then the group's
-    256 chunks {8192g + 1024i + 4c + e} by their sums (counter ((256g+c)/4, k, b, 3)), then
-    the chunk's entries (counter (x/4, k, b, 1)); keys weight / (-ln U), argmax via numpy."""
+@pytest.mark.parametrize("V", [16, 20001])
+def test_final_draw_follows_documented_race(oracle_mod, V):
+    """With every draft accepted the bonus token comes from the documented race: the
+    entry x with the largest p_k(x) / E_x, E_x = -ln U of word x mod 4 of Philox counter
+    (x/4, k, b, 1); replayed here with the library-pinned Philox and numpy's argmax."""
     rng = np.random.default_rng(14)
     B, k = 24, 2
     seed = 777
     L = np.zeros((B, k + 1, V), np.float32)
     L[:, k] = rng.normal(0, 1.5, (B, V)).astype(np.float32)
-    Q = np.full((B, k, V), 1.0 / V, np.float32)
-    L[:, :k] = 0.0
     d = rng.integers(0, V, (B, k)).astype(np.int32)
-    if V & (V - 1):  # q = 1/V exactly only for powers of two: accept by construction instead
-        Q[:] = 0.0
-        Q[np.arange(B)[:, None], np.arange(k)[None, :], d] = 1e-30
+    Q = np.zeros((B, k, V), np.float32)
+    Q[np.arange(B)[:, None], np.arange(k)[None, :], d] = 1e-30  # u q < p always: every draft is kept
     tok, alen, _, gap, _ = oracle_mod.accept(L, d, Q, seed, np.ones(B, np.int32), np.ones(B, np.float32))
     assert np.all(alen == k)
     key = [seed & 0xFFFFFFFF, seed >> 32]
-
-    def e_of(index, level, b):
-        w = oracle_mod.philox4x32_10([index // 4, k, b, level], key)[index % 4]
-        return -np.log(oracle_mod.uniform(int(w)))
-
-    x_all = np.arange(V)
-    chunk = ((x_all % 8192) % 1024) // 4
     for b in range(B):
         if gap[b] < 1e-9:
             continue
+        words = np.array([oracle_mod.philox4x32_10([c, k, b, 1], key) for c in range((V + 3) // 4)],
+                         np.uint64).reshape(-1)[:V]
+        u = ((words >> np.uint64(9)).astype(np.float64) + 0.5) / 8388608.0
         p = _softmax(L[b, k].astype(np.float64))
-        groups = [p[g * 8192:(g + 1) * 8192].sum() for g in range((V + 8191) // 8192)]
-        g = int(np.argmax([w / e_of(i, 2, b) for i, w in enumerate(groups)]))
-        in_g = (x_all // 8192) == g
-        sums = np.array([p[in_g & (chunk == c)].sum() for c in range(256)])
-        c = int(np.argmax([w / e_of(256 * g + i, 3, b) if w > 0 else 0.0 for i, w in enumerate(sums)]))
-        xs = x_all[in_g & (chunk == c)]
-        want = int(xs[np.argmax([p[x] / e_of(int(x), 1, b) for x in xs])])
-        assert tok[b, k] == want
+        assert tok[b, k] == int(np.argmax(p / -np.log(u)))
+
+
+def test_race_uses_the_rejected_position_counters(oracle_mod):
+    """A rejection at position m races with counters (x/4, m, b, 1): a one-hot draft
+    rejected at m = 1 draws from p_1 with the draft removed, keyed on m = 1, not 0."""
+    rng = np.random.default_rng(17)
+    B, k, V = 16, 2, 64
+    seed = 4321
+    L = np.zeros((B, k + 1, V), np.float32)
+    L[:, 1] = rng.normal(0, 1.0, (B, V)).astype(np.float32)
+    d = np.zeros((B, k), np.int32)
+    d[:, 1] = 5
+    L[:, 1, 5] = -1e30  # p_1(5) = 0: draft 1 is always rejected
+    Q = np.zeros((B, k, V), np.float32)
+    Q[:, 0, 0] = 1e-30  # draft 0 is always kept
+    Q[:, 1, 5] = 1.0
+    tok, alen, _, gap, _ = oracle_mod.accept(L, d, Q, seed, np.ones(B, np.int32), np.ones(B, np.float32))
+    assert np.all(alen == 1)
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    for b in range(B):
+        words = np.array([oracle_mod.philox4x32_10([c, 1, b, 1], key) for c in range(V // 4)],
+                         np.uint64).reshape(-1)
+        u = ((words >> np.uint64(9)).astype(np.float64) + 0.5) / 8388608.0
+        w = np.maximum(_softmax(L[b, 1].astype(np.float64)) - Q[b, 1].astype(np.float64), 0.0)
+        assert tok[b, 1] == int(np.argmax(np.where(w > 0, w / -np.log(u), -1.0)))
 
 
 def test_sampling_is_deterministic_per_seed(oracle_mod):
