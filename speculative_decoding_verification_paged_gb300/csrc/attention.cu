@@ -130,65 +130,72 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t D, uint64_t he
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int MT>
-static int launch_main(const Params& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       cudaStream_t stream) {
-  auto kern = verify_attention_kernel<D, MT>;
-  const size_t smem = smem_bytes<D, MT>(p.batch);
-  static LaunchMemo memo;
+// Launch settings of one kernel instance on the current device: raises its
+// dynamic shared-memory limit to `smem` (never lowers it) and works out the
+// persistent grid, once per (device, shared-memory size), under the instance's
+// lock. Every launch of the instance, with or without a caller workspace, takes
+// its grid from here, so no call can lower the limit another one relies on.
+struct Settings {
+  int grid = 0;
+  size_t smem = 0;
+};
+
+template <typename Kern>
+static int settings_for(LaunchMemo& memo, Kern kern, size_t smem, int threads, bool one_per_sm, Settings* st) {
   const int dev = current_device();
   if (dev < 0) return SPEC_ERR_LAUNCH;
-  int grid = 0;
-  {
-    std::lock_guard<std::mutex> lock(memo.mu);
-    if (memo.grid_smem[dev] != smem) {
-      if (!grant_smem_locked(memo, (const void*)kern, dev, smem)) return SPEC_ERR_LAUNCH;
-      int sms = 0, per_sm = 0;
-      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
-        return SPEC_ERR_LAUNCH;
-      if (per_sm < 1) return SPEC_ERR_UNSUPPORTED;
-      memo.grid[dev] = sms * per_sm > kMaxGrid ? kMaxGrid : sms * per_sm;
-      memo.grid_smem[dev] = smem;
-    }
-    grid = memo.grid[dev];
+  std::lock_guard<std::mutex> lock(memo.mu);
+  if (!grant_smem_locked(memo, (const void*)kern, dev, smem)) return SPEC_ERR_LAUNCH;
+  if (memo.grid_smem[dev] != smem) {
+    int sms = 0, per_sm = 1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
+    if (!one_per_sm && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess)
+      return SPEC_ERR_LAUNCH;
+    if (per_sm < 1) return SPEC_ERR_UNSUPPORTED;
+    memo.grid[dev] = sms * per_sm > kMaxGrid ? kMaxGrid : sms * per_sm;
+    memo.grid_smem[dev] = smem;
   }
-  kern<<<grid, kThreads, smem, stream>>>(p, tq, tk, tv);
+  st->grid = memo.grid[dev];
+  st->smem = smem;
+  return SPEC_OK;
+}
+
+template <int D, int MT>
+static LaunchMemo& memo_main() {
+  static LaunchMemo memo;
+  return memo;
+}
+
+template <int MT, int S, int NP>
+static LaunchMemo& memo_tc() {
+  static LaunchMemo memo;
+  return memo;
+}
+
+template <int D, int MT>
+static int settings_main(int batch, Settings* st) {
+  return settings_for(memo_main<D, MT>(), verify_attention_kernel<D, MT>, smem_bytes<D, MT>(batch), kThreads,
+                      false, st);
+}
+
+// The tcgen05 kernel runs one CTA per SM.
+template <int MT, int S, int NP>
+static int settings_tc(int batch, Settings* st) {
+  return settings_for(memo_tc<MT, S, NP>(), tc::verify_attention_tc_kernel<MT, S, NP>,
+                      tc::smem_bytes<MT, S, NP>(batch), tc::kThreads, true, st);
+}
+
+template <int D, int MT>
+static int launch_main(const Params& p, const Settings& st, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, cudaStream_t stream) {
+  verify_attention_kernel<D, MT><<<st.grid, kThreads, st.smem, stream>>>(p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
-template <int D>
-static int launch_main_d(const Params& p, int mt, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, cudaStream_t stream) {
-  switch (mt) {
-    case 1: return launch_main<D, 1>(p, tq, tk, tv, stream);
-    case 2: return launch_main<D, 2>(p, tq, tk, tv, stream);
-    default: return launch_main<D, 4>(p, tq, tk, tv, stream);
-  }
-}
-
-// The tcgen05 kernel: one CTA per SM (its grid never exceeds the mma.sync kernel's).
 template <int MT, int S, int NP>
-static int launch_tc(const Params& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     cudaStream_t stream) {
-  auto kern = tc::verify_attention_tc_kernel<MT, S, NP>;
-  const size_t smem = tc::smem_bytes<MT, S, NP>(p.batch);
-  static LaunchMemo memo;
-  const int dev = current_device();
-  if (dev < 0) return SPEC_ERR_LAUNCH;
-  int grid = 0;
-  {
-    std::lock_guard<std::mutex> lock(memo.mu);
-    if (memo.grid_smem[dev] != smem) {
-      if (!grant_smem_locked(memo, (const void*)kern, dev, smem)) return SPEC_ERR_LAUNCH;
-      int sms = 0;
-      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-      memo.grid[dev] = sms > kMaxGrid ? kMaxGrid : sms;
-      memo.grid_smem[dev] = smem;
-    }
-    grid = memo.grid[dev];
-  }
-  kern<<<grid, tc::kThreads, smem, stream>>>(p, tq, tk, tv);
+static int launch_tc(const Params& p, const Settings& st, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, cudaStream_t stream) {
+  tc::verify_attention_tc_kernel<MT, S, NP><<<st.grid, tc::kThreads, st.smem, stream>>>(p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
@@ -254,14 +261,57 @@ static void plan_mma_d(int mt, spec_attn_plan* pl) {
   }
 }
 
-// Builds the tensor maps for the chosen kernel's key tile and launches it.
-static int dispatch(const Params& p, int D, int bs, const void* q, const void* k_cache, const void* v_cache,
-                    int64_t num_blocks, cudaStream_t stream) {
-  const int R = p.rows_per_seq, G = p.gqa;
-  const int mt = m_tiles(R * G);
+template <int D>
+static int settings_main_d(int mt, int batch, Settings* st) {
+  switch (mt) {
+    case 1: return settings_main<D, 1>(batch, st);
+    case 2: return settings_main<D, 2>(batch, st);
+    default: return settings_main<D, 4>(batch, st);
+  }
+}
+
+template <int D>
+static int launch_main_d(const Params& p, int mt, const Settings& st, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, cudaStream_t stream) {
+  switch (mt) {
+    case 1: return launch_main<D, 1>(p, st, tq, tk, tv, stream);
+    case 2: return launch_main<D, 2>(p, st, tq, tk, tv, stream);
+    default: return launch_main<D, 4>(p, st, tq, tk, tv, stream);
+  }
+}
+
+// The kernel a call runs and its launch settings (grid, shared memory) on the
+// current device. Both entry points call this before they lay out their
+// scratch, so the allocation-free one sizes its partial slots by the grid of
+// the kernel that is actually launched.
+struct Prepared {
   Choice ch;
-  const int rc = choose_kernel(D, mt, p.batch, &ch);
+  Settings st;
+  int mt = 1;
+};
+
+static int prepare(int D, int rows, int batch, Prepared* pr) {
+  pr->mt = m_tiles(rows);
+  const int rc = choose_kernel(D, pr->mt, batch, &pr->ch);
   if (rc != SPEC_OK) return rc;
+  if (pr->ch.kind == Kernel::kTc) {
+    if (pr->mt == 1) return pr->ch.stages == 3 ? settings_tc<1, 3, 2>(batch, &pr->st)
+                                              : settings_tc<1, 2, 2>(batch, &pr->st);
+    if (pr->mt == 2) return settings_tc<2, 2, 2>(batch, &pr->st);
+    return settings_tc<4, 2, 1>(batch, &pr->st);
+  }
+  switch (D) {
+    case 64: return settings_main_d<64>(pr->mt, batch, &pr->st);
+    case 128: return settings_main_d<128>(pr->mt, batch, &pr->st);
+    default: return settings_main_d<256>(pr->mt, batch, &pr->st);
+  }
+}
+
+// Builds the tensor maps for the prepared kernel's key tile and launches it.
+static int dispatch(const Params& p, const Prepared& pr, int D, int bs, const void* q, const void* k_cache,
+                    const void* v_cache, int64_t num_blocks, cudaStream_t stream) {
+  const int R = p.rows_per_seq, G = p.gqa, mt = pr.mt;
+  const Choice& ch = pr.ch;
   const int tk = ch.kind == Kernel::kTc ? tc::TK : tile_keys(D, mt);
   CUtensorMap tq, tk_map, tv_map;
   if (!make_map(&tq, q, D, p.num_q_heads, (uint64_t)p.batch * R, (uint32_t)G, (uint32_t)R) ||
@@ -269,15 +319,15 @@ static int dispatch(const Params& p, int D, int bs, const void* q, const void* k
       !make_map(&tv_map, v_cache, D, p.num_kv_heads, (uint64_t)num_blocks * bs, 1, (uint32_t)(bs < tk ? bs : tk)))
     return SPEC_ERR_LAUNCH;
   if (ch.kind == Kernel::kTc) {
-    if (mt == 1) return ch.stages == 3 ? launch_tc<1, 3, 2>(p, tq, tk_map, tv_map, stream)
-                                    : launch_tc<1, 2, 2>(p, tq, tk_map, tv_map, stream);
-    if (mt == 2) return launch_tc<2, 2, 2>(p, tq, tk_map, tv_map, stream);
-    return launch_tc<4, 2, 1>(p, tq, tk_map, tv_map, stream);
+    if (mt == 1) return ch.stages == 3 ? launch_tc<1, 3, 2>(p, pr.st, tq, tk_map, tv_map, stream)
+                                    : launch_tc<1, 2, 2>(p, pr.st, tq, tk_map, tv_map, stream);
+    if (mt == 2) return launch_tc<2, 2, 2>(p, pr.st, tq, tk_map, tv_map, stream);
+    return launch_tc<4, 2, 1>(p, pr.st, tq, tk_map, tv_map, stream);
   }
   switch (D) {
-    case 64: return launch_main_d<64>(p, mt, tq, tk_map, tv_map, stream);
-    case 128: return launch_main_d<128>(p, mt, tq, tk_map, tv_map, stream);
-    default: return launch_main_d<256>(p, mt, tq, tk_map, tv_map, stream);
+    case 64: return launch_main_d<64>(p, mt, pr.st, tq, tk_map, tv_map, stream);
+    case 128: return launch_main_d<128>(p, mt, pr.st, tq, tk_map, tv_map, stream);
+    default: return launch_main_d<256>(p, mt, pr.st, tq, tk_map, tv_map, stream);
   }
 }
 
@@ -311,33 +361,35 @@ extern "C" int spec_verify_attention_plan(const spec_attn_desc* d, int32_t k_dra
   return SPEC_OK;
 }
 
-extern "C" int spec_verify_attention(const void* q, const void* k_cache, const void* v_cache,
-                                     const int32_t* block_table, const int32_t* ctx_lens, int32_t k_draft,
-                                     float* out, const spec_attn_desc* d, void* workspace,
-                                     size_t workspace_bytes, int32_t* dev_err, spec_stream_t stream_) {
-  if (!attn::desc_ok(d, k_draft)) return SPEC_ERR_INVALID_ARG;
+namespace specv {
+namespace attn {
+
+// Host-side checks shared by both entry points (workspace aside).
+static int check_call(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_table,
+                      const int32_t* ctx_lens, int k_draft, const float* out, const spec_attn_desc* d) {
+  if (!desc_ok(d, k_draft)) return SPEC_ERR_INVALID_ARG;
   if (d->batch == 0) return SPEC_OK;
   if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !out) return SPEC_ERR_INVALID_ARG;
-  if (!attn::shape_supported(d, k_draft)) return SPEC_ERR_UNSUPPORTED;
-  const attn::Layout L = attn::layout_for(d, k_draft);
-  if (workspace == nullptr || workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return SPEC_ERR_INVALID_ARG;
+  if (!shape_supported(d, k_draft)) return SPEC_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
        reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out)) & 15)
     return SPEC_ERR_INVALID_ARG;
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  return SPEC_OK;
+}
 
-  const int R = k_draft + 1, G = d->num_q_heads / d->num_kv_heads, D = d->head_dim;
-  const int bs = d->block_size;
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  attn::Params p;
+// The kernel parameter block for a call whose scratch starts at `ws`
+// (arrival counters at 0, log-sum-exp and partial outputs at the offsets).
+static Params make_params(const int32_t* block_table, const int32_t* ctx_lens, int k_draft, float* out,
+                          const spec_attn_desc* d, uint8_t* ws, size_t lse_off, size_t opart_off,
+                          int32_t* dev_err) {
+  const int R = k_draft + 1, G = d->num_q_heads / d->num_kv_heads;
+  Params p;
   p.block_table = block_table;
   p.ctx_lens = ctx_lens;
   p.out = out;
   p.counters = reinterpret_cast<int32_t*>(ws);
-  p.lse = reinterpret_cast<float*>(ws + L.lse_off);
-  p.opart = reinterpret_cast<float*>(ws + L.opart_off);
+  p.lse = reinterpret_cast<float*>(ws + lse_off);
+  p.opart = reinterpret_cast<float*>(ws + opart_off);
   p.dev_err = dev_err;
   p.num_blocks = d->num_blocks;
   p.batch = d->batch;
@@ -347,11 +399,34 @@ extern "C" int spec_verify_attention(const void* q, const void* k_cache, const v
   p.gqa = G;
   p.n_rows = R * G;
   int shift = 0;
-  while ((1 << shift) < bs) ++shift;
+  while ((1 << shift) < d->block_size) ++shift;
   p.block_shift = shift;
   p.max_blocks = d->max_blocks_per_seq;
-  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
-  return attn::dispatch(p, D, bs, q, k_cache, v_cache, d->num_blocks, stream);
+  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)d->head_dim));
+  return p;
+}
+
+}  // namespace attn
+}  // namespace specv
+
+extern "C" int spec_verify_attention(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, const int32_t* ctx_lens, int32_t k_draft,
+                                     float* out, const spec_attn_desc* d, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_err, spec_stream_t stream_) {
+  if (!attn::desc_ok(d, k_draft)) return SPEC_ERR_INVALID_ARG;
+  if (d->batch == 0) return SPEC_OK;
+  int rc = attn::check_call(q, k_cache, v_cache, block_table, ctx_lens, k_draft, out, d);
+  if (rc != SPEC_OK) return rc;
+  const attn::Layout L = attn::layout_for(d, k_draft);
+  if (workspace == nullptr || workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0) return SPEC_ERR_INVALID_ARG;
+  attn::Prepared pr;
+  rc = attn::prepare(d->head_dim, (k_draft + 1) * (d->num_q_heads / d->num_kv_heads), d->batch, &pr);
+  if (rc != SPEC_OK) return rc;
+  const attn::Params p = attn::make_params(block_table, ctx_lens, k_draft, out, d, static_cast<uint8_t*>(workspace),
+                                           L.lse_off, L.opart_off, dev_err);
+  return attn::dispatch(p, pr, d->head_dim, d->block_size, q, k_cache, v_cache, d->num_blocks,
+                        reinterpret_cast<cudaStream_t>(stream_));
 }
 
 // ---------------------------------------------------------------------------
@@ -372,33 +447,6 @@ constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Largest persistent grid a launch can use: the mma.sync kernel's occupancy (the
-// tcgen05 kernel runs one CTA per SM, never more CTAs than this).
-template <int D, int MT>
-static int noalloc_grid(int batch, int* grid) {
-  auto kern = verify_attention_kernel<D, MT>;
-  const size_t smem = smem_bytes<D, MT>(batch);
-  int dev = 0, sms = 0, per_sm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return SPEC_ERR_LAUNCH;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SPEC_ERR_LAUNCH;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
-    return SPEC_ERR_LAUNCH;
-  if (per_sm < 1) return SPEC_ERR_UNSUPPORTED;
-  *grid = sms * per_sm > kMaxGrid ? kMaxGrid : sms * per_sm;
-  return SPEC_OK;
-}
-
-template <int D>
-static int noalloc_grid_d(int mt, int batch, int* grid) {
-  switch (mt) {
-    case 1: return noalloc_grid<D, 1>(batch, grid);
-    case 2: return noalloc_grid<D, 2>(batch, grid);
-    default: return noalloc_grid<D, 4>(batch, grid);
-  }
-}
-
 }  // namespace attn
 }  // namespace specv
 
@@ -410,12 +458,23 @@ extern "C" int spec_verify_attention_noalloc(const void* q, const void* k_cache,
                                              spec_stream_t stream_) {
   if (!attn::desc_ok(d, k_draft)) return SPEC_ERR_INVALID_ARG;
   if (d->batch == 0) return SPEC_OK;
-  if (!q || !k_cache || !v_cache || !block_table || !ctx_lens || !out) return SPEC_ERR_INVALID_ARG;
-  if (!attn::shape_supported(d, k_draft)) return SPEC_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
-       reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out)) & 15)
-    return SPEC_ERR_INVALID_ARG;
+  int rc = attn::check_call(q, k_cache, v_cache, block_table, ctx_lens, k_draft, out, d);
+  if (rc != SPEC_OK) return rc;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+  // Scratch this shape needs at most: arrival counters, then two partial slots
+  // per CTA of the largest persistent grid. A shape that cannot fit even then
+  // is rejected before any device call.
+  const int64_t n_rows = (int64_t)(k_draft + 1) * (d->num_q_heads / d->num_kv_heads);
+  const size_t counters_bytes = attn::align256((size_t)d->batch * d->num_kv_heads * 4);
+  auto scratch_total = [&](int64_t grid, size_t* lse_off, size_t* opart_off) {
+    const int64_t slots = 2 * grid;
+    *lse_off = counters_bytes;
+    *opart_off = *lse_off + attn::align256((size_t)(slots * n_rows * 4));
+    return *opart_off + attn::align256((size_t)(slots * n_rows * d->head_dim * 4));
+  };
+  size_t lse_off = 0, opart_off = 0;
+  if (scratch_total(1, &lse_off, &opart_off) > attn::kNoAllocScratchBytes) return SPEC_ERR_SCRATCH_LIMIT;
 
   // Set-up, once per device, with that device current: the device address of
   // the scratch array (host code cannot use the symbol itself).
@@ -435,48 +494,16 @@ extern "C" int spec_verify_attention_noalloc(const void* q, const void* k_cache,
     scratch = scratch_addr[dev];
   }
 
-  const int R = k_draft + 1, G = d->num_q_heads / d->num_kv_heads, D = d->head_dim;
-  const int bs = d->block_size;
-  const int mt = attn::m_tiles(R * G);
-  int grid = 0, rc = SPEC_OK;
-  switch (D) {
-    case 64: rc = attn::noalloc_grid_d<64>(mt, d->batch, &grid); break;
-    case 128: rc = attn::noalloc_grid_d<128>(mt, d->batch, &grid); break;
-    default: rc = attn::noalloc_grid_d<256>(mt, d->batch, &grid); break;
-  }
+  // The kernel this call launches and its grid, from the same per-instance
+  // settings the workspace form uses; the partial slots follow that grid.
+  attn::Prepared pr;
+  rc = attn::prepare(d->head_dim, (int)n_rows, d->batch, &pr);
   if (rc != SPEC_OK) return rc;
-  // Scratch layout for this grid: arrival counters, then two partial slots per CTA.
-  const int64_t n_rows = (int64_t)R * G;
-  const int64_t slots = 2 * (int64_t)grid;
-  const size_t counters_bytes = attn::align256((size_t)d->batch * d->num_kv_heads * 4);
-  const size_t lse_off = counters_bytes;
-  const size_t opart_off = lse_off + attn::align256((size_t)(slots * n_rows * 4));
-  const size_t total = opart_off + attn::align256((size_t)(slots * n_rows * D * 4));
-  if (total > attn::kNoAllocScratchBytes) return SPEC_ERR_SCRATCH_LIMIT;
+  if (scratch_total(pr.st.grid, &lse_off, &opart_off) > attn::kNoAllocScratchBytes) return SPEC_ERR_SCRATCH_LIMIT;
 
   uint8_t* ws = static_cast<uint8_t*>(scratch);
   // The counters must start at zero; every call shares the array, so clear them here.
   if (cudaMemsetAsync(ws, 0, counters_bytes, stream) != cudaSuccess) return SPEC_ERR_LAUNCH;
-
-  attn::Params p;
-  p.block_table = block_table;
-  p.ctx_lens = ctx_lens;
-  p.out = out;
-  p.counters = reinterpret_cast<int32_t*>(ws);
-  p.lse = reinterpret_cast<float*>(ws + lse_off);
-  p.opart = reinterpret_cast<float*>(ws + opart_off);
-  p.dev_err = dev_err;
-  p.num_blocks = d->num_blocks;
-  p.batch = d->batch;
-  p.rows_per_seq = R;
-  p.num_q_heads = d->num_q_heads;
-  p.num_kv_heads = d->num_kv_heads;
-  p.gqa = G;
-  p.n_rows = R * G;
-  int shift = 0;
-  while ((1 << shift) < bs) ++shift;
-  p.block_shift = shift;
-  p.max_blocks = d->max_blocks_per_seq;
-  p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)D));
-  return attn::dispatch(p, D, bs, q, k_cache, v_cache, d->num_blocks, stream);
+  const attn::Params p = attn::make_params(block_table, ctx_lens, k_draft, out, d, ws, lse_off, opart_off, dev_err);
+  return attn::dispatch(p, pr, d->head_dim, d->block_size, q, k_cache, v_cache, d->num_blocks, stream);
 }

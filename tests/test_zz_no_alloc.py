@@ -4,9 +4,11 @@ Some callers may not allocate device memory when they call the library (an
 engine's per-step enqueue path, a runtime plugin whose enqueue contract
 forbids allocation, a process that reserved all device memory up front).
 For them the library keeps its attention scratch in a fixed array and offers
-this entry point without a workspace argument. The test calls it through the
+this entry point without a workspace argument. The tests call it through the
 C ABI twice in a row (the second call reuses the array the first left behind)
-and checks both results against the workspace form of the same call.
+and require both results to equal, bit for bit, the workspace form of the same
+call (same kernel, same grid, same split plan), and the oracle within the
+attention tolerance.
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test; it also passes on its own in a fresh process.
@@ -14,10 +16,11 @@ run every other test; it also passes on its own in a fresh process.
 
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
-from helpers import ATTN_MAX_ABS, ATTN_REL_L2, attention_errors
+from helpers import ATTN_MAX_ABS, ATTN_REL_L2, attention_errors, oracle_attention_for
 from speculative_decoding_verification_paged_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -34,13 +37,23 @@ def _call_noalloc(sv, lib, a, w, out, err):
         ctypes.c_void_p(err.data_ptr()), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-@pytest.mark.parametrize("name", ["llama8b_eagle3", "tiny"])
-def test_noalloc_matches_workspace_call_twice(sv, name):
+def _ragged(name):
+    """Ragged context mixes, so that units split across CTAs and partial slots are used."""
+    w = wl.WORKLOADS[name]
+    if name == "llama8b_eagle3":  # mma.sync, 16 packed rows
+        return w.replace(batch=12, ctx_lens=(2048, 17, 4, 700, 64, 65, 1999, 2048, 130, 5, 1024, 333))
+    if name == "hybrid_gdn":  # D = 256, 24 packed rows: the largest partial slots per CTA
+        return w.replace(batch=6, ctx_lens=(4100, 4, 1500, 63, 2049, 777), ctx_range=None)
+    if name == "longctx":  # D = 128 with 64 packed rows: the tcgen05 kernel
+        return w.replace(batch=2, ctx_lens=(3000, 700), ctx_range=None)
+    return w
+
+
+@pytest.mark.parametrize("name", ["llama8b_eagle3", "tiny", "hybrid_gdn", "longctx"])
+def test_noalloc_matches_workspace_call_twice(sv, oracle_mod, name):
     lib = sv.load_library()
     assert lib.spec_verify_attention_noalloc_limit() == 32 << 20
-    w = wl.WORKLOADS[name]
-    if name == "llama8b_eagle3":  # ragged lengths so that units split across CTAs
-        w = w.replace(batch=12, ctx_lens=(2048, 17, 4, 700, 64, 65, 1999, 2048, 130, 5, 1024, 333))
+    w = _ragged(name)
     a = wl.make_attention_inputs(w, device=DEV)
     shape = (w.batch, w.rows, w.num_q_heads, w.head_dim)
     ref = torch.empty(shape, dtype=torch.float32, device=DEV)
@@ -56,8 +69,34 @@ def test_noalloc_matches_workspace_call_twice(sv, name):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     for out in outs:
-        mx, rel = attention_errors(out.cpu().numpy(), ref.cpu().double().numpy())
+        assert torch.equal(out, ref)
+    want = oracle_attention_for(oracle_mod, a)
+    mx, rel = attention_errors(outs[1].cpu().numpy(), want)
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+
+
+@pytest.mark.parametrize("name", ["llama8b_eagle3", "longctx"])
+def test_noalloc_small_batch_then_workspace_large_batch(sv, oracle_mod, name):
+    """A small allocation-free call, then a larger workspace call of the same kernel
+    instance: the first must not leave the kernel's shared-memory limit below what
+    the second needs."""
+    lib = sv.load_library()
+    big = _ragged(name)
+    small = big.replace(batch=1, ctx_lens=big.ctx_lens[:1])
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    a_s = wl.make_attention_inputs(small, device=DEV)
+    out_s = torch.empty((small.batch, small.rows, small.num_q_heads, small.head_dim), device=DEV)
+    assert _call_noalloc(sv, lib, a_s, small, out_s, err) == 0
+    a_b = wl.make_attention_inputs(big, device=DEV, seed=big.seed + 5)
+    out_b = torch.empty((big.batch, big.rows, big.num_q_heads, big.head_dim), device=DEV)
+    sv.spec_verify_attention(a_b["q"], a_b["k_cache"], a_b["v_cache"], a_b["block_table"], a_b["ctx_lens"],
+                             big.k_draft, out_b, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for a, out in ((a_s, out_s), (a_b, out_b)):
+        mx, rel = attention_errors(out.cpu().numpy(), oracle_attention_for(oracle_mod, a))
         assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+    assert np.isfinite(out_b.cpu().numpy()).all()
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(sv):
