@@ -33,15 +33,17 @@ from speculative_decoding_verification_paged_gb300 import workloads as wl  # noq
 
 METRIC = "verified tokens/s per verify step (1 GB300); verify-attn & accept HBM GB/s vs peak"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "llama8b_eagle3"
+DEFAULT_WORKLOAD = "hybrid_gdn"
 L2_FLUSH_BYTES = 512 << 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-# The device code of each verify-attention kernel: a recorded ncu traffic figure
-# stays valid while these files hash to the recorded value (host launch code may change).
+# The device code of each kernel: a recorded ncu traffic figure stays valid while
+# these files hash to the recorded value (host launch code may change).
 _CSRC = "speculative_decoding_verification_paged_gb300/csrc/"
-ATTN_KERNEL_SOURCES = {
-    "mma": [_CSRC + "common.cuh", _CSRC + "attention_device.cuh", _CSRC + "attention_mma.cuh"],
-    "tc": [_CSRC + "common.cuh", _CSRC + "attention_device.cuh", _CSRC + "attention_tc.cuh"],
+KERNEL_SOURCES = {
+    "attention/mma": [_CSRC + "common.cuh", _CSRC + "attention_device.cuh", _CSRC + "attention_mma.cuh"],
+    "attention/tc": [_CSRC + "common.cuh", _CSRC + "attention_device.cuh", _CSRC + "attention_tc.cuh"],
+    "accept": [_CSRC + "common.cuh", _CSRC + "accept.cu"],
+    "commit": [_CSRC + "common.cuh", _CSRC + "commit.cu"],
 }
 
 
@@ -274,19 +276,40 @@ def kernel_sources_sha256(paths):
     return h.hexdigest()
 
 
-def recorded_traffic(workload, plan):
-    """DRAM bytes per attention call from an ncu capture, if the capture ran the kernel instance
-    the library plans for this call (`plan`, from spec_verify_attention_plan) and that kernel's
-    device sources are unchanged since."""
+def traffic_key(kernel, plan=None):
+    """The source set a kernel's traffic record is keyed to."""
+    return f"attention/{plan['kernel']}" if kernel == "attention" else kernel
+
+
+def recorded_traffic(kernel, workload, plan=None, units=None):
+    """DRAM bytes per call of `kernel` on `workload` from an ncu capture, if the capture ran the
+    instance the library launches now (attention: the plan spec_verify_attention_plan reports) and
+    the kernel's device sources are unchanged since. A record taken on a smaller case of the same
+    kernel (fewer recurrent-state layers) is scaled to the call by its unit count, since the
+    commit's traffic grows in proportion to the states it moves."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
-        entry = json.load(f).get(workload)
-    if not entry or entry.get("plan") != plan:
+        entry = json.load(f).get(kernel, {}).get(workload)
+    if not entry:
         return None
-    if entry.get("kernel_sources_sha256") != kernel_sources_sha256(ATTN_KERNEL_SOURCES[plan["kernel"]]):
+    if kernel == "attention" and entry.get("plan") != plan:
         return None
+    if entry.get("kernel_sources_sha256") != kernel_sources_sha256(KERNEL_SOURCES[traffic_key(kernel, plan)]):
+        return None
+    per_unit = entry.get("dram_bytes_per_unit")
+    if per_unit is not None:
+        return per_unit * units if units else None
     return entry.get("dram_bytes_per_call")
+
+
+def dominant_traffic(kernel, workload, plan, w, select):
+    """Recorded DRAM bytes per call of the step's dominant kernel, or None."""
+    if kernel == "attention":
+        return recorded_traffic("attention", workload, plan)
+    if kernel == "commit" and not select:
+        return recorded_traffic("commit", workload, units=w.gdn_layers * w.batch)
+    return None
 
 
 # --------------------------------------------------------------------------
@@ -439,10 +462,13 @@ def run_native(args, world, rank, local):
     mb = commit_bytes(w, "select" if select else "copy")
     ta, tc, tm = statistics.mean(t_attn), statistics.mean(t_acc), statistics.mean(t_cmt)
     plan = sv.spec_verify_attention_plan(a["q"], a["k_cache"], a["block_table"], w.k_draft)
+    # every position of every row read (logits, and the draft rows of the sampling rows): the
+    # bytes an acceptance without early exit would move, reported beside the early-exit basis
+    full_read = w.batch * 4 * w.vocab * (R + w.k_draft)
     kernels = {
         "attention": {"ms": ta, "bytes": ab, "GBps": ab / ta / 1e6, "frac": ab / ta / 1e6 / peak, "plan": plan},
         "accept": {"ms": tc, "bytes": cb, "GBps": cb / tc / 1e6, "frac": cb / tc / 1e6 / peak,
-                   "full_read_bytes": w.batch * 4 * w.vocab * (R + w.k_draft)},
+                   "full_read_bytes": full_read, "frac_full_read": full_read / tc / 1e6 / peak},
     }
     if w.gdn_layers:
         kernels["commit"] = {"ms": tm, "bytes": mb, "GBps": mb / tm / 1e6, "frac": mb / tm / 1e6 / peak,
@@ -455,7 +481,7 @@ def run_native(args, world, rank, local):
     dk = kernels[dominant]
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": dk["GBps"], "peak": peak, "unit": "GB/s",
                 "frac": dk["frac"], "peak_source": peak_kind,
-                "traffic": recorded_traffic(args.config, plan) if dominant == "attention" else None,
+                "traffic": dominant_traffic(dominant, args.config, plan, w, select),
                 "same_run_ceilings": live_ceilings(dev)}
 
     e2e = None
@@ -487,10 +513,13 @@ def run_native(args, world, rank, local):
 
 
 def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush, gv=None, gdn_verify=None):
-    """Same metric through the public API with the step's inputs in pinned host memory (the recurrent
-    state, like the model weights, stays resident; the step's activations are copied in)."""
-    names = ["q", "k_cache", "v_cache", "block_table", "ctx_lens"]
-    host = {n: a[n].cpu().pin_memory() for n in names}
+    """Same metric through the public API with the step's inputs in pinned host memory. The
+    serving state stays resident in HBM, as it does in an engine: the paged KV cache, the
+    recurrent state and its checkpoints. The step's activations and scheduling data are copied
+    in every step: q, the block table and context lengths, the target logits, the draft tokens
+    and draft probabilities, per-row mode and temperature (and, with --gdn-verify, the
+    recurrence's q, k, v and gates). The outputs are read back."""
+    host = {n: a[n].cpu().pin_memory() for n in ("q", "block_table", "ctx_lens")}
     for n in ["target_logits", "draft_tokens", "draft_probs", "mode", "temperature"]:
         host[n] = acc_in[n].cpu().pin_memory()
     gdn_host = {}
@@ -508,7 +537,7 @@ def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush
     def step():
         for n, t in host.items():
             devbuf[n].copy_(t, non_blocking=True)
-        sv.spec_verify_attention(devbuf["q"], devbuf["k_cache"], devbuf["v_cache"], devbuf["block_table"],
+        sv.spec_verify_attention(devbuf["q"], a["k_cache"], a["v_cache"], devbuf["block_table"],
                                  devbuf["ctx_lens"], w.k_draft, out, workspace=ws, dev_err=err)
         if gv is not None:
             for n, t in gdn_host.items():  # the step's activations into the buffers the recurrence reads
@@ -542,70 +571,83 @@ def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush
 # --------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 # --------------------------------------------------------------------------
-def oracle_step_estimate(w, mode, budget_s, seed_offset=0, commit="copy", gdn_verify=False):
-    """Time the oracle on a bounded sample of one step; return (s per full step, tokens, sample text, threads)."""
-    import oracle
-    oracle.build()
-    a = wl.make_attention_inputs(w, device="cpu", seed=w.seed + seed_offset)
-    acc_in = wl.make_accept_inputs(w, device="cpu", seed=w.seed + seed_offset, mode=mode)
-    q = a["q"].view(torch.int16).numpy().view(np.uint16)
-    kc = a["k_cache"].view(torch.int16).numpy().view(np.uint16)
-    vc = a["v_cache"].view(torch.int16).numpy().view(np.uint16)
-    table, ctx = a["block_table"].numpy(), a["ctx_lens"].numpy()
-    threads = oracle.max_threads()
-    # attention: whole sequences until the budget is spent, scaled by context length
-    t0 = time.perf_counter()
-    done_ctx, done = 0, 0
-    order = list(range(w.batch))
-    while done < len(order) and time.perf_counter() - t0 < budget_s * 0.7:
-        b = order[done]
-        oracle.verify_attention(q, kc, vc, table, ctx, seqs=np.array([b], np.int32))
-        done_ctx += int(ctx[b])
-        done += 1
-    t_attn_sample = time.perf_counter() - t0
-    t_attn = t_attn_sample * float(ctx.sum()) / max(done_ctx, 1)
-    t1 = time.perf_counter()
-    tok, alen, _, _, _ = oracle.accept(acc_in["target_logits"].numpy(), acc_in["draft_tokens"].numpy(),
-                                       acc_in["draft_probs"].numpy(), acc_in["philox_seed"],
-                                       acc_in["mode"].numpy(), acc_in["temperature"].numpy())
-    t_acc = time.perf_counter() - t1
-    t_cmt = 0.0
-    if w.gdn_layers and commit == "select":
-        live_row, ckpt_rows = (t.numpy() for t in select_tables(w, "cpu"))
-        t2 = time.perf_counter()
-        oracle.commit_select(alen, live_row, ckpt_rows, w.rows, 0)
-        t_cmt = time.perf_counter() - t2
-    elif w.gdn_layers:
-        g = wl.make_gdn_inputs(w.replace(gdn_layers=1), device="cpu", seed=w.seed + seed_offset)
-        live = g["live_state"].numpy()
-        t2 = time.perf_counter()
-        oracle.commit_state(g["snapshots"].numpy(), alen, live)
-        t_cmt = (time.perf_counter() - t2) * w.gdn_layers
-    t_gdn, gdn_rows = 0.0, 0
-    if gdn_verify and w.gdn_layers:  # one layer; a few rows (all heads), scaled to the batch
-        gdn_rows = min(4, w.batch)
-        x = wl.make_gdn_verify_inputs(w.replace(batch=gdn_rows), device="cpu", seed=w.seed + seed_offset)
-        arrays = [x[n][0].numpy() for n in ("q", "k", "v", "g", "beta")]
-        t3 = time.perf_counter()
-        oracle.gdn_verify(*arrays, x["state"][0].numpy(), scale=x["scale"])
-        t_gdn = (time.perf_counter() - t3) * w.batch / gdn_rows
-    tokens = float(np.sum(alen + 1))
-    sample = (f"attention over {done}/{w.batch} sequences ({done_ctx} of {int(ctx.sum())} context tokens, "
-              f"scaled by tokens) + acceptance of all {w.batch} rows"
-              + ((" + zero-copy commit of all layers" if commit == "select" else
-                  f" + commit of 1/{w.gdn_layers} layers (scaled)") if w.gdn_layers else "")
-              + (f" + one gated-delta-net layer over {gdn_rows}/{w.batch} rows (scaled)" if gdn_rows else ""))
-    return t_attn + t_acc + t_cmt + t_gdn, tokens, sample, threads
+class OracleStep:
+    """The CPU oracle over one step of a workload, timed on a bounded sample (inputs drawn once)."""
+
+    def __init__(self, w, mode, seed_offset=0, commit="copy", gdn_verify=False):
+        import oracle
+        oracle.build()
+        self.oracle, self.w, self.commit = oracle, w, commit
+        a = wl.make_attention_inputs(w, device="cpu", seed=w.seed + seed_offset)
+        self.acc_in = wl.make_accept_inputs(w, device="cpu", seed=w.seed + seed_offset, mode=mode)
+        self.q = a["q"].view(torch.int16).numpy().view(np.uint16)
+        self.kc = a["k_cache"].view(torch.int16).numpy().view(np.uint16)
+        self.vc = a["v_cache"].view(torch.int16).numpy().view(np.uint16)
+        self.table, self.ctx = a["block_table"].numpy(), a["ctx_lens"].numpy()
+        self.threads = oracle.max_threads()
+        self.g = None
+        if w.gdn_layers and commit != "select":
+            self.g = wl.make_gdn_inputs(w.replace(gdn_layers=1), device="cpu", seed=w.seed + seed_offset)
+        self.gdn = None
+        if gdn_verify and w.gdn_layers:  # one layer; a few rows (all heads), scaled to the batch
+            rows = min(4, w.batch)
+            x = wl.make_gdn_verify_inputs(w.replace(batch=rows), device="cpu", seed=w.seed + seed_offset)
+            self.gdn = ([x[n][0].numpy() for n in ("q", "k", "v", "g", "beta")], x["state"][0].numpy(),
+                        x["scale"], rows)
+
+    def run(self, budget_s):
+        """Seconds per full step (sampled parts scaled), verified tokens, the sample, threads."""
+        o, w, acc_in = self.oracle, self.w, self.acc_in
+        # attention: whole sequences, a few at a time so that every thread has a (sequence,
+        # kv head) unit, until the budget is spent; scaled by context tokens
+        per_call = max(1, -(-self.threads // w.num_kv_heads))
+        t0 = time.perf_counter()
+        done_ctx, done = 0, 0
+        while done < w.batch and time.perf_counter() - t0 < budget_s * 0.7:
+            seqs = np.arange(done, min(w.batch, done + per_call), dtype=np.int32)
+            o.verify_attention(self.q, self.kc, self.vc, self.table, self.ctx, seqs=seqs)
+            done_ctx += int(self.ctx[seqs].sum())
+            done += len(seqs)
+        t_attn = (time.perf_counter() - t0) * float(self.ctx.sum()) / max(done_ctx, 1)
+        t1 = time.perf_counter()
+        tok, alen, _, _, _ = o.accept(acc_in["target_logits"].numpy(), acc_in["draft_tokens"].numpy(),
+                                      acc_in["draft_probs"].numpy(), acc_in["philox_seed"],
+                                      acc_in["mode"].numpy(), acc_in["temperature"].numpy())
+        t_acc = time.perf_counter() - t1
+        t_cmt = 0.0
+        if w.gdn_layers and self.commit == "select":
+            live_row, ckpt_rows = (t.numpy() for t in select_tables(w, "cpu"))
+            t2 = time.perf_counter()
+            o.commit_select(alen, live_row, ckpt_rows, w.rows, 0)
+            t_cmt = time.perf_counter() - t2
+        elif self.g is not None:
+            live = self.g["live_state"].numpy()
+            t2 = time.perf_counter()
+            o.commit_state(self.g["snapshots"].numpy(), alen, live)
+            t_cmt = (time.perf_counter() - t2) * w.gdn_layers
+        t_gdn, gdn_rows = 0.0, 0
+        if self.gdn is not None:
+            arrays, state, scale, gdn_rows = self.gdn
+            t3 = time.perf_counter()
+            o.gdn_verify(*arrays, state, scale=scale)
+            t_gdn = (time.perf_counter() - t3) * w.batch / gdn_rows
+        tokens = float(np.sum(alen + 1))
+        sample = (f"attention over {done}/{w.batch} sequences ({done_ctx} of {int(self.ctx.sum())} context tokens, "
+                  f"scaled by tokens) + acceptance of all {w.batch} rows"
+                  + ((" + zero-copy commit of all layers" if self.commit == "select" else
+                      f" + commit of 1/{w.gdn_layers} layers (scaled)") if w.gdn_layers else "")
+                  + (f" + one gated-delta-net layer over {gdn_rows}/{w.batch} rows (scaled)" if gdn_rows else ""))
+        return t_attn + t_acc + t_cmt + t_gdn, tokens, sample, self.threads
 
 
 def run_reference(args, world, rank):
     w = workload_for(args)
     mode = args.mode or w.mode
-    per_step_budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step_budget = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    step = OracleStep(w, mode, commit=args.commit, gdn_verify=args.gdn_verify)
     times, tokens, sample, threads = [], 0.0, "", 1
     for i in range(args.warmup + args.steps):
-        s, tokens, sample, threads = oracle_step_estimate(w, mode, per_step_budget, commit=args.commit,
-                                                          gdn_verify=args.gdn_verify)
+        s, tokens, sample, threads = step.run(per_step_budget)
         if i >= args.warmup:
             times.append(s)
     ms = statistics.mean(times) * 1e3
@@ -637,8 +679,8 @@ def main():
             result["cpu_baseline"] = None
         else:
             w = workload_for(args)
-            s, tokens, sample, threads = oracle_step_estimate(w, args.mode or w.mode, args.cpu_seconds,
-                                                              commit=args.commit, gdn_verify=args.gdn_verify)
+            s, tokens, sample, threads = OracleStep(w, args.mode or w.mode, commit=args.commit,
+                                                    gdn_verify=args.gdn_verify).run(args.cpu_seconds)
             result["cpu_baseline"] = {"value": tokens / s, "unit": UNIT, "cores": threads, "kind": "oracle",
                                       "sample": sample}
         print(json.dumps(result), flush=True)

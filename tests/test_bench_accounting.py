@@ -54,24 +54,32 @@ def test_commit_and_gdn_bytes_by_hand():
 
 def test_recorded_traffic_follows_plan_and_kernel_sources(tmp_path, monkeypatch):
     """A recorded ncu DRAM figure is reported only for the kernel instance it was
-    captured on and only while that kernel's device sources are unchanged."""
+    captured on and only while that kernel's device sources are unchanged; a record
+    per unit (a smaller capture of the same kernel) scales by the call's units."""
     import json
     src = tmp_path / "k.cuh"
     src.write_text("// kernel v1\n")
+    (tmp_path / "c.cu").write_text("// commit v1\n")
     plan = dict(kernel="mma", m_tiles=1, keys_per_tile=64, stages=3, p_buffers=0, ctas_per_sm=2)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    monkeypatch.setattr(bench, "ATTN_KERNEL_SOURCES", {"mma": ["k.cuh"], "tc": ["other.cuh"]})
-    record = {"w": {"plan": plan, "kernel_sources_sha256": bench.kernel_sources_sha256(["k.cuh"]),
-                    "dram_bytes_per_call": 1234}}
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", {"attention/mma": ["k.cuh"], "attention/tc": ["other.cuh"],
+                                                  "commit": ["c.cu"]})
+    record = {"attention": {"w": {"plan": plan, "kernel_sources_sha256": bench.kernel_sources_sha256(["k.cuh"]),
+                                  "dram_bytes_per_call": 1234}},
+              "commit": {"w": {"kernel_sources_sha256": bench.kernel_sources_sha256(["c.cu"]),
+                               "dram_bytes_per_unit": 10}}}
     traffic = tmp_path / "traffic.json"
     traffic.write_text(json.dumps(record))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(traffic))
-    assert bench.recorded_traffic("w", plan) == 1234
-    assert bench.recorded_traffic("unrecorded", plan) is None
-    assert bench.recorded_traffic("w", dict(plan, stages=4)) is None       # another instance runs
-    assert bench.recorded_traffic("w", dict(plan, kernel="tc")) is None    # another kernel runs
-    src.write_text("// kernel v2\n")                                      # the kernel changed
-    assert bench.recorded_traffic("w", plan) is None
+    assert bench.recorded_traffic("attention", "w", plan) == 1234
+    assert bench.recorded_traffic("attention", "unrecorded", plan) is None
+    assert bench.recorded_traffic("attention", "w", dict(plan, stages=4)) is None    # another instance runs
+    assert bench.recorded_traffic("attention", "w", dict(plan, kernel="tc")) is None  # another kernel runs
+    assert bench.recorded_traffic("commit", "w", units=7) == 70
+    assert bench.recorded_traffic("accept", "w") is None                               # nothing recorded
+    src.write_text("// kernel v2\n")                                                 # the kernel changed
+    assert bench.recorded_traffic("attention", "w", plan) is None
+    assert bench.recorded_traffic("commit", "w", units=7) == 70
 
 
 def test_kernel_sources_hash_covers_names_and_bytes(tmp_path, monkeypatch):
@@ -89,8 +97,10 @@ def test_committed_traffic_records_name_their_kernel_sources():
     with open(bench.TRAFFIC_FILE) as f:
         rec = json.load(f)
     assert rec
-    for name, entry in rec.items():
-        assert entry["kernel_sources"] == bench.ATTN_KERNEL_SOURCES[entry["plan"]["kernel"]], name
-        assert entry["dram_bytes_per_call"] > 0
-        for rel in entry["kernel_sources"]:
-            assert os.path.exists(os.path.join(ROOT, rel)), rel
+    for kernel, per_workload in rec.items():
+        for name, entry in per_workload.items():
+            key = bench.traffic_key(kernel, entry.get("plan"))
+            assert entry["kernel_sources"] == bench.KERNEL_SOURCES[key], (kernel, name)
+            assert (entry.get("dram_bytes_per_call") or entry.get("dram_bytes_per_unit")) > 0
+            for rel in entry["kernel_sources"]:
+                assert os.path.exists(os.path.join(ROOT, rel)), rel
