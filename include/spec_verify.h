@@ -220,21 +220,16 @@ int spec_verify_attention_plan(const spec_attn_desc* d, int32_t k_draft, spec_at
  *  Draft j is accepted iff u_j * q_j(d_j) < p_j(d_j), u_j uniform in (0,1);
  *  m = first rejected j, else k. The last emitted token is drawn from
  *  w = max(0, p_m - q_m) (from p_m itself if that is all zero) when m < k, and
- *  from p_k when m == k. The draw is an exponential race: the candidate with
- *  the largest w / E, E = -ln U, wins, which samples it with probability
- *  w / sum(w) without normalising w. It runs at three levels, each an exact
- *  draw given the level above: (1) the groups of 8192 consecutive entries,
- *  weighted by their sums of w; (2) the 256 chunks of the winning group g,
- *  chunk c = entries {8192 g + 1024 i + 4 c + e : i < 8, e < 4}, weighted by
- *  their sums; (3) the entries of the winning chunk. Ties go to the lowest
- *  index; candidates of zero weight never win.
+ *  from p_k when m == k. The draw is an exponential race over the whole
+ *  vocabulary: every entry x with w_x > 0 gets the key w_x / E_x, E_x = -ln U_x,
+ *  and the largest key wins, which samples x with probability w_x / sum(w)
+ *  without normalising w. Ties go to the lowest index; entries of zero weight
+ *  never win.
  *
  *  Random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed by
  *  (philox_seed low word, philox_seed high word). u_j uses word 0 of counter
- *  (0, j, b, 0). The races at position m use, for group g, word (g mod 4) of
- *  counter (g / 4, m, b, 2); for chunk c of group g, word ((256 g + c) mod 4)
- *  of counter ((256 g + c) / 4, m, b, 3); for entry x, word (x mod 4) of
- *  counter (x / 4, m, b, 1). A word w maps to ((w >> 9) + 0.5) * 2^-23.
+ *  (0, j, b, 0); U_x of the race at position m uses word (x mod 4) of counter
+ *  (x / 4, m, b, 1). A word w maps to ((w >> 9) + 0.5) * 2^-23.
  *
  *  target_logits [B, k+1, V] fp32
  *  draft_tokens  [B, k] int32

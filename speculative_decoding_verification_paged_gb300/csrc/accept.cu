@@ -11,26 +11,37 @@
 // in the reject sampler's expected output of lmdeploy PR #3945.
 //
 // Design (GB300): one thread-block cluster per batch row, its CTAs splitting
-// the vocabulary into contiguous slices of whole 8192-logit groups (one to
-// six groups per CTA; at most 16 CTAs, 8 where the device cannot schedule a
-// 16-CTA cluster).
-// Positions are processed in order and the row stops at the first rejection,
-// so logits past it are never read (early exit). For each position every CTA
-// pulls its slice into shared memory with one bulk asynchronous copy (TMA,
-// mbarrier completion; position 0's copy is issued first thing, before the row
-// is validated), prefetches into L2 what comes next once the slice has landed
-// (the next position, and the draft probabilities a rejection would read),
-// reduces it (max / sum of exp / argmax) with warp shuffles, and publishes a
-// partial that every CTA of the cluster reads through distributed shared
-// memory, in rank order, so all CTAs reach bit-identical decisions without
-// any global-memory round trip. The correction / bonus token is a three-level
-// exponential race (groups of 8192 logits, their 256 chunks of 32, then the
-// chunk's logits): every CTA sums the weights of its groups and chunks in one
-// pass over the slice already in shared memory, all CTAs race the groups from
-// the published sums, and only the CTA holding the winning group races its
-// chunks and the winning chunk's entries, so Philox and logarithms are needed
-// for ~300 candidates per draw instead of one per logit.
+// the vocabulary into contiguous slices (a multiple of 4 logits each; at most
+// 16 CTAs, 8 where the device cannot schedule a 16-CTA cluster). Positions are
+// processed in order and the row stops at the first rejection, so logits past
+// it are never read (early exit), and nothing is fetched ahead of a decision.
+// For each position every CTA pulls its slice into shared memory with one
+// bulk asynchronous copy (TMA engine, mbarrier completion; position 0's copy
+// is issued first thing, before the row is validated). Each thread folds its
+// float4 groups of the slice into one partial in a single pass (a running
+// max with its sum of exponentials, or a running argmax), each warp combines
+// its lanes by shuffles and pushes the result straight into an exchange slot
+// of every CTA of the cluster (distributed shared memory), and one cluster
+// barrier per position publishes them: there is no CTA-wide barrier on the
+// path. Every warp of every CTA then combines the same partials in the same
+// order, so all CTAs reach bit-identical decisions. Lane j of every warp holds
+// draft j with its target logit and draft probability, read by shuffle at the
+// decisions. CTAs have 128 threads where six fit an SM and the grid fills it
+// (more rows resident), 256 otherwise.
+//
+// The correction / bonus token is the exponential race over the whole
+// vocabulary: entry x has the key w_x / E_x, E_x = -ln U_x, U_x from word
+// x mod 4 of Philox counter (x/4, m, b, 1), and the largest key wins. Each
+// thread first computes, for every entry of its slice, the weight and the
+// uniform and keeps the bounds w U / (1-U) <= w / E <= w / (1-U) (from
+// 1-U <= -ln U <= (1-U)/U), writing the upper bound over the slice; the
+// largest lower bound of the warp then rules out every entry whose upper bound
+// falls below it, and only the few entries left get the exact key (the
+// logarithm). The winner of each warp is exchanged like the statistics. A
+// rejected row's draft probabilities are read only here, after the decision.
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "launch_memo.h"
@@ -38,13 +49,12 @@
 namespace specv {
 namespace acc {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 16;
-constexpr int kGroup = 8192;         // logits per race group; a CTA's slice is whole groups
-constexpr int kChunks = 256;         // chunks per group (one per thread)
-constexpr int kMaxGroupsPerCta = 6;  // slice <= 48K logits (192 KB of shared memory)
+constexpr int kMaxWarps = 8;
 constexpr int kMaxK = 31;
+constexpr int kMinSlice = 4096;       // logits per CTA before another CTA joins the row
+constexpr int kMaxSlice = 48 * 1024;  // logits per CTA (192 KB of shared memory)
+constexpr int kBatch = 4;             // float4 groups per thread whose loads are in flight together
 
 struct Params {
   const float* logits;
@@ -56,114 +66,79 @@ struct Params {
   int32_t* accept_len;
   int32_t* dev_err;
   uint32_t seed_lo, seed_hi;
-  int batch, k, vocab, slice, csize, gpc;  // gpc: race groups per CTA (slice = gpc * kGroup)
-  int bulk;      // 1: rows are 16-byte aligned, use bulk copies
-  int prefetch;  // 1: prefetch the next position's slice into L2
+  int batch, k, vocab, slice, csize;
+  int bulk;  // 1: rows are 16-byte aligned, use bulk copies and float4 loads
 };
 
-// Partial published by each CTA for one reduction.
+// A partial pushed by one warp for one exchange.
 struct __align__(16) Part {
-  float f0;   // greedy: max logit; sampling: max logit of the slice; race: best key
-  float f1;   // sampling: sum of exp relative to f0; race: sum of residual weights
-  int32_t i0; // greedy / race: index of the best element
+  float f0;    // max logit, best race key, or the argmax value
+  float f1;    // sum of exponentials relative to f0
+  int32_t i0;  // argmax / race index
   int32_t pad;
 };
 
 struct Shared {
-  // Cluster exchange, push model: each CTA writes its partials into slot
-  // [its rank] of every peer before a cluster barrier, so everything read after
-  // the barrier is local and no CTA touches another's memory after its last one.
-  Part pos[kMaxK + 1][kMaxCluster];                   // per position: (max, sum) or (max, argmax)
-  float group_w[2][kMaxCluster * kMaxGroupsPerCta];   // per race: weight sum of every group
-  float chunk_w[kMaxGroupsPerCta * kChunks];          // this CTA's chunk weight sums (current race)
-  float wf[kWarps];
-  float wg[kWarps];
-  int32_t wi[kWarps];
-  int32_t draft[kMaxK];  // the row's draft tokens
-  float l_draft[kMaxK];  // target logit of each draft token, read once at start
-  float q_draft[kMaxK];  // draft probability of each draft token
+  // Exchange, push model: warp w of CTA r writes its partial into slot
+  // [r * warps + w] of every CTA of the cluster before a cluster barrier, so
+  // everything read after the barrier is local. Two slots alternate: a CTA
+  // writes slot e & 1 of exchange e only after the barrier of exchange e - 1,
+  // which every CTA reaches after reading exchange e - 2 from the same slot.
+  Part xch[2][kMaxCluster * kMaxWarps];
   uint64_t bar;
 };
 
-// Block-wide (max value, lowest index) reduction; result valid in every thread.
-__device__ __forceinline__ void block_argmax(Shared& sh, float& v, int& idx) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
-  }
-  __syncthreads();
-  if (lane == 0) { sh.wf[warp] = v; sh.wi[warp] = idx; }
-  __syncthreads();
-  v = sh.wf[0];
-  idx = sh.wi[0];
-  for (int w = 1; w < kWarps; ++w) {
-    const float ov = sh.wf[w];
-    const int oi = sh.wi[w];
-    if (ov > v || (ov == v && oi < idx)) { v = ov; idx = oi; }
-  }
+// Split cluster barrier used once at start-up: every CTA arrives as soon as it
+// runs and waits just before its first push into a peer's shared memory, so no
+// CTA writes into a peer that has not started (the rule for distributed shared
+// memory); by then the barrier has long completed.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory"); }
+
+// Combine two (max, sum of exp2((x - max) c2)) pairs; commutative, so a
+// butterfly leaves the same bits in every lane.
+__device__ __forceinline__ void ms_combine(float& m, float& s, float om, float os, float c2) {
+  const float nm = fmaxf(m, om);
+  const float a = m == -INFINITY ? 0.f : s * fast_exp2((m - nm) * c2);
+  const float b = om == -INFINITY ? 0.f : os * fast_exp2((om - nm) * c2);
+  m = nm;
+  s = a + b;
 }
 
-__device__ __forceinline__ float block_max(Shared& sh, float v) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
-  if (lane == 0) sh.wf[warp] = v;
-  __syncthreads();
-  v = sh.wf[0];
-  for (int w = 1; w < kWarps; ++w) v = fmaxf(v, sh.wf[w]);
-  return v;
-}
-
-__device__ __forceinline__ float block_sum(Shared& sh, float v) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) sh.wg[warp] = v;
-  __syncthreads();
-  v = sh.wg[0];
-  for (int w = 1; w < kWarps; ++w) v += sh.wg[w];
-  return v;
-}
-
-// Slice values x in [0, n) are read as float4 groups when the slice is 16-byte
-// aligned (always when bulk copies are used); `fn(x, v)` sees every element once.
-template <typename F>
-__device__ __forceinline__ void for_slice(const float* buf, int n, bool vec, F fn) {
-  if (vec) {
-    const float4* b4 = reinterpret_cast<const float4*>(buf);
-    for (int g = threadIdx.x; g * 4 < n; g += kThreads) {
-      const float4 v = b4[g];
-      fn(4 * g, v.x);
-      fn(4 * g + 1, v.y);
-      fn(4 * g + 2, v.z);
-      fn(4 * g + 3, v.w);
-    }
-  } else {
-    for (int x = threadIdx.x; x < n; x += kThreads) fn(x, buf[x]);
+// (value, index) with the larger value, the lower index on ties.
+__device__ __forceinline__ void vi_combine(float& v, int& i, float ov, int oi) {
+  if (ov > v || (ov == v && oi < i)) {
+    v = ov;
+    i = oi;
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
+template <int T>
+__global__ void __launch_bounds__(T, T == 128 ? 6 : 3) accept_kernel(const Params p) {
+  constexpr int kWarps = T / 32;
   extern __shared__ __align__(128) float buf[];
   __shared__ Shared sh;
-  const int tid = threadIdx.x;
+  float4* buf4 = reinterpret_cast<float4*>(buf);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int csize = p.csize;
   const int rank = (int)cluster_ctarank();
   const int b = blockIdx.x / csize;
   const int k = p.k, R = k + 1, V = p.vocab;
-  const int x0 = rank * p.slice;
-  const int n = min(p.slice, V - x0);  // >= 1 by construction of csize
-  const int lane = tid & 31;
+  const int x0 = rank * p.slice;              // a multiple of 4: group g holds Philox counter x0/4 + g
+  const int n = min(p.slice, V - x0);         // >= 1 by construction of csize
+  const int ngroups = (n + 3) >> 2;
+  const bool full = (n & 3) == 0;             // every float4 group lies inside the slice
   bool bulk = p.bulk != 0;
-  const bool vec = bulk;  // 16-byte aligned slices
   uint32_t phase = 0;
   bool pending = false;  // a bulk copy was issued and not yet observed complete
+  int xs = 0;            // exchanges so far (slot parity)
   auto row_ptr = [&](int j) { return p.logits + ((int64_t)b * R + j) * V + x0; };
+  // Copy position j's slice into shared memory. Bulk: one copy by thread 0,
+  // completion on the mbarrier. Plain (unaligned rows): every thread loads the
+  // groups it processes itself, so no barrier is needed; entries past the
+  // slice read as -inf.
   auto issue_row = [&](int j) {
     if (bulk) {
       if (tid == 0) {
@@ -173,7 +148,12 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
       pending = true;
     } else {
       const float* src = row_ptr(j);
-      for (int x = tid; x < n; x += kThreads) buf[x] = src[x];
+      for (int g = tid; g < ngroups; g += T) {
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = 4 * g + e < n ? src[4 * g + e] : -INFINITY;
+        buf4[g] = make_float4(v[0], v[1], v[2], v[3]);
+      }
     }
   };
   // Position 0 is read whatever the row holds, so its copy starts before anything
@@ -184,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
     fence_mbar_init();
   }
   if (bulk) issue_row(0);
+  cluster_arrive_relaxed();
 
   // ---- row validation (identical in every CTA of the cluster): the mode, the
   // temperature and the drafts (lane j holds d_j, k <= 31) are loaded together
@@ -194,13 +175,25 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
   bool valid = md == SPEC_MODE_GREEDY || md == SPEC_MODE_SAMPLE;
   int32_t err_bit = valid ? 0 : SPEC_DEVERR_MODE;
   if (token_bad) { valid = false; err_bit |= SPEC_DEVERR_TOKEN; }
-  float T = 1.f;
+  float T_ = 1.f;
   if (valid && md == SPEC_MODE_SAMPLE) {
-    T = t_row;
-    if (!(T > 0.f) || !isfinite(T)) { valid = false; err_bit |= SPEC_DEVERR_TEMPERATURE; }
+    T_ = t_row;
+    if (!(T_ > 0.f) || !isfinite(T_)) { valid = false; err_bit |= SPEC_DEVERR_TEMPERATURE; }
   }
-  if (tid < k) sh.draft[tid] = d_lane;
-  __syncthreads();
+  const bool greedy = md == SPEC_MODE_GREEDY;
+  // Lane j of every warp holds draft j, its target logit and its draft
+  // probability; decisions read them by shuffle, so there is no shared copy and
+  // no block barrier. The logit and probability are first used at position 0's
+  // decision, so their loads arrive while the slice is in flight. Without draft
+  // probabilities the draft distribution is one-hot at the drafted token.
+  float l_d = 0.f, q_d = 1.f;
+  if (lane < k && valid && !greedy) {
+    l_d = __ldg(p.logits + ((int64_t)b * R + lane) * V + d_lane);
+    if (p.probs) q_d = __ldg(p.probs + ((int64_t)b * k + lane) * V + d_lane);
+  }
+  // The mbarrier that thread 0 initialised is visible to every thread after this
+  // wait (its init fence is a release at cluster scope, the wait an acquire).
+  cluster_wait();  // every CTA of the cluster is running (see cluster_arrive_relaxed)
   if (!valid) {
     if (rank == 0 && tid == 0) {
       raise_error(p.dev_err, err_bit);
@@ -211,22 +204,11 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
     if (pending && !mbar_wait_bounded(&sh.bar, phase) && tid == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
     return;  // uniform across the cluster: no CTA touches another's shared memory
   }
-  const int32_t* d = sh.draft;
-  const bool greedy = md == SPEC_MODE_GREEDY;
-  const float c2 = (1.0f / T) * 1.4426950408889634f;  // logit -> log2 units of p
-  // The target logit and draft probability of each draft token are first read
-  // after the block barriers of position 0's reductions: they load while the
-  // slice is in flight.
-  if (!greedy && tid < k) {
-    sh.l_draft[tid] = __ldg(p.logits + ((int64_t)b * R + tid) * V + d_lane);
-    // without draft probabilities the draft distribution is one-hot at the drafted token
-    sh.q_draft[tid] = p.probs ? __ldg(p.probs + ((int64_t)b * k + tid) * V + d_lane) : 1.f;
-  }
+  const float c2 = (1.0f / T_) * 1.4426950408889634f;  // logit -> log2 units of p
 
-  // Wait for position j's slice; once it has landed, pull what position j may
-  // need next into L2 (the next position, and the draft probabilities a
-  // rejection at j reads), so these prefetches never compete with the slice.
-  auto wait_row = [&](int j) {
+  // Wait for the slice in flight (bulk copies; every thread observes the
+  // mbarrier itself, so no block barrier follows).
+  auto wait_row = [&]() {
     if (bulk && pending) {
       const bool ok = mbar_wait_bounded(&sh.bar, phase);
       phase ^= 1u;
@@ -236,273 +218,252 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
         bulk = false;  // stop issuing copies; later rows use plain loads
       }
     }
-    // same 16-byte alignment rule as the bulk copy
-    if (bulk && p.prefetch && tid == 0 && j < k) {
-      bulk_prefetch_l2(row_ptr(j + 1), (uint32_t)n * 4u);
-      if (!greedy && p.probs) bulk_prefetch_l2(p.probs + ((int64_t)b * k + j) * V + x0, (uint32_t)n * 4u);
-    }
-    __syncthreads();
   };
-  // Push this CTA's partial for position j into slot [rank] of every peer, then
-  // wait for all of the cluster's partials (all reads after this are local).
-  auto exchange = [&](int j, Part v) {
-    if (tid < csize) st_cluster_v4(map_to_rank(smem_u32(&sh.pos[j][rank]), (uint32_t)tid), v.f0, v.f1, v.i0, 0);
+  // Push this warp's partial (the same in all its lanes) into every CTA of the
+  // cluster, then wait for the cluster's partials; returns the slot to read.
+  auto exchange = [&](float f0, float f1, int i0) -> const Part* {
+    const int slot = xs & 1;
+    ++xs;
+    if (lane < csize)
+      st_cluster_v4(map_to_rank(smem_u32(&sh.xch[slot][rank * kWarps + warp]), (uint32_t)lane), f0, f1, i0, 0);
     cluster_sync_all();
+    return sh.xch[slot];
   };
-  // (best value, lowest index) over the cluster's partials of position j, by a
-  // fixed shuffle tree, so every CTA gets a bit-identical result.
-  auto cluster_best = [&](int j, float& bv, int& bi) {
-    float v = -INFINITY;
-    int i = INT32_MAX;
-    if (lane < csize) {
-      v = sh.pos[j][lane].f0;
-      i = sh.pos[j][lane].i0;
-    }
+  const int nparts = csize * kWarps;
+  // Softmax statistics of the whole row from the exchanged (max, sum) partials.
+  auto row_stats = [&](const Part* x, float& M, float& Z) {
+    float m = -INFINITY, s = 0.f;
+    for (int i = lane; i < nparts; i += 32) ms_combine(m, s, x[i].f0, x[i].f1, c2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-      if (ov > v || (ov == v && oi < i)) { v = ov; i = oi; }
+      const float om = __shfl_xor_sync(0xffffffffu, m, o), os = __shfl_xor_sync(0xffffffffu, s, o);
+      ms_combine(m, s, om, os, c2);
     }
+    M = m;
+    Z = s;
+  };
+  // (best value, lowest index) over the exchanged partials.
+  auto row_best = [&](const Part* x, float& bv, int& bi) {
+    float v = -INFINITY;
+    int i = INT32_MAX;
+    for (int t = lane; t < nparts; t += 32) vi_combine(v, i, x[t].f0, x[t].i0);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) vi_combine(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
     bv = v;
     bi = i;
   };
-  // Softmax statistics of the whole row from the cluster's (slice max, slice sum) pairs.
-  auto cluster_stats = [&](int j, float& M, float& Z) {
-    float mr = -INFINITY, zr = 0.f;
-    if (lane < csize) {
-      mr = sh.pos[j][lane].f0;
-      zr = sh.pos[j][lane].f1;
-    }
-    float mm = mr;
+  auto warp_best = [&](float& v, int& i) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
-    float zz = (lane < csize && mr != -INFINITY) ? zr * fast_exp2((mr - mm) * c2) : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
-    M = mm;
-    Z = zz;
+    for (int o = 16; o > 0; o >>= 1) vi_combine(v, i, __shfl_xor_sync(0xffffffffu, v, o), __shfl_xor_sync(0xffffffffu, i, o));
   };
-  // Write the row's result: accepted drafts, the final token, -1 padding.
+  // Write the row's result (one warp, lane j writes position j): accepted
+  // drafts, the final token, -1 padding.
   auto write_row = [&](int m, int token) {
-    int32_t* o = p.out_tokens + (int64_t)b * R;
-    for (int j = 0; j < m; ++j) o[j] = d[j];
-    o[m] = token;
-    for (int j = m + 1; j < R; ++j) o[j] = -1;
-    p.accept_len[b] = m;
+    if (lane < R) p.out_tokens[(int64_t)b * R + lane] = lane < m ? d_lane : (lane == m ? token : -1);
+    if (lane == 0) p.accept_len[b] = m;
+  };
+  // Four consecutive values at group g of a row slice in global memory (16-byte
+  // loads when rows are aligned; scalar loads, zero past the slice, otherwise).
+  auto load4 = [&](const float* src, int g) -> float4 {
+    if (p.bulk) return __ldg(reinterpret_cast<const float4*>(src) + g);
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = 4 * g + e < n ? src[4 * g + e] : 0.f;
+    return make_float4(v[0], v[1], v[2], v[3]);
   };
 
-  // Three-level exponential race over this row's weights at position `pos`
-  // (an exact sampler of w / sum(w)): group g (8192 consecutive logits) wins
-  // with key W_g / E, E = -ln U from word g%4 of Philox counter (g/4, pos, b, 2);
-  // in that group chunk c = {8192g + 1024i + 4c + e} wins with key S_c / E from
-  // counter ((256g+c)/4, pos, b, 3); in that chunk entry x wins with w_x / E
-  // from counter (x/4, pos, b, 1). Ties go to the lowest index.
-  // Weights, written over the slice in place as they are computed:
-  //   residual: buf holds e_x = exp2((l - m) c2) from the statistics pass and
-  //             w = max(0, e_x * f - q_x) with f = exp2((m - M) c2) / Z;
-  //   plain:    buf holds logits and w = exp2((l - M) c2).
-  // The CTA holding the winning group writes the output row (accept length m).
-  // Returns false in every CTA if all weights are 0 (nothing written).
-  auto race = [&](bool residual, float M, float f, const float* qrow, int pos, int slot, int m) -> bool {
-    // ---- pass over the slice: weights (in place), chunk sums (thread t owns chunk t of each group), group sums
-    for (int gl = 0; gl < p.gpc; ++gl) {
-      const int gbase = gl * kGroup;
-      float qv[8][4];
+  // Exponential race at position `pos` over the slice's logits (in buf):
+  //   residual: w = max(0, exp2((l - M) c2) * invZ - q)  (q: one-hot at the rejected draft when qrow is null)
+  //   plain:    w = exp2((l - M) c2)                     (scale does not matter to the race)
+  // Returns the winning index (the same in every CTA), or -1 if every weight is 0.
+  // Overwrites the slice with the key upper bounds.
+  auto race = [&](bool residual, float M, float invZ, const float* qrow, int pos) -> int {
+    const uint32_t cbase = (uint32_t)x0 >> 2;
+    const float mc2 = M * c2;
+    const int dpos = __shfl_sync(0xffffffffu, d_lane, pos);  // the rejected draft (one-hot q)
+    // The draft row of the rejected position is read in full below: ask L2 for
+    // all of this thread's pieces of it at once, so the batched loads hit L2.
+    if (residual && qrow != nullptr)
+      for (int g = tid; g < ngroups; g += T) asm volatile("prefetch.global.L2 [%0];\n" ::"l"(qrow + 4 * g));
+    // One pass, kBatch groups of the thread at a time: their draft-probability
+    // loads are issued first, the Philox blocks (which need no data) are
+    // computed while those loads are in flight, then each group's weights and
+    // key bounds are formed and the upper bounds written over the slice.
+    float lb_max = 0.f;
+    for (int g0 = tid; g0 < ngroups; g0 += kBatch * T) {
+      float4 q4[kBatch];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int off = gbase + 1024 * i + 4 * tid;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qv[i][e] = 0.f;
-        if (residual && off < n) {
-          if (qrow == nullptr) {  // one-hot draft distribution at the rejected draft token
-#pragma unroll
-            for (int e = 0; e < 4; ++e) qv[i][e] = (x0 + off + e == d[pos]) ? 1.f : 0.f;
-          } else if (vec) {
-            const float4 q4 = __ldg(reinterpret_cast<const float4*>(qrow + off));
-            qv[i][0] = q4.x; qv[i][1] = q4.y; qv[i][2] = q4.z; qv[i][3] = q4.w;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) qv[i][e] = (off + e < n) ? qrow[off + e] : 0.f;
-          }
-        }
+      for (int i = 0; i < kBatch; ++i) {
+        const int g = g0 + i * T;
+        q4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (residual && qrow != nullptr && g < ngroups) q4[i] = load4(qrow, g);
       }
-      float cs = 0.f;
+      Philox4 r[kBatch];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int off = gbase + 1024 * i + 4 * tid;
+      for (int i = 0; i < kBatch; ++i)
+        r[i] = philox4x32_10(cbase + (uint32_t)(g0 + i * T), (uint32_t)pos, (uint32_t)b, 1u, p.seed_lo, p.seed_hi);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (off + e < n) {
-            const float v = buf[off + e];
-            const float wt = residual ? fmaxf(v * f - qv[i][e], 0.f) : fast_exp2((v - M) * c2);
-            buf[off + e] = wt;
-            cs += wt;
-          }
-        }
-      }
-      sh.chunk_w[gl * kChunks + tid] = cs;
-      const float gsum = block_sum(sh, cs);
-      // push this group's sum to every CTA of the cluster
-      if (tid < csize)
-        st_cluster_f32(map_to_rank(smem_u32(&sh.group_w[slot][rank * p.gpc + gl]), (uint32_t)tid), gsum);
-    }
-    cluster_sync_all();
-    // ---- level 1, the same in every CTA: warp 0 races the groups from the exchanged
-    // sums and broadcasts (winner, total) through shared memory
-    const int n_groups = (V + kGroup - 1) / kGroup;
-    float gbest = -1.f, total = 0.f;
-    int gwin = INT32_MAX;
-    for (int gi = lane; tid < 32 && gi < ((n_groups + 31) & ~31); gi += 32) {
-      const float wg = gi < n_groups ? sh.group_w[slot][gi] : 0.f;
-      float key = 0.f;
-      if (wg > 0.f) {
-        const Philox4 w = philox4x32_10((uint32_t)gi >> 2, (uint32_t)pos, (uint32_t)b, 2u, p.seed_lo, p.seed_hi);
-        key = wg / -logf(word_to_uniform(w.v[gi & 3]));
-      }
-      float kk = key, tt = wg;
-      int ii = gi < n_groups ? gi : INT32_MAX;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ok = __shfl_xor_sync(0xffffffffu, kk, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, ii, o);
-        tt += __shfl_xor_sync(0xffffffffu, tt, o);
-        if (ok > kk || (ok == kk && oi < ii)) { kk = ok; ii = oi; }
-      }
-      total += tt;
-      if (kk > gbest || (kk == gbest && ii < gwin)) { gbest = kk; gwin = ii; }
-    }
-    if (tid == 0) {
-      sh.wf[0] = total;
-      sh.wi[0] = gwin;
-    }
-    __syncthreads();
-    total = sh.wf[0];
-    gwin = sh.wi[0];
-    __syncthreads();  // sh.wf / sh.wi are reused by the block reductions below
-    if (!(total > 0.f)) return false;  // the same in every CTA
-    const int owner = gwin / p.gpc, glw = gwin - owner * p.gpc;
-    if (rank != owner) return true;
-    // ---- level 2 (owner CTA): race the winning group's chunks
-    const float sc = sh.chunk_w[glw * kChunks + tid];
-    float key = 0.f;
-    if (sc > 0.f) {
-      const uint32_t ci = (uint32_t)(gwin * kChunks + tid);
-      const Philox4 w = philox4x32_10(ci >> 2, (uint32_t)pos, (uint32_t)b, 3u, p.seed_lo, p.seed_hi);
-      key = sc / -logf(word_to_uniform(w.v[ci & 3]));
-    }
-    int cwin = tid;
-    block_argmax(sh, key, cwin);
-    // ---- level 3: race the winning chunk's entries (warp 0, lane i: entries 1024 i + 4c + e)
-    if (tid < 32) {
-      float best = -1.f;
-      int bx = INT32_MAX;
-      if (tid < 8) {
-        const int off = glw * kGroup + 1024 * tid + 4 * cwin;
-        if (off < n) {
-          const Philox4 w =
-              philox4x32_10((uint32_t)((x0 + off) >> 2), (uint32_t)pos, (uint32_t)b, 1u, p.seed_lo, p.seed_hi);
+      for (int i = 0; i < kBatch; ++i) {
+        const int g = g0 + i * T;
+        if (g < ngroups) {
+          const float4 l4 = buf4[g];
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float qv[4] = {q4[i].x, q4[i].y, q4[i].z, q4[i].w};
+          const bool tail = !full && g == ngroups - 1;
+          float ub[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            if (off + e < n) {
-              const float wt = buf[off + e];
-              if (wt > 0.f) {
-                const float kx = wt / -logf(word_to_uniform(w.v[e]));
-                if (kx > best) { best = kx; bx = x0 + off + e; }
-              }
+            const float pe = fast_exp2(fmaf(lv[e], c2, -mc2));
+            float qe = qv[e];
+            if (residual && qrow == nullptr) qe = (x0 + 4 * g + e == dpos) ? 1.f : 0.f;
+            float w = residual ? fmaxf(pe * invZ - qe, 0.f) : pe;
+            if (tail && 4 * g + e >= n) w = 0.f;
+            // the word's top 23 bits j as the float 1 + j 2^-23 in [1, 2): then
+            // U = (2j + 1) 2^-24 = f1 - (1 - 2^-24) and 1 - U are exact subtractions
+            const float f1 = __uint_as_float(0x3F800000u | (r[i].v[e] >> 9));
+            const float u = f1 - 0.999999940395355224609375f;
+            const float v = 1.f - u;
+            ub[e] = __fdividef(w, v);
+            lb_max = fmaxf(lb_max, ub[e] * u);
+          }
+          buf4[g] = make_float4(ub[0], ub[1], ub[2], ub[3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lb_max = fmaxf(lb_max, __shfl_xor_sync(0xffffffffu, lb_max, o));
+    // exact keys for the entries whose upper bound reaches the warp's best lower bound
+    float best = -1.f;
+    int bx = INT32_MAX;
+    for (int g = tid; g < ngroups; g += T) {
+      const float4 u4 = buf4[g];
+      const float ub[4] = {u4.x, u4.y, u4.z, u4.w};
+      bool any = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) any |= ub[e] > 0.f && ub[e] >= lb_max;
+      if (any) {
+        const Philox4 r = philox4x32_10(cbase + (uint32_t)g, (uint32_t)pos, (uint32_t)b, 1u, p.seed_lo, p.seed_hi);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (ub[e] > 0.f && ub[e] >= lb_max) {
+            const float u = word_to_uniform(r.v[e]);
+            const float key = (ub[e] * (1.f - u)) / -logf(u);
+            if (key > best) {
+              best = key;
+              bx = x0 + 4 * g + e;
             }
           }
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, best, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bx, o);
-        if (ov > best || (ov == best && oi < bx)) { best = ov; bx = oi; }
-      }
-      if (tid == 0) write_row(m, bx);
     }
-    return true;
+    warp_best(best, bx);
+    const Part* x = exchange(best, 0.f, bx);
+    float kv;
+    int win;
+    row_best(x, kv, win);
+    return kv > 0.f ? win : -1;
   };
 
   if (!bulk) issue_row(0);  // with bulk copies position 0 is already in flight
   for (int j = 0; j <= k; ++j) {
-    wait_row(j);
+    wait_row();
     if (greedy) {
-      // ---- argmax of the slice, then of the cluster (ranks are in vocab order)
-      float v = -INFINITY;
-      int idx = INT32_MAX;
-      for_slice(buf, n, vec, [&](int x, float l) {
-        if (l > v) { v = l; idx = x0 + x; }
-      });
-      block_argmax(sh, v, idx);
-      exchange(j, Part{v, 0.f, idx, 0});
+      // ---- argmax of the slice (lowest index on ties), then of the row. Four
+      // independent running maxima (one per float4 lane) keep four compare
+      // chains in flight; each starts at its first element, so equal values
+      // still resolve to the lowest index when the four are merged.
+      float v4[4];
+      int i4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v4[e] = -INFINITY;
+        i4[e] = tid < ngroups ? x0 + 4 * tid + e : INT32_MAX;
+      }
+      for (int g = tid; g < ngroups; g += T) {
+        const float4 l4 = buf4[g];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if ((full || 4 * g + e < n) && lv[e] > v4[e]) {
+            v4[e] = lv[e];
+            i4[e] = x0 + 4 * g + e;
+          }
+        }
+      }
+      float v = v4[0];
+      int idx = i4[0];
+#pragma unroll
+      for (int e = 1; e < 4; ++e) vi_combine(v, idx, v4[e], i4[e]);
+      warp_best(v, idx);
+      const Part* x = exchange(v, 0.f, idx);
       float bv;
       int bi;
-      cluster_best(j, bv, bi);
-      if (j < k && d[j] == bi) {
+      row_best(x, bv, bi);
+      if (j < k && __shfl_sync(0xffffffffu, d_lane, j) == bi) {
         issue_row(j + 1);
         continue;
       }
-      if (rank == 0 && tid == 0) write_row(j, bi);
+      if (rank == 0 && warp == 0) write_row(j, bi);
       break;
     }
-    if (j == k) {
-      // ---- every draft accepted: bonus token from p_k, weights exp((l - max)/T)
-      float mx = -INFINITY;
-      for_slice(buf, n, vec, [&](int, float l) { mx = fmaxf(mx, l); });
-      mx = block_max(sh, mx);
-      exchange(j, Part{mx, 0.f, 0, 0});
-      float M, Zunused;
-      cluster_stats(j, M, Zunused);
-      race(false, M, 1.f, nullptr, k, 0, k);
-      break;
+    // ---- sampling: max and sum of exp2((l - max) c2) of the slice in one pass,
+    // with two running (max, sum) pairs over alternate groups (two chains in flight)
+    auto fold = [&](const float4 l4, float& m, float& s) {
+      const float gm = fmaxf(fmaxf(l4.x, l4.y), fmaxf(l4.z, l4.w));
+      if (gm == -INFINITY) return;
+      if (gm > m) {
+        if (m != -INFINITY) s *= fast_exp2((m - gm) * c2);
+        m = gm;
+      }
+      s += (fast_exp2((l4.x - m) * c2) + fast_exp2((l4.y - m) * c2)) +
+           (fast_exp2((l4.z - m) * c2) + fast_exp2((l4.w - m) * c2));
+    };
+    float m = -INFINITY, s = 0.f, mb = -INFINITY, sb = 0.f;
+    for (int g = tid; g < ngroups; g += 2 * T) {
+      fold(buf4[g], m, s);
+      if (g + T < ngroups) fold(buf4[g + T], mb, sb);
     }
-    // ---- sampling statistics of p_j = softmax(l / T): slice max, then
-    // e = exp2((l - max) c2) written over the slice (the race reuses it) and summed
-    float mx = -INFINITY;
-    for_slice(buf, n, vec, [&](int, float l) { mx = fmaxf(mx, l); });
-    mx = block_max(sh, mx);
-    float z = 0.f;
-    if (vec) {
-      float4* b4 = reinterpret_cast<float4*>(buf);
-      for (int g4 = tid; g4 * 4 < n; g4 += kThreads) {
-        float4 v = b4[g4];
-        v.x = fast_exp2((v.x - mx) * c2); v.y = fast_exp2((v.y - mx) * c2);
-        v.z = fast_exp2((v.z - mx) * c2); v.w = fast_exp2((v.w - mx) * c2);
-        b4[g4] = v;
-        z += (v.x + v.y) + (v.z + v.w);
+    ms_combine(m, s, mb, sb, c2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, m, o), os = __shfl_xor_sync(0xffffffffu, s, o);
+      ms_combine(m, s, om, os, c2);
+    }
+    const Part* x = exchange(m, s, 0);
+    float M, Z;
+    row_stats(x, M, Z);
+    int token;
+    if (j < k) {
+      const float pd = fast_exp2((__shfl_sync(0xffffffffu, l_d, j) - M) * c2) / Z;
+      const float qd = __shfl_sync(0xffffffffu, q_d, j);
+      const Philox4 wu = philox4x32_10(0u, (uint32_t)j, (uint32_t)b, 0u, p.seed_lo, p.seed_hi);
+      const float u = word_to_uniform(wu.v[0]);
+      if (u * qd < pd) {
+        issue_row(j + 1);
+        continue;
+      }
+      // ---- rejected at j: race over max(0, p_j - q_j), or over p_j if that is all zero
+      const float* qrow = p.probs ? p.probs + ((int64_t)b * k + j) * V + x0 : nullptr;
+      token = race(true, M, 1.f / Z, qrow, j);
+      if (token < 0) {
+        // all-zero residual (rare): reload the logits over the overwritten slice, race over p_j
+        const float* src = row_ptr(j);
+        for (int g = tid; g < ngroups; g += T) {
+          float4 v = load4(src, g);
+          if (!p.bulk) {
+            if (4 * g + 1 >= n) v.y = -INFINITY;
+            if (4 * g + 2 >= n) v.z = -INFINITY;
+            if (4 * g + 3 >= n) v.w = -INFINITY;
+          }
+          buf4[g] = v;
+        }
+        token = race(false, M, 1.f, nullptr, j);
       }
     } else {
-      for (int x = tid; x < n; x += kThreads) {
-        const float e = fast_exp2((buf[x] - mx) * c2);
-        buf[x] = e;
-        z += e;
-      }
+      // ---- every draft accepted: bonus token from p_k
+      token = race(false, M, 1.f, nullptr, k);
     }
-    z = block_sum(sh, z);
-    exchange(j, Part{mx, z, 0, 0});
-    float M, Z;
-    cluster_stats(j, M, Z);
-    const float pd = fast_exp2((sh.l_draft[j] - M) * c2) / Z;
-    const float qd = sh.q_draft[j];
-    const Philox4 wu = philox4x32_10(0u, (uint32_t)j, (uint32_t)b, 0u, p.seed_lo, p.seed_hi);
-    const float u = word_to_uniform(wu.v[0]);
-    if (u * qd < pd) {
-      issue_row(j + 1);
-      continue;
-    }
-    // ---- rejected at j: race over max(0, p_j - q_j), or over p_j if that is all zero
-    const float f = fast_exp2((mx - M) * c2) / Z;  // e_x * f = p_j(x) on this slice
-    const float* qrow = p.probs ? p.probs + ((int64_t)b * k + j) * V + x0 : nullptr;
-    if (!race(true, M, f, qrow, j, 0, j)) {
-      // all-zero residual (rare): reload the logits over the overwritten slice and race over p_j
-      __syncthreads();
-      const float* src = row_ptr(j);
-      for (int x = tid; x < n; x += kThreads) buf[x] = src[x];
-      __syncthreads();
-      race(false, M, 1.f, nullptr, j, 1, j);
-    }
+    if (rank == 0 && warp == 0) write_row(j, token);
     break;
   }
 
@@ -513,15 +474,91 @@ __global__ void __launch_bounds__(kThreads, 4) accept_kernel(const Params p) {
   // barrier, and nothing after it reads or writes another CTA's memory.
 }
 
-// Cluster size and slice: the slice is a whole number of race groups, at most
-// 16 CTAs per cluster (the limit on one GPC), at most kMaxGroupsPerCta groups each.
-static int pick_cluster(int vocab, int max_csize, int& slice, int& gpc) {
-  const int n_groups = (vocab + kGroup - 1) / kGroup;
-  int c = n_groups < max_csize ? n_groups : max_csize;
-  gpc = (n_groups + c - 1) / c;
-  c = (n_groups + gpc - 1) / gpc;  // every CTA owns at least one logit
-  slice = gpc * kGroup;
-  return c;
+// Cluster size and slice: at most `max_csize` CTAs, slices of at least
+// kMinSlice logits (fewer CTAs for small vocabularies), a multiple of 4 each.
+static int pick_cluster(int vocab, int max_csize, int& slice) {
+  int c = (vocab + kMinSlice - 1) / kMinSlice;
+  c = c < 1 ? 1 : (c > max_csize ? max_csize : c);
+  slice = (vocab + c - 1) / c;
+  slice = (slice + 3) & ~3;
+  return (vocab + slice - 1) / slice;  // every CTA owns at least one logit
+}
+
+// Static shared memory per CTA (the Shared struct) plus what the runtime reserves.
+constexpr size_t kStaticBytes = sizeof(Shared) + 1024;
+
+// 128 threads per CTA where six CTAs fit an SM (small slices: more rows
+// resident) and the grid is large enough to use them, else 256 (more warps to
+// hide each CTA's latencies). SPEC_ACCEPT_THREADS=128 or =256 overrides.
+static int pick_threads(int slice, int64_t ctas, int sms) {
+  const char* env = getenv("SPEC_ACCEPT_THREADS");
+  if (env != nullptr && strcmp(env, "128") == 0) return 128;
+  if (env != nullptr && strcmp(env, "256") == 0) return 256;
+  if (ctas <= 2 * (int64_t)sms) return 256;
+  return 6 * ((size_t)slice * 4 + kStaticBytes) <= 228 * 1024 ? 128 : 256;
+}
+
+struct Plan {
+  int vocab = 0, csize = 0, slice = 0;
+};
+
+template <int T>
+static int launch(Params p, int batch, int vocab, cudaStream_t stream) {
+  auto kern = accept_kernel<T>;
+  const int dev = current_device();
+  if (dev < 0) return SPEC_ERR_LAUNCH;
+  // The cluster plan (size, slice) depends only on the device and the
+  // vocabulary: it is worked out once per (device, vocabulary) together with
+  // the kernel attributes, under a lock shared by all host threads.
+  static LaunchMemo memo;
+  static Plan plans[kMaxDevices];
+  static bool attrs_set[kMaxDevices];
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.blockDim = dim3(T, 1, 1);
+  cfg.stream = stream;
+  {
+    std::lock_guard<std::mutex> lock(memo.mu);
+    if (!attrs_set[dev]) {
+      // 16-CTA clusters are beyond the portable size; the largest shared-memory
+      // carveout keeps as many slices resident as fit
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+          cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+        return SPEC_ERR_LAUNCH;
+      attrs_set[dev] = true;
+    }
+    if (plans[dev].vocab != vocab) {  // vocab >= 1, so 0 marks "no plan yet"
+      // Clusters larger than 8 CTAs are not guaranteed to fit a GPC; if the
+      // device cannot hold one, use 8 CTAs with larger slices.
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        if (p.slice > kMaxSlice) return SPEC_ERR_UNSUPPORTED;
+        if (!grant_smem_locked(memo, (const void*)kern, dev, (size_t)p.slice * sizeof(float))) return SPEC_ERR_LAUNCH;
+        if (p.csize <= 8) break;
+        cfg.gridDim = dim3((unsigned)p.csize, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)p.slice * sizeof(float);
+        attr[0].val.clusterDim.x = (unsigned)p.csize;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0) break;
+        (void)cudaGetLastError();
+        p.csize = pick_cluster(vocab, 8, p.slice);
+      }
+      plans[dev].csize = p.csize;
+      plans[dev].slice = p.slice;
+      plans[dev].vocab = vocab;
+    }
+    p.csize = plans[dev].csize;
+    p.slice = plans[dev].slice;
+  }
+  cfg.gridDim = dim3((unsigned)(batch * p.csize), 1, 1);
+  cfg.dynamicSmemBytes = (size_t)p.slice * sizeof(float);
+  attr[0].val.clusterDim.x = (unsigned)p.csize;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return SPEC_ERR_LAUNCH;
+  return SPEC_OK;
 }
 
 }  // namespace acc
@@ -538,9 +575,9 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
   if (!target_logits || !draft_tokens || !mode || !temperature || !out_tokens || !accept_len)
     return SPEC_ERR_INVALID_ARG;
   if (k_draft > acc::kMaxK) return SPEC_ERR_UNSUPPORTED;
-  int slice = 0, gpc = 0;
-  const int csize = acc::pick_cluster(vocab, acc::kMaxCluster, slice, gpc);
-  if (gpc > acc::kMaxGroupsPerCta) return SPEC_ERR_UNSUPPORTED;
+  int slice = 0;
+  const int csize = acc::pick_cluster(vocab, acc::kMaxCluster, slice);
+  if (slice > acc::kMaxSlice) return SPEC_ERR_UNSUPPORTED;
   if ((int64_t)batch * csize > INT32_MAX) return SPEC_ERR_UNSUPPORTED;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
@@ -560,64 +597,12 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
   p.vocab = vocab;
   p.slice = slice;
   p.csize = csize;
-  p.gpc = gpc;
   const bool aligned = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(target_logits) & 15) == 0) &&
                        (draft_probs == nullptr || (reinterpret_cast<uintptr_t>(draft_probs) & 15) == 0);
   p.bulk = aligned ? 1 : 0;
-  p.prefetch = 1;
-
-  auto kern = acc::accept_kernel;
-  const int dev = current_device();
-  if (dev < 0) return SPEC_ERR_LAUNCH;
-  // The cluster plan (size, slice, groups per CTA) depends only on the device and
-  // the vocabulary: it is worked out once per (device, vocabulary), together with
-  // the kernel attributes, under a lock shared by all host threads.
-  static LaunchMemo memo;
-  static int plan_vocab[kMaxDevices], plan_csize[kMaxDevices], plan_slice[kMaxDevices], plan_gpc[kMaxDevices];
-  static bool nonportable[kMaxDevices];
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.blockDim = dim3(acc::kThreads, 1, 1);
-  cfg.stream = stream;
-  {
-    std::lock_guard<std::mutex> lock(memo.mu);
-    if (plan_vocab[dev] != vocab) {  // vocab >= 1, so 0 marks "no plan yet"
-      // Clusters larger than 8 CTAs are not guaranteed to fit a GPC; if the
-      // device cannot hold one, use 8 CTAs with larger slices.
-      for (int attempt = 0; attempt < 2; ++attempt) {
-        if (!grant_smem_locked(memo, (const void*)kern, dev, (size_t)p.slice * sizeof(float))) return SPEC_ERR_LAUNCH;
-        if (p.csize <= 8) break;
-        if (!nonportable[dev]) {
-          if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-            return SPEC_ERR_LAUNCH;
-          nonportable[dev] = true;
-        }
-        cfg.gridDim = dim3((unsigned)p.csize, 1, 1);
-        cfg.dynamicSmemBytes = (size_t)p.slice * sizeof(float);
-        attr[0].val.clusterDim.x = (unsigned)p.csize;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters > 0) break;
-        (void)cudaGetLastError();
-        p.csize = acc::pick_cluster(vocab, 8, p.slice, p.gpc);
-        if (p.gpc > acc::kMaxGroupsPerCta) return SPEC_ERR_UNSUPPORTED;
-      }
-      plan_csize[dev] = p.csize;
-      plan_slice[dev] = p.slice;
-      plan_gpc[dev] = p.gpc;
-      plan_vocab[dev] = vocab;
-    }
-    p.csize = plan_csize[dev];
-    p.slice = plan_slice[dev];
-    p.gpc = plan_gpc[dev];
-  }
-  cfg.gridDim = dim3((unsigned)(batch * p.csize), 1, 1);
-  cfg.dynamicSmemBytes = (size_t)p.slice * sizeof(float);
-  attr[0].val.clusterDim.x = (unsigned)p.csize;
-  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) return SPEC_ERR_LAUNCH;
-  return SPEC_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SPEC_ERR_LAUNCH;
+  return acc::pick_threads(slice, (int64_t)batch * csize, sms) == 128 ? acc::launch<128>(p, batch, vocab, stream)
+                                                                      : acc::launch<256>(p, batch, vocab, stream);
 }
