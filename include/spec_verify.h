@@ -124,12 +124,12 @@ size_t spec_verify_attention_workspace(const spec_attn_desc* d, int32_t k_draft)
  * chosen on the device from ctx_lens, so no host synchronisation is needed.
  * Calls may come from several host threads at once (each with its own
  * workspace and stream).
- * Kernels: D = 128 with (k_draft+1)*G >= 17 packed query rows runs on the
- * 5th-generation tensor cores (tcgen05, 128-key tiles, accumulators in tensor
- * memory) when that kernel's shared-memory plan fits the batch; other shapes
- * run on mma.sync tiles. The environment variable SPEC_ATTN_KERNEL=tc or =mma
- * overrides the choice for D = 128. Both give the same result within rounding
- * (fp32 accumulation in both).
+ * Kernels: D = 128 or 256 with (k_draft+1)*G >= 17 packed query rows runs on
+ * the 5th-generation tensor cores (tcgen05, 128-key tiles, accumulators in
+ * tensor memory) when that kernel's shared-memory plan fits the batch; other
+ * shapes run on mma.sync tiles. The environment variable SPEC_ATTN_KERNEL=tc
+ * or =mma overrides the choice for D = 128 and 256. Both give the same result
+ * within rounding (fp32 accumulation in both).
  * Device errors: a sequence with an out-of-range ctx_len (SPEC_DEVERR_CTX_LEN)
  * or block id (SPEC_DEVERR_BLOCK_ID) gets out rows of zeros.
  * Supported: D in {64,128,256}; bs in {16,32,64,128}; (k_draft+1)*G <= 64.
@@ -183,9 +183,10 @@ size_t spec_verify_attention_noalloc_limit(void);
  *
  * Returns SPEC_ERR_INVALID_ARG for an invalid descriptor or a null plan,
  * SPEC_ERR_UNSUPPORTED for a shape spec_verify_attention rejects the same way,
- * and SPEC_ERR_LAUNCH when a device query it needs fails (D = 128 with 17 or
- * more packed rows reads the current device's shared-memory limit; other
- * shapes need no device). Launches nothing and touches no device memory.
+ * and SPEC_ERR_LAUNCH when a device query it needs fails (D = 128 or 256 with
+ * 17 or more packed rows, or with SPEC_ATTN_KERNEL=tc, reads the current
+ * device's shared-memory limit; other shapes need no device). Launches
+ * nothing and touches no device memory.
  */
 #define SPEC_ATTN_KERNEL_MMA 1 /* mma.sync m16n8k16 tiles                    */
 #define SPEC_ATTN_KERNEL_TC 2  /* tcgen05 MMAs, accumulators in tensor memory */

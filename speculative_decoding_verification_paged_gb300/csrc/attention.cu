@@ -166,7 +166,7 @@ static LaunchMemo& memo_main() {
   return memo;
 }
 
-template <int MT, int S, int NP>
+template <int D, int MT, int S, int NP>
 static LaunchMemo& memo_tc() {
   static LaunchMemo memo;
   return memo;
@@ -179,10 +179,10 @@ static int settings_main(int batch, Settings* st) {
 }
 
 // The tcgen05 kernel runs one CTA per SM.
-template <int MT, int S, int NP>
+template <int D, int MT, int S, int NP>
 static int settings_tc(int batch, Settings* st) {
-  return settings_for(memo_tc<MT, S, NP>(), tc::verify_attention_tc_kernel<MT, S, NP>,
-                      tc::smem_bytes<MT, S, NP>(batch), tc::kThreads, true, st);
+  return settings_for(memo_tc<D, MT, S, NP>(), tc::verify_attention_tc_kernel<D, MT, S, NP>,
+                      tc::smem_bytes<D, MT, S, NP>(batch), tc::kThreads, true, st);
 }
 
 template <int D, int MT>
@@ -192,22 +192,24 @@ static int launch_main(const Params& p, const Settings& st, const CUtensorMap& t
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
-template <int MT, int S, int NP>
+template <int D, int MT, int S, int NP>
 static int launch_tc(const Params& p, const Settings& st, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t stream) {
-  tc::verify_attention_tc_kernel<MT, S, NP><<<st.grid, tc::kThreads, st.smem, stream>>>(p, tq, tk, tv);
+  tc::verify_attention_tc_kernel<D, MT, S, NP><<<st.grid, tc::kThreads, st.smem, stream>>>(p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
 enum class Kernel { kMma, kTc };
 
-// Which kernel runs a call. D = 128 with 32 or more packed query rows per kv head
-// takes the tcgen05 kernel (its MMAs stay wide, where mma.sync tiles become
-// compute-bound), 16 rows the mma.sync kernel (at that width both are bound by
-// HBM and the mma.sync kernel, two CTAs per SM, hides its per-unit work better).
-// The environment variable SPEC_ATTN_KERNEL=tc or =mma overrides the choice; the
-// tcgen05 kernel also needs its shared-memory plan to fit the batch. Both compute
-// the same result within rounding.
+// Which kernel runs a call. D = 128 or 256 with 32 or more packed query rows
+// per kv head (17 or more, padded to 32 or 64) takes the tcgen05 kernel (its
+// MMAs stay wide, where mma.sync tiles become compute-bound or, at D = 256,
+// register-bound), 16 rows the mma.sync kernel (at that width both are bound
+// by HBM and the mma.sync kernel, two CTAs per SM at D = 128, hides its
+// per-unit work better). The environment variable SPEC_ATTN_KERNEL=tc or =mma
+// overrides the choice for D = 128 and 256; the tcgen05 kernel also needs its
+// shared-memory plan to fit the batch. Both compute the same result within
+// rounding.
 struct Choice {
   Kernel kind;
   int stages;     // tcgen05: K/V ring stages (the mma.sync kernel's are fixed by Cfg)
@@ -217,7 +219,7 @@ struct Choice {
 // Returns SPEC_OK, or SPEC_ERR_LAUNCH when the device query the tcgen05 plan needs fails.
 static int choose_kernel(int D, int mt, int batch, Choice* c) {
   *c = Choice{Kernel::kMma, 0, 0};
-  if (D != 128) return SPEC_OK;
+  if (D != 128 && D != 256) return SPEC_OK;
   const char* env = getenv("SPEC_ATTN_KERNEL");
   const bool force_tc = env != nullptr && strcmp(env, "tc") == 0;
   const bool force_mma = env != nullptr && strcmp(env, "mma") == 0;
@@ -226,16 +228,26 @@ static int choose_kernel(int D, int mt, int batch, Choice* c) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return SPEC_ERR_LAUNCH;
-  // stages x P buffers per row count, most overlap first (the instances dispatch launches)
-  size_t need3 = SIZE_MAX, need2 = SIZE_MAX;
+  // stages x P buffers per row count, most overlap first (the instances dispatch
+  // launches). At D = 256 one 128-key K + V stage is 128 KB, so there is one.
+  size_t need3 = SIZE_MAX, need2 = SIZE_MAX, need1 = SIZE_MAX;
   int np = 2;
-  switch (mt) {
-    case 1: need3 = tc::smem_bytes<1, 3, 2>(batch); need2 = tc::smem_bytes<1, 2, 2>(batch); break;
-    case 2: need2 = tc::smem_bytes<2, 2, 2>(batch); break;
-    default: need2 = tc::smem_bytes<4, 2, 1>(batch); np = 1; break;
+  if (D == 128) {
+    switch (mt) {
+      case 1: need3 = tc::smem_bytes<128, 1, 3, 2>(batch); need2 = tc::smem_bytes<128, 1, 2, 2>(batch); break;
+      case 2: need2 = tc::smem_bytes<128, 2, 2, 2>(batch); break;
+      default: need2 = tc::smem_bytes<128, 4, 2, 1>(batch); np = 1; break;
+    }
+  } else {
+    switch (mt) {
+      case 1: need1 = tc::smem_bytes<256, 1, 1, 2>(batch); break;
+      case 2: need1 = tc::smem_bytes<256, 2, 1, 2>(batch); break;
+      default: need1 = tc::smem_bytes<256, 4, 1, 1>(batch); np = 1; break;
+    }
   }
   if (need3 <= (size_t)optin) c->stages = 3;
   else if (need2 <= (size_t)optin) c->stages = 2;
+  else if (need1 <= (size_t)optin) c->stages = 1;
   else return SPEC_OK;
   c->kind = Kernel::kTc;
   c->p_buffers = np;
@@ -295,10 +307,15 @@ static int prepare(int D, int rows, int batch, Prepared* pr) {
   const int rc = choose_kernel(D, pr->mt, batch, &pr->ch);
   if (rc != SPEC_OK) return rc;
   if (pr->ch.kind == Kernel::kTc) {
-    if (pr->mt == 1) return pr->ch.stages == 3 ? settings_tc<1, 3, 2>(batch, &pr->st)
-                                              : settings_tc<1, 2, 2>(batch, &pr->st);
-    if (pr->mt == 2) return settings_tc<2, 2, 2>(batch, &pr->st);
-    return settings_tc<4, 2, 1>(batch, &pr->st);
+    if (D == 256) {
+      if (pr->mt == 1) return settings_tc<256, 1, 1, 2>(batch, &pr->st);
+      if (pr->mt == 2) return settings_tc<256, 2, 1, 2>(batch, &pr->st);
+      return settings_tc<256, 4, 1, 1>(batch, &pr->st);
+    }
+    if (pr->mt == 1) return pr->ch.stages == 3 ? settings_tc<128, 1, 3, 2>(batch, &pr->st)
+                                              : settings_tc<128, 1, 2, 2>(batch, &pr->st);
+    if (pr->mt == 2) return settings_tc<128, 2, 2, 2>(batch, &pr->st);
+    return settings_tc<128, 4, 2, 1>(batch, &pr->st);
   }
   switch (D) {
     case 64: return settings_main_d<64>(pr->mt, batch, &pr->st);
@@ -319,10 +336,15 @@ static int dispatch(const Params& p, const Prepared& pr, int D, int bs, const vo
       !make_map(&tv_map, v_cache, D, p.num_kv_heads, (uint64_t)num_blocks * bs, 1, (uint32_t)(bs < tk ? bs : tk)))
     return SPEC_ERR_LAUNCH;
   if (ch.kind == Kernel::kTc) {
-    if (mt == 1) return ch.stages == 3 ? launch_tc<1, 3, 2>(p, pr.st, tq, tk_map, tv_map, stream)
-                                    : launch_tc<1, 2, 2>(p, pr.st, tq, tk_map, tv_map, stream);
-    if (mt == 2) return launch_tc<2, 2, 2>(p, pr.st, tq, tk_map, tv_map, stream);
-    return launch_tc<4, 2, 1>(p, pr.st, tq, tk_map, tv_map, stream);
+    if (D == 256) {
+      if (mt == 1) return launch_tc<256, 1, 1, 2>(p, pr.st, tq, tk_map, tv_map, stream);
+      if (mt == 2) return launch_tc<256, 2, 1, 2>(p, pr.st, tq, tk_map, tv_map, stream);
+      return launch_tc<256, 4, 1, 1>(p, pr.st, tq, tk_map, tv_map, stream);
+    }
+    if (mt == 1) return ch.stages == 3 ? launch_tc<128, 1, 3, 2>(p, pr.st, tq, tk_map, tv_map, stream)
+                                    : launch_tc<128, 1, 2, 2>(p, pr.st, tq, tk_map, tv_map, stream);
+    if (mt == 2) return launch_tc<128, 2, 2, 2>(p, pr.st, tq, tk_map, tv_map, stream);
+    return launch_tc<128, 4, 2, 1>(p, pr.st, tq, tk_map, tv_map, stream);
   }
   switch (D) {
     case 64: return launch_main_d<64>(p, mt, pr.st, tq, tk_map, tv_map, stream);

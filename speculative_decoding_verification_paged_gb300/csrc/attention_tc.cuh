@@ -1,10 +1,12 @@
-// Tensor-core (tcgen05) kernel for D = 128.
+// Tensor-core (tcgen05) kernel for D = 128 and D = 256.
 //
 // The keys are the MMA's M dimension (128 per tile) and the packed query rows
 // are N (16, 32 or 64), so every M = 128 MMA is fully used for any row count:
-//   S^T[128 keys x N] = K[128 x 128] . Q^T            (K, Q K-major in smem)
-//   O^T[128 d x N]   += V^T[128 x 128 keys] . P^T     (V and P MN-major)
-// with S^T (two buffers) and O^T in tensor memory. Warp 0 stages K/V/Q with
+//   S^T[128 keys x N] = K[128 x D] . Q^T              (K, Q K-major in smem)
+//   O^T[D x N]       += V^T[D x 128 keys] . P^T       (V and P MN-major)
+// with S^T (two buffers) and O^T in tensor memory; for D = 256, O^T is two
+// halves of 128 lanes (dims 0-127 and 128-255), each the accumulator of its
+// own M = 128 P.V MMA, at consecutive column blocks. Warp 0 stages K/V/Q with
 // TMA, warp 1 issues the MMAs (one thread; QK of tile i+1 before P.V of tile
 // i), warps 2-9 run the softmax in two warpgroups, each owning half of the
 // rows; a warp reads the 32-lane quarter of tensor memory that its index
@@ -21,7 +23,6 @@ namespace specv {
 namespace attn {
 namespace tc {
 
-constexpr int D = 128;
 constexpr int TK = 128;                      // keys per tile (MMA M)
 constexpr int kSoftmaxWarps = 8;             // two warpgroups, each owning half the query rows
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
@@ -32,15 +33,17 @@ constexpr int kRegBudgetThreads = 384;
 constexpr int kBarGroup0 = 2;                // named barriers: one per softmax warpgroup,
 constexpr int kBarSoftmax = 4;               // all softmax warps,
 constexpr int kBarTail = 5;                  // MMA warp + softmax warps
-constexpr int kTmemCols = 256;               // S^T buffers at columns 0 and N, O^T at 2N
+constexpr int kTmemCols = 256;               // S^T buffers at columns 0 and N, O^T halves from 2N
 
-template <int MT>
+template <int D, int MT>
 struct Cfg {
   static constexpr int N = 16 * MT;                     // packed query rows (MMA N)
   static constexpr int CW = N / 2;                      // rows (tensor-memory columns) per warpgroup
-  static constexpr int TILE_BYTES = TK * D * 2;         // 32 KB: two [128][64] slices
+  static constexpr int SUBS = D / 64;                   // 128-byte-wide column slices
+  static constexpr int HALVES = D / 128;                // O^T halves of 128 lanes
+  static constexpr int TILE_BYTES = TK * D * 2;         // SUBS [128][64] slices: 32 KB (D = 128), 64 KB
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K + V
-  static constexpr int Q_BYTES = N * D * 2;             // two [N][64] slices
+  static constexpr int Q_BYTES = N * D * 2;             // SUBS [N][64] slices
   static constexpr int P_BYTES = N * TK * 2;            // one of P_hi / P_lo: [128 keys][N rows]
   // P is the P.V operand B in MN-major layout: the N rows of a key are contiguous
   // (N * 2 bytes) and swizzled at that width (32, 64 or 128 bytes), so a softmax
@@ -48,13 +51,14 @@ struct Cfg {
   static constexpr uint32_t P_LAYOUT = N == 16 ? 6u : (N == 32 ? 4u : 2u);
   static constexpr int P_SWZ_SHIFT = N == 16 ? 2 : (N == 32 ? 1 : 0);  // key bits that pick the XOR
   static constexpr int P_SWZ_MASK = N == 16 ? 1 : (N == 32 ? 3 : 7);
+  static_assert(2 * N + HALVES * N <= kTmemCols, "S^T buffers and O^T fit the allocated columns");
 };
 
 // Dynamic shared memory: stages + query buffers, NP P buffers (hi + lo), barriers,
 // reductions, output row offsets, and the per-sequence plan (which grows with the batch).
-template <int MT, int S, int NP>
+template <int D, int MT, int S, int NP>
 size_t smem_bytes(int batch) {
-  using C = Cfg<MT>;
+  using C = Cfg<D, MT>;
   return 1024 + (size_t)S * (C::STAGE_BYTES + C::Q_BYTES) + (size_t)NP * 2 * C::P_BYTES + 64 * 8 + 4 * 64 * 4 +
          64 * 4 + 64 * 8 + 64 + align256((size_t)(batch + 2) * 4) + align256((size_t)batch * 4) + 128;
 }
@@ -117,11 +121,11 @@ __device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)
   tmem_wait_st();
 }
 
-template <int MT, int S, int NP>
+template <int D, int MT, int S, int NP>
 __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kernel(
     const Params p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v) {
-  using C = Cfg<MT>;
+  using C = Cfg<D, MT>;
   constexpr int N = C::N, CW = C::CW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -233,11 +237,11 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     tmem_relinquish();
   }
   // padded query rows stay zero in every query buffer (TMA writes rows < R*G only)
-  for (int i = tid; i < S * 2 * (N - p.n_rows) * 8; i += kThreads) {
+  for (int i = tid; i < S * C::SUBS * (N - p.n_rows) * 8; i += kThreads) {
     const int ch = i % 8, rest = i / 8;
     const int r = p.n_rows + rest % (N - p.n_rows);
     const int bsub = rest / (N - p.n_rows);
-    const int buf = bsub / 2, sub = bsub % 2;
+    const int buf = bsub / C::SUBS, sub = bsub % C::SUBS;
     *reinterpret_cast<uint4*>(qbuf + buf * C::Q_BYTES + sub * N * 128 + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
   }
   fence_proxy_async_smem();  // zeroed rows are read by the tensor core
@@ -299,15 +303,16 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
           mbar_arrive_expect_tx(&full_k[s], (uint32_t)C::TILE_BYTES + q_bytes);
           if (fresh) {
             const uint32_t qdst = q_u32 + slot * C::Q_BYTES;
-            tma_load_3d(qdst, &tm_q, 0, g * G, b * R, &full_k[s]);
-            tma_load_3d(qdst + N * 128, &tm_q, 64, g * G, b * R, &full_k[s]);
+#pragma unroll
+            for (int sub = 0; sub < C::SUBS; ++sub)
+              tma_load_3d(qdst + sub * N * 128, &tm_q, sub * 64, g * G, b * R, &full_k[s]);
           }
           const uint32_t kdst = ring_u32 + s * C::STAGE_BYTES;
 #pragma unroll
           for (int pc = 0; pc < TK / 16; ++pc) {
             if (pc >= pieces) break;
 #pragma unroll
-            for (int sub = 0; sub < 2; ++sub)
+            for (int sub = 0; sub < C::SUBS; ++sub)
               tma_load_3d(kdst + sub * TK * 128 + pc * BH * 128, &tm_k, sub * 64, g, zc[pc], &full_k[s]);
           }
         }
@@ -322,7 +327,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
         for (int pc = 0; pc < TK / 16; ++pc) {
           if (pc >= pieces) break;
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub)
+          for (int sub = 0; sub < C::SUBS; ++sub)
             tma_load_3d(vdst + sub * TK * 128 + pc * BH * 128, &tm_v, sub * 64, g_prev, zprev[pc], &full_v[s]);
         }
       }
@@ -382,10 +387,13 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
         for (int part = 0; part < 2; ++part) {
 #pragma unroll
           for (int kk = 0; kk < TK / 16; ++kk) {
-            const uint32_t voff = (kk * 2048) >> 4;
             const uint32_t poff = (part * C::P_BYTES + kk * 32 * N) >> 4;
-            umma_bf16(tmem_o, vmn + vb + voff, pmn + pb + poff, idesc_pv,
-                      (pv_fresh && part == 0 && kk == 0) ? 0u : 1u);
+#pragma unroll
+            for (int h = 0; h < C::HALVES; ++h) {  // dims [128h, 128h + 128): V slices 2h, 2h + 1
+              const uint32_t voff = (h * 2 * TK * 128 + kk * 2048) >> 4;
+              umma_bf16(tmem_o + (uint32_t)(h * N), vmn + vb + voff, pmn + pb + poff, idesc_pv,
+                        (pv_fresh && part == 0 && kk == 0) ? 0u : 1u);
+            }
           }
         }
         umma_commit(&pv_done[i % NP]);  // P buffer free, O^T holds tiles <= i
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     }
     named_sync(bar_group, 128);
     const bool bad = fin_bad;
-    const int d = q4 * 32 + lane;  // the O^T lane this thread reads
+    const int d = q4 * 32 + lane;  // the O^T lane this thread reads (in each half)
     constexpr int CH = CW < 16 ? CW : 16;  // columns per step
 #pragma unroll
     for (int c = 0; c < CW; c += CH) {
@@ -465,14 +473,17 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
           __stcg(p.lse + (int64_t)F.slot * p.n_rows + r, lse2);
         }
       }
-      float ov[CH];
-      tmem_load_cols<CH>(tmem_o + lane_off + c0 + c, ov);
 #pragma unroll
-      for (int e = 0; e < CH; ++e) {
-        const int r = c0 + c + e;
-        if (r < p.n_rows) {
-          const int64_t off = F.complete ? s_rowoff[r] : ((int64_t)F.slot * p.n_rows + r) * D;
-          __stcg((F.complete ? p.out : p.opart) + off + d, ov[e] * inv[e]);
+      for (int h = 0; h < C::HALVES; ++h) {
+        float ov[CH];
+        tmem_load_cols<CH>(tmem_o + (uint32_t)(h * N) + lane_off + c0 + c, ov);
+#pragma unroll
+        for (int e = 0; e < CH; ++e) {
+          const int r = c0 + c + e;
+          if (r < p.n_rows) {
+            const int64_t off = F.complete ? s_rowoff[r] : ((int64_t)F.slot * p.n_rows + r) * D;
+            __stcg((F.complete ? p.out : p.opart) + off + h * 128 + d, ov[e] * inv[e]);
+          }
         }
       }
     }
@@ -615,11 +626,14 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
           if constexpr (!kMaxInSmem) m_reg[kMaxInSmem ? 0 : c + e] = mn;
         }
         if (!cu_fresh) {
-          float ov[CH];
-          tmem_load_cols<CH>(tmem_o + lane_off + c0 + c, ov);
 #pragma unroll
-          for (int e = 0; e < CH; ++e) ov[e] *= alpha[e];
-          tmem_store_cols<CH>(tmem_o + lane_off + c0 + c, ov);
+          for (int h = 0; h < C::HALVES; ++h) {
+            float ov[CH];
+            tmem_load_cols<CH>(tmem_o + (uint32_t)(h * N) + lane_off + c0 + c, ov);
+#pragma unroll
+            for (int e = 0; e < CH; ++e) ov[e] *= alpha[e];
+            tmem_store_cols<CH>(tmem_o + (uint32_t)(h * N) + lane_off + c0 + c, ov);
+          }
         }
       }
       if constexpr (kMaxInSmem) {
@@ -634,12 +648,20 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     }
     // ---- keys past the context in the last tile may hold stale bytes: zero those V rows
     if (t0 + TK > ctx) {
+      // With one stage the previous tile's V may still be in flight here, and the
+      // V barrier's parity would then name an earlier phase: wait until the
+      // previous tile's P.V is done (its V landed and consumed) before asking for
+      // this tile's V. With two or more stages the V of tile i - S has landed
+      // before QK of tile i is issued, so the parity is already unambiguous.
+      if constexpr (S == 1) {
+        if (i > 0) wait_pv(i - 1);
+      }
       if (!mbar_wait_bounded(&full_v[stage], (uint32_t)((i / S) & 1)) && st == 0)
         raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);  // V of this tile has landed
       const int valid = ctx - t0;
       uint8_t* vt = ring + stage * C::STAGE_BYTES + C::TILE_BYTES;
-      for (int j = st; j < (TK - valid) * 16; j += kSoftmaxThreads) {
-        const int row = valid + j / 16, ch = j % 16;
+      for (int j = st; j < (TK - valid) * (D / 8); j += kSoftmaxThreads) {
+        const int row = valid + j / (D / 8), ch = j % (D / 8);
         *reinterpret_cast<uint4*>(vt + (ch >> 3) * TK * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) =
             make_uint4(0, 0, 0, 0);
       }

@@ -2,9 +2,10 @@
 
 Small cases and the named workloads at their full sizes are checked in full,
 every sequence and every output element, from the same device inputs. Tolerances: max-abs <= 1e-2 and relative L2 <=
-2e-3 per case. Head dim 128 has two kernels (tcgen05, the default from 32 packed
-rows up, and mma.sync; SPEC_ATTN_KERNEL=tc / =mma forces one); every
-head-dim-128 case runs both, and one case runs the default choice.
+2e-3 per case. Head dims 128 and 256 have two kernels (tcgen05, the default
+from 17 packed rows up, and mma.sync; SPEC_ATTN_KERNEL=tc / =mma forces one);
+every case with those head dims runs both, and one case runs the default
+choice.
 """
 
 import zlib
@@ -46,6 +47,11 @@ TC_CASES = [
     ("tc_mt2_k7_bs64", 4, (8, 200, 513, 1500), 64, 16, 4, 128, 7),
     ("tc_mt4_bs16", 3, (5, 300, 1200), 16, 64, 4, 128, 3),
     ("tc_mt4_k7_bs32", 3, (8, 640, 1030), 32, 16, 2, 128, 7),
+    # head dim 256: one 128-key stage, O^T in two 128-lane halves
+    ("tc_d256_mt1_bs32", 4, (4, 127, 129, 900), 32, 8, 2, 256, 3),
+    ("tc_d256_mt2_rows24_bs64", 5, (5, 64, 130, 1000, 2500), 64, 24, 4, 256, 3),
+    ("tc_d256_mt2_k7_bs16", 3, (9, 385, 1400), 16, 8, 2, 256, 7),
+    ("tc_d256_mt4_bs128", 3, (9, 256, 1500), 128, 16, 2, 256, 7),
 ]
 
 
@@ -72,7 +78,7 @@ def run_attention(sv, a, w, **kw):
 @pytest.mark.parametrize("case", SMALL + TC_CASES, ids=[c[0] for c in SMALL + TC_CASES])
 def test_attention_small_cases_full_parity(sv, oracle_mod, case, attn_kernel):
     name, B, ctx, bs, Hq, Hkv, D, k = case
-    if D != 128 and attn_kernel == "tc":
+    if D == 64 and attn_kernel == "tc":
         pytest.skip("one kernel for this head dim")
     w = wl.Workload(name=name, batch=B, ctx_lens=ctx, block_size=bs, num_q_heads=Hq, num_kv_heads=Hkv,
                     head_dim=D, k_draft=k, seed=zlib.crc32(name.encode()) % 1000)
@@ -99,7 +105,7 @@ def test_attention_full_size_every_sequence(sv, oracle_mod, name, attn_kernel):
     times: every sequence of the batch against the oracle, element by element, so every
     unit the stream-K plan cuts across CTAs (and merges by log-sum-exp) is compared."""
     w = wl.WORKLOADS[name]
-    if w.head_dim != 128 and attn_kernel == "tc":
+    if w.head_dim == 64 and attn_kernel == "tc":
         pytest.skip("one kernel for this head dim")
     a = wl.make_attention_inputs(w, device=DEV)
     out, err = run_attention(sv, a, w)
@@ -163,27 +169,25 @@ def test_attention_default_kernel_choice(sv, oracle_mod, monkeypatch, name):
     assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
 
 
-@pytest.mark.parametrize("name,kind", [("longctx", "tc"), ("llama8b_eagle3", "mma"), ("hybrid_gdn", "mma")])
+@pytest.mark.parametrize("name,kind", [("longctx", "tc"), ("llama8b_eagle3", "mma"), ("hybrid_gdn", "tc")])
 def test_attention_plan_names_the_kernel_that_runs(sv, monkeypatch, name, kind):
-    """spec_verify_attention_plan names the kernel the call runs. The two head-dim-128
-    kernels round differently, so the default call's output equals, bit for bit,
+    """spec_verify_attention_plan names the kernel the call runs. The two kernels of
+    a head dim round differently, so the default call's output equals, bit for bit,
     that of the kernel the plan names when SPEC_ATTN_KERNEL forces it, and differs
-    from the other's; head dim 256 has the mma.sync kernel only."""
+    from the other's."""
     monkeypatch.delenv("SPEC_ATTN_KERNEL", raising=False)
     w = wl.WORKLOADS[name].replace(batch=3, ctx_lens=(129, 3000, 9), ctx_range=None)
     a = wl.make_attention_inputs(w, device=DEV)
     plan_of = lambda: sv.spec_verify_attention_plan(a["q"], a["k_cache"], a["block_table"], w.k_draft)
     plan = plan_of()
     assert plan["kernel"] == kind
-    assert plan["stages"] >= 2
+    assert plan["stages"] >= (1 if w.head_dim == 256 and kind == "tc" else 2)
     if kind == "tc":
         assert plan["keys_per_tile"] == 128 and plan["p_buffers"] >= 1 and plan["ctas_per_sm"] == 1
     else:
         assert plan["p_buffers"] == 0
     default, err = run_attention(sv, a, w)
     assert err == 0
-    if w.head_dim != 128:
-        return
     forced = {}
     for k in ("tc", "mma"):
         monkeypatch.setenv("SPEC_ATTN_KERNEL", k)
@@ -212,10 +216,10 @@ def _random_shape(rng):
 @pytest.mark.parametrize("seed", range(12))
 def test_attention_random_shapes(sv, oracle_mod, attn_kernel, seed):
     """Seeded random shapes: every head dim, block size, GQA group and draft length
-    within the supported range, ragged contexts, both kernels where D = 128."""
+    within the supported range, ragged contexts, both kernels where D = 128 or 256."""
     rng = np.random.default_rng(1000 + seed)
     B, ctx, bs, Hq, Hkv, D, k = _random_shape(rng)
-    if D != 128 and attn_kernel == "tc":
+    if D == 64 and attn_kernel == "tc":
         pytest.skip("one kernel for this head dim")
     w = wl.Workload(name=f"rand{seed}", batch=B, ctx_lens=ctx, block_size=bs, num_q_heads=Hq,
                     num_kv_heads=Hkv, head_dim=D, k_draft=k, seed=seed)
