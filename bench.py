@@ -518,7 +518,9 @@ def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush
     recurrent state and its checkpoints. The step's activations and scheduling data are copied
     in every step: q, the block table and context lengths, the target logits, the draft tokens
     and draft probabilities, per-row mode and temperature (and, with --gdn-verify, the
-    recurrence's q, k, v and gates). The outputs are read back."""
+    recurrence's q, k, v and gates). The outputs are read back. Within a step the acceptance
+    inputs are copied on a second stream while the attention call runs, as an engine would
+    overlap them."""
     host = {n: a[n].cpu().pin_memory() for n in ("q", "block_table", "ctx_lens")}
     for n in ["target_logits", "draft_tokens", "draft_probs", "mode", "temperature"]:
         host[n] = acc_in[n].cpu().pin_memory()
@@ -526,6 +528,8 @@ def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush
     if gv is not None:
         gdn_host = {n: gv[n].cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
     devbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    attn_inputs = ("q", "block_table", "ctx_lens")
+    side = torch.cuda.Stream(device=dev)  # the acceptance inputs arrive while attention runs
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     toks_h = torch.empty(toks.shape, dtype=toks.dtype).pin_memory()
     alen_h = torch.empty(alen.shape, dtype=alen.dtype).pin_memory()
@@ -535,14 +539,20 @@ def run_e2e(sv, w, a, acc_in, commit, out, ws, toks, alen, err, dev, args, flush
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def step():
-        for n, t in host.items():
-            devbuf[n].copy_(t, non_blocking=True)
+        side.wait_stream(stream)  # the previous step is done with the buffers
+        with torch.cuda.stream(side):
+            for n, t in host.items():
+                if n not in attn_inputs:
+                    devbuf[n].copy_(t, non_blocking=True)
+        for n in attn_inputs:
+            devbuf[n].copy_(host[n], non_blocking=True)
         sv.spec_verify_attention(devbuf["q"], a["k_cache"], a["v_cache"], devbuf["block_table"],
                                  devbuf["ctx_lens"], w.k_draft, out, workspace=ws, dev_err=err)
         if gv is not None:
             for n, t in gdn_host.items():  # the step's activations into the buffers the recurrence reads
                 gv[n].copy_(t, non_blocking=True)
             gdn_verify()
+        stream.wait_stream(side)
         sv.spec_accept(devbuf["target_logits"], devbuf["draft_tokens"], devbuf["draft_probs"],
                        acc_in["philox_seed"], devbuf["mode"], devbuf["temperature"], toks, alen, dev_err=err)
         commit()
