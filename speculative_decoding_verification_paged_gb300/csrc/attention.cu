@@ -166,7 +166,7 @@ static LaunchMemo& memo_main() {
   return memo;
 }
 
-template <int D, int MT, int S, int NP>
+template <int D, int MT, int S, int NP, int SV, int SQ>
 static LaunchMemo& memo_tc() {
   static LaunchMemo memo;
   return memo;
@@ -179,10 +179,10 @@ static int settings_main(int batch, Settings* st) {
 }
 
 // The tcgen05 kernel runs one CTA per SM.
-template <int D, int MT, int S, int NP>
+template <int D, int MT, int S, int NP, int SV = S, int SQ = S>
 static int settings_tc(int batch, Settings* st) {
-  return settings_for(memo_tc<D, MT, S, NP>(), tc::verify_attention_tc_kernel<D, MT, S, NP>,
-                      tc::smem_bytes<D, MT, S, NP>(batch), tc::kThreads, true, st);
+  return settings_for(memo_tc<D, MT, S, NP, SV, SQ>(), tc::verify_attention_tc_kernel<D, MT, S, NP, SV, SQ>,
+                      tc::smem_bytes<D, MT, S, NP, SV, SQ>(batch), tc::kThreads, true, st);
 }
 
 template <int D, int MT>
@@ -192,10 +192,10 @@ static int launch_main(const Params& p, const Settings& st, const CUtensorMap& t
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
-template <int D, int MT, int S, int NP>
+template <int D, int MT, int S, int NP, int SV = S, int SQ = S>
 static int launch_tc(const Params& p, const Settings& st, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t stream) {
-  tc::verify_attention_tc_kernel<D, MT, S, NP><<<st.grid, tc::kThreads, st.smem, stream>>>(p, tq, tk, tv);
+  tc::verify_attention_tc_kernel<D, MT, S, NP, SV, SQ><<<st.grid, tc::kThreads, st.smem, stream>>>(p, tq, tk, tv);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 
@@ -212,7 +212,8 @@ enum class Kernel { kMma, kTc };
 // rounding.
 struct Choice {
   Kernel kind;
-  int stages;     // tcgen05: K/V ring stages (the mma.sync kernel's are fixed by Cfg)
+  int stages;     // tcgen05: K ring stages (the V ring has as many, or two with three
+                  // K stages at 64 rows; the mma.sync kernel's are fixed by Cfg)
   int p_buffers;  // tcgen05: shared-memory buffers of P
 };
 
@@ -236,7 +237,11 @@ static int choose_kernel(int D, int mt, int batch, Choice* c) {
     switch (mt) {
       case 1: need3 = tc::smem_bytes<128, 1, 3, 2>(batch); need2 = tc::smem_bytes<128, 1, 2, 2>(batch); break;
       case 2: need2 = tc::smem_bytes<128, 2, 2, 2>(batch); break;
-      default: need2 = tc::smem_bytes<128, 4, 2, 1>(batch); np = 1; break;
+      default:  // 64 rows: three K stages, two V stages, one query buffer when they fit
+        need3 = tc::smem_bytes<128, 4, 3, 1, 2, 1>(batch);
+        need2 = tc::smem_bytes<128, 4, 2, 1>(batch);
+        np = 1;
+        break;
     }
   } else {
     switch (mt) {
@@ -315,7 +320,8 @@ static int prepare(int D, int rows, int batch, Prepared* pr) {
     if (pr->mt == 1) return pr->ch.stages == 3 ? settings_tc<128, 1, 3, 2>(batch, &pr->st)
                                               : settings_tc<128, 1, 2, 2>(batch, &pr->st);
     if (pr->mt == 2) return settings_tc<128, 2, 2, 2>(batch, &pr->st);
-    return settings_tc<128, 4, 2, 1>(batch, &pr->st);
+    return pr->ch.stages == 3 ? settings_tc<128, 4, 3, 1, 2, 1>(batch, &pr->st)
+                              : settings_tc<128, 4, 2, 1>(batch, &pr->st);
   }
   switch (D) {
     case 64: return settings_main_d<64>(pr->mt, batch, &pr->st);
@@ -344,7 +350,8 @@ static int dispatch(const Params& p, const Prepared& pr, int D, int bs, const vo
     if (mt == 1) return ch.stages == 3 ? launch_tc<128, 1, 3, 2>(p, pr.st, tq, tk_map, tv_map, stream)
                                     : launch_tc<128, 1, 2, 2>(p, pr.st, tq, tk_map, tv_map, stream);
     if (mt == 2) return launch_tc<128, 2, 2, 2>(p, pr.st, tq, tk_map, tv_map, stream);
-    return launch_tc<128, 4, 2, 1>(p, pr.st, tq, tk_map, tv_map, stream);
+    return ch.stages == 3 ? launch_tc<128, 4, 3, 1, 2, 1>(p, pr.st, tq, tk_map, tv_map, stream)
+                          : launch_tc<128, 4, 2, 1>(p, pr.st, tq, tk_map, tv_map, stream);
   }
   switch (D) {
     case 64: return launch_main_d<64>(p, mt, pr.st, tq, tk_map, tv_map, stream);

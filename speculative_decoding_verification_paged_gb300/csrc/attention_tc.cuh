@@ -42,7 +42,6 @@ struct Cfg {
   static constexpr int SUBS = D / 64;                   // 128-byte-wide column slices
   static constexpr int HALVES = D / 128;                // O^T halves of 128 lanes
   static constexpr int TILE_BYTES = TK * D * 2;         // SUBS [128][64] slices: 32 KB (D = 128), 64 KB
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // K + V
   static constexpr int Q_BYTES = N * D * 2;             // SUBS [N][64] slices
   static constexpr int P_BYTES = N * TK * 2;            // one of P_hi / P_lo: [128 keys][N rows]
   // P is the P.V operand B in MN-major layout: the N rows of a key are contiguous
@@ -54,12 +53,13 @@ struct Cfg {
   static_assert(2 * N + HALVES * N <= kTmemCols, "S^T buffers and O^T fit the allocated columns");
 };
 
-// Dynamic shared memory: stages + query buffers, NP P buffers (hi + lo), barriers,
-// reductions, output row offsets, and the per-sequence plan (which grows with the batch).
-template <int D, int MT, int S, int NP>
+// Dynamic shared memory: S K tiles, SV V tiles, SQ query buffers, NP P buffers
+// (hi + lo), barriers, reductions, output row offsets, and the per-sequence plan
+// (which grows with the batch).
+template <int D, int MT, int S, int NP, int SV = S, int SQ = S>
 size_t smem_bytes(int batch) {
   using C = Cfg<D, MT>;
-  return 1024 + (size_t)S * (C::STAGE_BYTES + C::Q_BYTES) + (size_t)NP * 2 * C::P_BYTES + 64 * 8 + 4 * 64 * 4 +
+  return 1024 + (size_t)(S + SV) * C::TILE_BYTES + (size_t)SQ * C::Q_BYTES + (size_t)NP * 2 * C::P_BYTES + 64 * 8 + 4 * 64 * 4 +
          64 * 4 + 64 * 8 + 64 + align256((size_t)(batch + 2) * 4) + align256((size_t)batch * 4) + 128;
 }
 
@@ -121,32 +121,37 @@ __device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)
   tmem_wait_st();
 }
 
-template <int D, int MT, int S, int NP>
+// S K stages, SV V stages and SQ query buffers (1, or at least S). K and V are
+// released separately, so the rings may differ in depth: a K tile is refilled
+// once its QK is done, a V tile once its P.V is done.
+template <int D, int MT, int S, int NP, int SV = S, int SQ = S>
 __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kernel(
     const Params p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v) {
   using C = Cfg<D, MT>;
   constexpr int N = C::N, CW = C::CW;
+  static_assert(SQ == 1 || SQ >= S, "a query buffer is reused only after the K stage that covers it");
+  static_assert(2 * S + 2 * SV + 2 + 2 + NP + 1 <= 64, "barriers fit their area");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;
-  uint8_t* qbuf = ring + S * C::STAGE_BYTES;
-  uint8_t* pbuf = qbuf + S * C::Q_BYTES;  // NP x (P_hi, P_lo)
+  uint8_t* ring = smem;                                // S K tiles, then SV V tiles
+  uint8_t* qbuf = ring + (S + SV) * C::TILE_BYTES;
+  uint8_t* pbuf = qbuf + SQ * C::Q_BYTES;  // NP x (P_hi, P_lo)
   // K and V of a stage arrive and are released separately: K is free once QK is
   // done, a tile earlier than V, so the producer can fetch the next K sooner.
   uint64_t* full_k = reinterpret_cast<uint64_t*>(pbuf + NP * 2 * C::P_BYTES);
   uint64_t* full_v = full_k + S;
-  uint64_t* empty_k = full_v + S;
+  uint64_t* empty_k = full_v + SV;
   uint64_t* empty_v = empty_k + S;
-  uint64_t* s_full = empty_v + S;   // [2]: S^T buffer b holds QK of the tile
+  uint64_t* s_full = empty_v + SV;  // [2]: S^T buffer b holds QK of the tile
   uint64_t* p_full = s_full + 2;  // [2]: P of tile i written (one arrival per softmax warp)
   uint64_t* pv_done = p_full + 2; // [NP]: P.V of the tile that used P buffer j is complete
   uint64_t* fin_bar = pv_done + NP;
   float* s_red = reinterpret_cast<float*>(full_k + 64);   // [4][64] per-quarter row reductions
   float* s_mrun = s_red + 4 * 64;                         // [64] running row max (64-row tiles)
   int64_t* s_rowoff = reinterpret_cast<int64_t*>(s_mrun + 64);  // [64] output offset of each row
-  int32_t* s_bad = reinterpret_cast<int32_t*>(s_rowoff + 64);  // [4]
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bad + 4);   // tensor-memory base
+  int32_t* s_bad = reinterpret_cast<int32_t*>(s_rowoff + 64);  // [8] per unit (seq & 7): a block id was bad
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(s_bad + 8);   // tensor-memory base
   int32_t* s_prefix = reinterpret_cast<int32_t*>(s_bad + 16);
   int32_t* s_ctx = s_prefix + ((p.batch + 2 + 63) & ~63);
   int32_t* s_misc = s_ctx + ((p.batch + 63) & ~63);
@@ -203,8 +208,10 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     if (tid == 0) {
       for (int s = 0; s < S; ++s) {
         mbar_init(&full_k[s], 1);
-        mbar_init(&full_v[s], 1);
         mbar_init(&empty_k[s], 1);
+      }
+      for (int s = 0; s < SV; ++s) {
+        mbar_init(&full_v[s], 1);
         mbar_init(&empty_v[s], 1);
       }
       for (int j = 0; j < 2; ++j) {
@@ -237,7 +244,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     tmem_relinquish();
   }
   // padded query rows stay zero in every query buffer (TMA writes rows < R*G only)
-  for (int i = tid; i < S * C::SUBS * (N - p.n_rows) * 8; i += kThreads) {
+  for (int i = tid; i < SQ * C::SUBS * (N - p.n_rows) * 8; i += kThreads) {
     const int ch = i % 8, rest = i / 8;
     const int r = p.n_rows + rest % (N - p.n_rows);
     const int bsub = rest / (N - p.n_rows);
@@ -272,7 +279,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
         const int b = ld.b;
         const int ctx = s_ctx[b];
         const int t0 = ld.tile * TK;
-        const int slot = ld.seq % S;
+        const int slot = ld.seq % SQ;
         const int s = j % S;
         bool bad = false;
 #pragma unroll
@@ -297,8 +304,13 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
         if (lane == 0) {
           if (j >= S && !mbar_wait_bounded(&empty_k[s], (uint32_t)(((j - S) / S) & 1)))
             raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
-          if (fresh) s_bad[slot] = 0;
-          if (bad) s_bad[slot] = 1;
+          // one query buffer: the previous unit's last QK (tile j - 1) must be done
+          // before this unit's queries overwrite it
+          if (SQ == 1 && S > 1 && fresh && j >= 1 &&
+              !mbar_wait_bounded(&empty_k[(j - 1) % S], (uint32_t)(((j - 1) / S) & 1)))
+            raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+          if (fresh) s_bad[ld.seq & 7] = 0;
+          if (bad) s_bad[ld.seq & 7] = 1;
           const uint32_t q_bytes = fresh ? (uint32_t)(R * G * D * 2) : 0u;
           mbar_arrive_expect_tx(&full_k[s], (uint32_t)C::TILE_BYTES + q_bytes);
           if (fresh) {
@@ -307,7 +319,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
             for (int sub = 0; sub < C::SUBS; ++sub)
               tma_load_3d(qdst + sub * N * 128, &tm_q, sub * 64, g * G, b * R, &full_k[s]);
           }
-          const uint32_t kdst = ring_u32 + s * C::STAGE_BYTES;
+          const uint32_t kdst = ring_u32 + s * C::TILE_BYTES;
 #pragma unroll
           for (int pc = 0; pc < TK / 16; ++pc) {
             if (pc >= pieces) break;
@@ -318,11 +330,11 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
         }
       }
       if (j >= 1 && lane == 0) {
-        const int jv = j - 1, s = jv % S;
-        if (jv >= S && !mbar_wait_bounded(&empty_v[s], (uint32_t)(((jv - S) / S) & 1)))
+        const int jv = j - 1, s = jv % SV;
+        if (jv >= SV && !mbar_wait_bounded(&empty_v[s], (uint32_t)(((jv - SV) / SV) & 1)))
           raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
         mbar_arrive_expect_tx(&full_v[s], (uint32_t)C::TILE_BYTES);
-        const uint32_t vdst = ring_u32 + s * C::STAGE_BYTES + C::TILE_BYTES;
+        const uint32_t vdst = ring_u32 + (S + s) * C::TILE_BYTES;
 #pragma unroll
         for (int pc = 0; pc < TK / 16; ++pc) {
           if (pc >= pieces) break;
@@ -360,8 +372,8 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
         const int s = i % S;
         if (!mbar_wait_bounded(&full_k[s], (uint32_t)((i / S) & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
         tc_fence_after();
-        const uint32_t kb = (ring_u32 + s * C::STAGE_BYTES) >> 4;
-        const uint32_t qb = (q_u32 + (q_seq % S) * C::Q_BYTES) >> 4;
+        const uint32_t kb = (ring_u32 + s * C::TILE_BYTES) >> 4;
+        const uint32_t qb = (q_u32 + (q_seq % SQ) * C::Q_BYTES) >> 4;
         const uint32_t dst = tmem + (uint32_t)((i & 1) * N);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -379,9 +391,9 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
       for (int i = 0; i < n_tiles; ++i) {
         if (i + 1 < n_tiles) issue_qk(i + 1);
         if (!mbar_wait_bounded(&p_full[i & 1], (uint32_t)((i >> 1) & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
-        if (!mbar_wait_bounded(&full_v[i % S], (uint32_t)((i / S) & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+        if (!mbar_wait_bounded(&full_v[i % SV], (uint32_t)((i / SV) & 1))) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
         tc_fence_after();
-        const uint32_t vb = (ring_u32 + (i % S) * C::STAGE_BYTES + C::TILE_BYTES) >> 4;
+        const uint32_t vb = (ring_u32 + (S + i % SV) * C::TILE_BYTES) >> 4;
         const uint32_t pb = (p_u32 + (i % NP) * 2 * C::P_BYTES) >> 4;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
@@ -397,7 +409,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
           }
         }
         umma_commit(&pv_done[i % NP]);  // P buffer free, O^T holds tiles <= i
-        umma_commit(&empty_v[i % S]);   // V of the stage can be refilled
+        umma_commit(&empty_v[i % SV]);  // V of the stage can be refilled
         if (i == n_tiles - 1) umma_commit(fin_bar);
         const int before = cpv.seq;
         cursor_advance(cpv, s_prefix, B, Hkv);
@@ -561,7 +573,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   };
 
   for (int i = 0; i < n_tiles; ++i) {
-    const int stage = i % S;
+    const int vstage = i % SV;
     if (!mbar_wait_bounded(&s_full[i & 1], (uint32_t)((i >> 1) & 1)) && st == 0)
       raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
     tc_fence_after();
@@ -648,18 +660,18 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     }
     // ---- keys past the context in the last tile may hold stale bytes: zero those V rows
     if (t0 + TK > ctx) {
-      // With one stage the previous tile's V may still be in flight here, and the
+      // With one V stage the previous tile's V may still be in flight here, and the
       // V barrier's parity would then name an earlier phase: wait until the
       // previous tile's P.V is done (its V landed and consumed) before asking for
-      // this tile's V. With two or more stages the V of tile i - S has landed
+      // this tile's V. With two or more V stages the V of tile i - SV has landed
       // before QK of tile i is issued, so the parity is already unambiguous.
-      if constexpr (S == 1) {
+      if constexpr (SV == 1) {
         if (i > 0) wait_pv(i - 1);
       }
-      if (!mbar_wait_bounded(&full_v[stage], (uint32_t)((i / S) & 1)) && st == 0)
+      if (!mbar_wait_bounded(&full_v[vstage], (uint32_t)((i / SV) & 1)) && st == 0)
         raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);  // V of this tile has landed
       const int valid = ctx - t0;
-      uint8_t* vt = ring + stage * C::STAGE_BYTES + C::TILE_BYTES;
+      uint8_t* vt = ring + (S + vstage) * C::TILE_BYTES;
       for (int j = st; j < (TK - valid) * (D / 8); j += kSoftmaxThreads) {
         const int row = valid + j / (D / 8), ch = j % (D / 8);
         *reinterpret_cast<uint4*>(vt + (ch >> 3) * TK * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4)) =
@@ -712,7 +724,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
       fin.c0 = (int)(u0 / W);
       fin.nseg = (int)((u0 + cu.ntiles - 1) / W) - fin.c0 + 1;
       fin.slot = piece_slot((int)blockIdx.x, fin.c0, u0, W);
-      fin_bad = s_bad[cu.seq % S] != 0;  // every tile of the unit in range is loaded by now
+      fin_bad = s_bad[cu.seq & 7] != 0;  // every tile of the unit in range is loaded by now
       pending = true;
     }
     const int before = cu.seq;
