@@ -195,7 +195,8 @@ typedef struct spec_attn_plan {
   int32_t kernel;        /* SPEC_ATTN_KERNEL_*                                   */
   int32_t m_tiles;       /* (k_draft+1)*G packed rows padded to 16*m_tiles: 1, 2, 4 */
   int32_t keys_per_tile; /* keys per K/V pipeline stage                          */
-  int32_t stages;        /* K/V pipeline stages in shared memory                 */
+  int32_t stages;        /* K/V pipeline stages in shared memory (tcgen05: K ring
+                            stages; its V ring has as many, or two with three K) */
   int32_t p_buffers;     /* tcgen05: shared-memory buffers of P; 0 for mma.sync  */
   int32_t ctas_per_sm;   /* resident CTAs per SM the kernel is compiled for      */
 } spec_attn_plan;
