@@ -88,22 +88,24 @@ def _plan(lib, kd=3, **kw):
 def test_attention_plan_without_a_device(lib, monkeypatch):
     """Plans that need no device query: the mma.sync instances, whose tile settings
     follow from the shared-memory arithmetic of their configuration (16 rows at
-    D = 128: 64-key stages of 32 KB, three stages, two CTAs per SM; 32 rows at
-    D = 256: 32-key stages, one CTA per SM, so a fourth stage)."""
+    D = 128: 64-key stages of 32 KB, three stages, two CTAs per SM; 24 rows at
+    D = 256, forced onto mma.sync: 32-key stages, one CTA per SM, so a fourth
+    stage). Head dims 128 and 256 with 17 or more rows take the tcgen05 kernel
+    when its shared-memory plan fits, which asks the device: no device here."""
     monkeypatch.delenv("SPEC_ATTN_KERNEL", raising=False)
     rc, p = _plan(lib, num_q_heads=32, num_kv_heads=8)  # (3+1) * 4 = 16 rows
     assert rc == 0
     assert p == dict(kernel=1, m_tiles=1, keys_per_tile=64, stages=3, p_buffers=0, ctas_per_sm=2)
-    rc, p = _plan(lib, num_q_heads=24, num_kv_heads=4, head_dim=256)  # 24 rows
-    assert rc == 0
-    assert p == dict(kernel=1, m_tiles=2, keys_per_tile=32, stages=4, p_buffers=0, ctas_per_sm=1)
     rc, p = _plan(lib, num_q_heads=4, num_kv_heads=1, head_dim=64)
     assert rc == 0 and p["kernel"] == 1 and p["m_tiles"] == 1 and p["keys_per_tile"] == 64
-    # D = 128 with 17+ rows asks the device for its shared-memory limit: no device here
     assert _plan(lib, kd=7, num_q_heads=64, num_kv_heads=8)[0] == -3
+    assert _plan(lib, num_q_heads=24, num_kv_heads=4, head_dim=256)[0] == -3
     monkeypatch.setenv("SPEC_ATTN_KERNEL", "mma")
     rc, p = _plan(lib, kd=7, num_q_heads=64, num_kv_heads=8)  # 64 rows, forced onto mma.sync
     assert rc == 0 and p["kernel"] == 1 and p["m_tiles"] == 4
+    rc, p = _plan(lib, num_q_heads=24, num_kv_heads=4, head_dim=256)  # 24 rows, forced onto mma.sync
+    assert rc == 0
+    assert p == dict(kernel=1, m_tiles=2, keys_per_tile=32, stages=4, p_buffers=0, ctas_per_sm=1)
     monkeypatch.delenv("SPEC_ATTN_KERNEL")
     assert lib.spec_verify_attention_plan(ctypes.byref(_desc()), 3, None) == -1
     assert _plan(lib, num_q_heads=7)[0] == -1
