@@ -250,7 +250,7 @@ int spec_verify_attention_plan(const spec_attn_desc* d, int32_t k_draft, spec_at
  * Device errors: a row with a draft token outside [0, V) (SPEC_DEVERR_TOKEN),
  * a sampling row with temperature not > 0 (SPEC_DEVERR_TEMPERATURE), or a mode
  * other than 0/1 (SPEC_DEVERR_MODE) gets out_tokens all -1 and accept_len -1.
- * Supported: k_draft <= 31; vocab <= 16 * 49152.
+ * Supported: k_draft <= 31; vocab <= 2^30.
  */
 int spec_accept(const float* target_logits, const int32_t* draft_tokens,
                 const float* draft_probs, uint64_t philox_seed, const int32_t* mode,

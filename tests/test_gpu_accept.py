@@ -225,8 +225,9 @@ def test_accept_invalid_rows_flagged(sv):
 
 @pytest.mark.parametrize("vocab", [1000, 1001], ids=["aligned", "unaligned"])
 def test_accept_many_waves(sv, oracle_mod, vocab):
-    """1400 rows of a 1000-word vocabulary (one CTA per row) run in several waves
-    of resident CTAs; aligned rows (bulk copies) and unaligned ones (plain loads)."""
+    """1400 rows of a 1000-word vocabulary (one CTA per row): more rows than the
+    device holds at once, so each CTA walks several rows; aligned rows (16-byte
+    loads) and unaligned ones (scalar loads)."""
     w = wl.WORKLOADS["tiny"].replace(vocab=vocab, batch=1400, mode="mixed")
     inp = wl.make_accept_inputs(w, device=DEV)
     tok, alen, err = run_accept(sv, inp, inp["mode"])
@@ -240,7 +241,7 @@ def test_accept_many_waves(sv, oracle_mod, vocab):
 def test_accept_all_zero_residual_races_over_p(sv, oracle_mod, batch):
     """Draft probabilities at twice the target's make max(0, p - q) zero everywhere
     while drafts are still rejected (whenever u >= 1/2): the correction token is
-    then drawn from p itself (the slice is reloaded over the residual weights)."""
+    then drawn from p itself (a second race over the same slice)."""
     w = wl.WORKLOADS["tiny"].replace(vocab=1000, batch=batch, mode="sample")
     inp = wl.make_accept_inputs(w, device=DEV)
     T = inp["temperature"].view(-1, 1, 1)
