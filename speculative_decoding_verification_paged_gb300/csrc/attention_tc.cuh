@@ -529,43 +529,68 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
       }
       named_sync(kBarSoftmax, kSoftmaxThreads);
       // out[row] = sum_pieces 2^(lse - M) * partial / sum_pieces 2^(lse - M), merged
-      // online; a thread's float4 columns load up to four pieces at a time
-      for (int idx = st; idx < p.n_rows * (D / 4); idx += kSoftmaxThreads) {
-        const int r = idx / (D / 4), d4 = idx - r * (D / 4);
-        float M = -INFINITY, wsum = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        bool nan = false;
-        for (int sg0 = 0; sg0 < F.nseg; sg0 += 4) {
-          float l[4];
-          float4 v[4];
+      // online; a thread takes kB float4 columns at once and loads up to kP pieces
+      // of all of them together, so kP pieces of kB columns cost one L2 round trip
+      constexpr int kB = 4, kP = 4;
+      for (int base = st; base < p.n_rows * (D / 4); base += kB * kSoftmaxThreads) {
+        float M[kB], wsum[kB];
+        float4 acc[kB];
+        bool nan[kB];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            l[u] = -INFINITY;
-            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (sg0 + u < F.nseg) {
-              const int64_t slot = piece_slot(F.c0 + sg0 + u, F.c0, F.u0, W);
-              l[u] = __ldcg(p.lse + slot * p.n_rows + r);
-              v[u] = __ldcg(reinterpret_cast<const float4*>(p.opart + (slot * p.n_rows + r) * D) + d4);
+        for (int c = 0; c < kB; ++c) {
+          M[c] = -INFINITY;
+          wsum[c] = 0.f;
+          acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          nan[c] = false;
+        }
+        for (int sg0 = 0; sg0 < F.nseg; sg0 += kP) {
+          float l[kP][kB];
+          float4 v[kP][kB];
+#pragma unroll
+          for (int u = 0; u < kP; ++u) {
+            const bool have = sg0 + u < F.nseg;
+            const int64_t slot = have ? piece_slot(F.c0 + sg0 + u, F.c0, F.u0, W) : 0;
+#pragma unroll
+            for (int c = 0; c < kB; ++c) {
+              const int idx = base + c * kSoftmaxThreads;
+              l[u][c] = -INFINITY;
+              v[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (have && idx < p.n_rows * (D / 4)) {
+                const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+                l[u][c] = __ldcg(p.lse + slot * p.n_rows + r);
+                v[u][c] = __ldcg(reinterpret_cast<const float4*>(p.opart + (slot * p.n_rows + r) * D) + d4);
+              }
             }
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            nan |= l[u] != l[u];
-            if (l[u] == -INFINITY) continue;
-            const float Mn = fmaxf(M, l[u]);
-            const float a = exp2f(M - Mn), wgt = exp2f(l[u] - Mn);
-            acc.x = acc.x * a + wgt * v[u].x;
-            acc.y = acc.y * a + wgt * v[u].y;
-            acc.z = acc.z * a + wgt * v[u].z;
-            acc.w = acc.w * a + wgt * v[u].w;
-            wsum = wsum * a + wgt;
-            M = Mn;
+          for (int u = 0; u < kP; ++u) {
+#pragma unroll
+            for (int c = 0; c < kB; ++c) {
+              const float lv = l[u][c];
+              nan[c] |= lv != lv;
+              if (!(lv > -INFINITY)) continue;
+              const float Mn = fmaxf(M[c], lv);
+              const float a = exp2f(M[c] - Mn), wgt = exp2f(lv - Mn);
+              acc[c].x = acc[c].x * a + wgt * v[u][c].x;
+              acc[c].y = acc[c].y * a + wgt * v[u][c].y;
+              acc[c].z = acc[c].z * a + wgt * v[u][c].z;
+              acc[c].w = acc[c].w * a + wgt * v[u][c].w;
+              wsum[c] = wsum[c] * a + wgt;
+              M[c] = Mn;
+            }
           }
         }
-        const float sc = (nan || wsum == 0.f) ? 0.f : 1.f / wsum;  // 0: invalid piece or no key seen
-        const float4 o = sc == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                   : make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
-        __stcg(reinterpret_cast<float4*>(p.out + s_rowoff[r]) + d4, o);
+#pragma unroll
+        for (int c = 0; c < kB; ++c) {
+          const int idx = base + c * kSoftmaxThreads;
+          if (idx < p.n_rows * (D / 4)) {
+            const int r = idx / (D / 4), d4 = idx - r * (D / 4);
+            const float sc = (nan[c] || wsum[c] == 0.f) ? 0.f : 1.f / wsum[c];  // 0: invalid piece or no key seen
+            const float4 o = sc == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                       : make_float4(acc[c].x * sc, acc[c].y * sc, acc[c].z * sc, acc[c].w * sc);
+            __stcg(reinterpret_cast<float4*>(p.out + s_rowoff[r]) + d4, o);
+          }
+        }
       }
       if (st == 0) p.counters[F.b * Hkv + F.g] = 0;
       named_sync(kBarSoftmax, kSoftmaxThreads);  // s_rowoff is reused
