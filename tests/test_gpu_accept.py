@@ -278,3 +278,21 @@ def test_binding_rejects_tensors_the_kernels_cannot_use(sv):
             sv.spec_accept(*args, stream=other)
     sv.spec_accept(*args, dev_err=torch.zeros(1, dtype=torch.int32, device=DEV))  # the valid call still works
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("vocab", [40000, 40001], ids=["aligned", "unaligned"])
+def test_accept_every_launch_configuration(sv, oracle_mod, monkeypatch, vocab):
+    """Every (threads per CTA, CTAs per cluster) the launch can pick, forced in turn
+    through SPEC_ACCEPT_CONFIG on one mixed case of 200 rows: small clusters hold
+    every row at once, 16-CTA clusters walk several rows each. Each result must
+    match the oracle like the launch's own choice does."""
+    w = wl.WORKLOADS["serving128"].replace(vocab=vocab, batch=200, mode="mixed")
+    inp = wl.make_accept_inputs(w, device=DEV)
+    rt, ra, margin, gap, rc = oracle_accept(oracle_mod, inp, inp["mode"])
+    assert rc == 0
+    for threads in (128, 256):
+        for csize in (1, 2, 4, 8, 16):
+            monkeypatch.setenv("SPEC_ACCEPT_CONFIG", f"{threads}x{csize}")
+            tok, alen, err = run_accept(sv, inp, inp["mode"])
+            bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
+            assert err == 0 and bad == 0, (threads, csize, err, bad)
