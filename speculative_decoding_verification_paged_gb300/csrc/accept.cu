@@ -544,10 +544,14 @@ static int resident_clusters(int dev, int li) {
 // Threads per CTA and cluster size. Among the configurations whose slices give
 // every thread at least one float4 group (and the one-CTA clusters), prefer
 // those that hold every row of the batch at once, and among them the fewest
-// groups per thread and position (the shortest chain per row), then the
-// smallest cluster; when none holds the batch, the one closest to 32 groups
-// per thread (each cluster walks several rows). SPEC_ACCEPT_CONFIG="TxC"
-// (T in {128, 256}, C a power of two <= 16) forces one.
+// groups per thread and position (the shortest chain per row); at equal
+// threads per row, 128-thread CTAs (finer placement over the SMs) unless they
+// need 16-CTA clusters (the cluster barrier and exchange grow with the
+// cluster), then the smallest cluster. Measured: serving128 49.6 us with 8 x
+// 128 against 52.1 with 4 x 256; hybrid_gdn 57.0 with 8 x 256 against 57.7
+// with 16 x 128. When none holds the batch, the one closest to 32 groups per
+// thread (each cluster walks several rows). SPEC_ACCEPT_CONFIG="TxC" (T in
+// {128, 256}, C a power of two <= 16) forces one.
 static bool choose_config(int dev, int batch, int vocab, Config& out) {
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
@@ -571,7 +575,8 @@ static bool choose_config(int dev, int batch, int vocab, Config& out) {
       const long groups = ((slice / 4) + T - 1) / T;  // float4 groups per thread and position
       const bool fits = clusters >= batch;
       const long dist = groups > 32 ? groups - 32 : 32 - groups;
-      const long score = fits ? (groups * 64 + li) * 2 + (T == 256 ? 0 : 1)
+      const bool preferred = T == 128 ? c <= 8 : 2 * c > 8;  // see above
+      const long score = fits ? groups * 1024 + (preferred ? 0 : 512) + li * 2 + (T == 256 ? 0 : 1)
                               : (1L << 40) + ((dist * 64 + li) * 2 + (T == 128 ? 0 : 1));
       if (!have || score < best_score) {
         have = true;
