@@ -122,14 +122,14 @@ __device__ __forceinline__ void vi_combine(float& v, int& i, float ov, int oi) {
   }
 }
 
-// Largest of three (one instruction on sm_100 and later).
+// Largest of three (the three-input PTX form, sm_100 and later).
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
 
-// Approximate reciprocal (the MUFU unit alone).
+// Approximate reciprocal (rcp.approx: no refinement steps).
 __device__ __forceinline__ float fast_rcp(float x) {
   float r;
   asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(r) : "f"(x));
@@ -161,7 +161,6 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
   const int ngroups = (n + 3) >> 2;
   const bool vec = p.vec != 0;
   const int nparts = csize * kWarps;
-  const float4 kNegInf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   const float4 kZero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   int xs = 0;           // exchanges so far (slot parity)
   bool joined = false;  // the start-up cluster barrier was waited on
