@@ -296,3 +296,18 @@ def test_accept_every_launch_configuration(sv, oracle_mod, monkeypatch, vocab):
             tok, alen, err = run_accept(sv, inp, inp["mode"])
             bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
             assert err == 0 and bad == 0, (threads, csize, err, bad)
+
+
+@pytest.mark.parametrize("vocab", [1, 2, 3, 5, 7])
+@pytest.mark.parametrize("k_draft", [1, 3])
+def test_accept_vocabularies_smaller_than_a_few_groups(sv, oracle_mod, vocab, k_draft):
+    """Vocabularies of fewer than two float4 groups (one CTA, most threads hold no
+    logit, scalar loads past the row's end filled), with one or three drafts."""
+    w = wl.WORKLOADS["tiny"].replace(vocab=vocab, k_draft=k_draft, batch=64, mode="mixed")
+    inp = wl.make_accept_inputs(w, device=DEV)
+    tok, alen, err = run_accept(sv, inp, inp["mode"])
+    rt, ra, margin, gap, rc = oracle_accept(oracle_mod, inp, inp["mode"])
+    assert err == 0 and rc == 0
+    bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
+    assert bad == 0
+    assert np.all((tok[:, : k_draft + 1] >= -1) & (tok[:, : k_draft + 1] < vocab))
