@@ -311,3 +311,26 @@ def test_accept_vocabularies_smaller_than_a_few_groups(sv, oracle_mod, vocab, k_
     bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
     assert bad == 0
     assert np.all((tok[:, : k_draft + 1] >= -1) & (tok[:, : k_draft + 1] < vocab))
+
+
+def test_accept_random_shapes(sv, oracle_mod):
+    """Seeded random shapes: batch 1-160, vocabulary 1-90000 (aligned or not), 1-12
+    drafts, noise and temperature ranges, mixed modes, with and without draft
+    probabilities; every one against the oracle."""
+    rng = np.random.default_rng(2027)
+    for case in range(14):
+        batch = int(rng.integers(1, 161))
+        vocab = int(rng.choice([int(rng.integers(1, 64)), int(rng.integers(64, 4096)), int(rng.integers(4096, 90000))]))
+        k = int(rng.integers(1, 13))
+        lo = float(rng.uniform(0.3, 1.0))
+        w = wl.WORKLOADS["tiny"].replace(
+            name=f"random{case}", batch=batch, vocab=vocab, k_draft=k, mode="mixed",
+            logit_sigma=float(rng.uniform(0.5, 4.0)), noise_sigma=float(rng.uniform(0.1, 2.0)),
+            temperature=(lo, lo + float(rng.uniform(0.0, 1.0))), seed=100 + case)
+        inp = wl.make_accept_inputs(w, device=DEV)
+        probs = "given" if case % 3 else "none"
+        tok, alen, err = run_accept(sv, inp, inp["mode"], probs=probs)
+        rt, ra, margin, gap, rc = oracle_accept(oracle_mod, inp, inp["mode"], probs=probs)
+        assert err == 0 and rc == 0, (case, batch, vocab, k)
+        bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
+        assert bad == 0, (case, batch, vocab, k, probs)
