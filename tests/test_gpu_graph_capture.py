@@ -4,7 +4,8 @@ A serving engine may capture its verify step before it ever ran it eagerly. The
 first call of each entry point does one-time launch set-up (function attributes,
 occupancy queries, the tensor-map encoder); none of it may break the capture.
 A fresh process captures spec_verify_attention and spec_accept as its first
-calls, replays the graph and compares the results with eager calls.
+calls (and, for the hybrid workload, the gated delta rule and the commit),
+replays the graphs and compares the results with eager calls.
 """
 
 import os
@@ -44,8 +45,33 @@ for name in ("llama8b_eagle3", "hybrid_gdn"):  # mma.sync and tcgen05 attention
                                  out, workspace=ws, dev_err=err)
         sv.spec_accept(acc["target_logits"], acc["draft_tokens"], acc["draft_probs"], acc["philox_seed"],
                        acc["mode"], acc["temperature"], toks, alen, dev_err=err)
+    # the hybrid step's other calls: the gated delta rule of one layer and the
+    # commit of its checkpoint of the accepted prefix
+    if name == "hybrid_gdn":
+        w1 = w.replace(gdn_layers=1)
+        x = wl.make_gdn_verify_inputs(w1, device=dev, layers=1)
+        q, k, v, gg, beta = (x[f][0] for f in ("q", "k", "v", "g", "beta"))
+        Bq, Rq, H, dk = q.shape
+        dv = v.shape[3]
+        snaps = torch.zeros((Bq, Rq, H, dv, dk), device=dev)
+        gout = torch.empty((Bq, Rq, H, dv), device=dev)
+        live = torch.zeros((1, Bq, H * dv * dk), device=dev)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=side):
+            sv.spec_gdn_verify(q, k, v, gg, beta, x["state"][0], snaps, gout, x["scale"], dev_err=err)
+            sv.spec_commit_state(snaps.view(1, Bq, Rq, H * dv * dk), alen, live, dev_err=err)
     g.replay()
+    if name == "hybrid_gdn":
+        g2.replay()
     torch.cuda.synchronize()
+    if name == "hybrid_gdn":
+        snaps_e = torch.zeros_like(snaps)
+        gout_e = torch.empty_like(gout)
+        live_e = torch.zeros_like(live)
+        sv.spec_gdn_verify(q, k, v, gg, beta, x["state"][0], snaps_e, gout_e, x["scale"], dev_err=err)
+        sv.spec_commit_state(snaps_e.view(1, Bq, Rq, H * dv * dk), alen, live_e, dev_err=err)
+        torch.cuda.synchronize()
+        assert torch.equal(snaps, snaps_e) and torch.equal(gout, gout_e) and torch.equal(live, live_e)
     out2 = torch.empty_like(out)
     toks2 = torch.empty_like(toks)
     alen2 = torch.empty_like(alen)
