@@ -266,3 +266,17 @@ def test_attention_minimal_context_row0_is_v0(sv):
         v0 = a["v_cache"][phys, 0].float()  # [Hkv, D]
         for h in range(8):
             assert torch.allclose(out[b, 0, h], v0[h // 4], atol=1e-6, rtol=0)
+
+
+@pytest.mark.parametrize("Hq,ctx", [(16, 60000), (4, 60000), (16, 700)], ids=["rows64", "rows16", "rows64_short"])
+def test_attention_one_unit_split_over_every_cta(sv, oracle_mod, attn_kernel, Hq, ctx):
+    """One sequence with one kv head: its single unit is cut into a piece per CTA
+    (over a hundred for a 60000-token context), and the last CTA to arrive merges
+    them all; a short context gives a few pieces of one tile each."""
+    w = wl.Workload(name="one_unit", batch=1, ctx_lens=(ctx,), block_size=128, num_q_heads=Hq, num_kv_heads=1,
+                    head_dim=128, k_draft=3, seed=ctx % 101 + Hq)
+    a = wl.make_attention_inputs(w, device=DEV)
+    out, err = run_attention(sv, a, w)
+    assert err == 0
+    mx, rel = attention_errors(out.cpu().numpy(), oracle_attention_for(oracle_mod, a))
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
