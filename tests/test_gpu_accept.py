@@ -334,3 +334,25 @@ def test_accept_random_shapes(sv, oracle_mod):
         assert err == 0 and rc == 0, (case, batch, vocab, k)
         bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
         assert bad == 0, (case, batch, vocab, k, probs)
+
+
+def test_accept_extreme_temperatures(sv, oracle_mod):
+    """Per-row temperatures from 0.001 (p one-hot for practical purposes: most
+    exponentials underflow) to 1000 (p nearly flat over the vocabulary)."""
+    temps = [1e-3, 0.05, 0.3, 1.0, 4.0, 20.0, 1000.0]
+    B = 7 * len(temps)
+    w = wl.WORKLOADS["tiny"].replace(batch=B, vocab=5000, k_draft=3, mode="sample", logit_sigma=3.0, seed=77)
+    inp = wl.make_accept_inputs(w, device=DEV)
+    T = torch.tensor([temps[i % len(temps)] for i in range(B)], dtype=torch.float32, device=DEV)
+    inp["temperature"] = T
+    # draft probabilities at each row's own temperature, drafts drawn from them
+    g = torch.Generator(device=DEV).manual_seed(5)
+    dl = inp["target_logits"][:, :3, :] + torch.randn((B, 3, 5000), generator=g, device=DEV)
+    inp["draft_probs"] = torch.softmax(dl / T.view(B, 1, 1), dim=-1).contiguous()
+    inp["draft_tokens"] = torch.multinomial(inp["draft_probs"].view(B * 3, 5000), 1, generator=g).view(B, 3) \
+        .to(torch.int32).contiguous()
+    tok, alen, err = run_accept(sv, inp, inp["mode"])
+    rt, ra, margin, gap, rc = oracle_accept(oracle_mod, inp, inp["mode"])
+    assert err == 0 and rc == 0
+    bad, _ = compare_accept(tok, alen, rt, ra, margin, gap)
+    assert bad == 0
