@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, MT>::MIN_BLOCKS) verify_atten
     const int bs = 1 << p.block_shift;
     const int BH = bs < TK ? bs : TK;  // rows per KV box
     const int pieces = TK / BH;
+    const uint64_t kv_pol = l2_evict_first_policy();  // K and V are read once
     Cursor ld = cursor_at(f0, s_prefix, B, Hkv);
     bool fresh = true;
     int win_b = -1, win_base = 0, win_val = 0;
@@ -169,8 +170,8 @@ __global__ void __launch_bounds__(kThreads, Cfg<D, MT>::MIN_BLOCKS) verify_atten
 #pragma unroll
           for (int sub = 0; sub < C::SUBS; ++sub) {
             const uint32_t off = sub * TK * 128 + pc * BH * 128;
-            tma_load_3d(kdst + off, &tm_k, sub * 64, g, zc[pc], &full[s]);
-            tma_load_3d(vdst + off, &tm_v, sub * 64, g, zc[pc], &full[s]);
+            tma_load_3d_hint(kdst + off, &tm_k, sub * 64, g, zc[pc], &full[s], kv_pol);
+            tma_load_3d_hint(vdst + off, &tm_v, sub * 64, g, zc[pc], &full[s], kv_pol);
           }
         }
       }

@@ -266,6 +266,9 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     const int bs = 1 << p.block_shift;
     const int BH = bs < TK ? bs : TK;
     const int pieces = TK / BH;
+    // K and V are read once: evict them first, so that the code of the unit-boundary
+    // and final paths, the block table and the queries stay in L2
+    const uint64_t kv_pol = l2_evict_first_policy();
     Cursor ld = cursor_at(f0, s_prefix, B, Hkv);
     bool fresh = true;
     int win_b = -1, win_base = 0, win_val = 0;
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
             if (pc >= pieces) break;
 #pragma unroll
             for (int sub = 0; sub < C::SUBS; ++sub)
-              tma_load_3d(kdst + sub * TK * 128 + pc * BH * 128, &tm_k, sub * 64, g, zc[pc], &full_k[s]);
+              tma_load_3d_hint(kdst + sub * TK * 128 + pc * BH * 128, &tm_k, sub * 64, g, zc[pc], &full_k[s], kv_pol);
           }
         }
       }
@@ -340,7 +343,8 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
           if (pc >= pieces) break;
 #pragma unroll
           for (int sub = 0; sub < C::SUBS; ++sub)
-            tma_load_3d(vdst + sub * TK * 128 + pc * BH * 128, &tm_v, sub * 64, g_prev, zprev[pc], &full_v[s]);
+            tma_load_3d_hint(vdst + sub * TK * 128 + pc * BH * 128, &tm_v, sub * 64, g_prev, zprev[pc], &full_v[s],
+                           kv_pol);
         }
       }
       __syncwarp();
@@ -458,12 +462,17 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
 
   // Write the finished unit piece: output rows (whole unit) or a normalised partial.
   // A unit split over several CTAs is merged by the last one to finish its piece.
+  // Where the rows fit the P buffers (free here: every P.V is done), they are
+  // staged there and written by bulk copies that one thread issues, so no
+  // softmax thread waits on thousands of scattered stores.
+  constexpr bool kStage = D <= NP * TK;  // N rows x D fp32 fit NP x (P_hi, P_lo)
+  float* s_inv = reinterpret_cast<float*>(s_rowoff);  // [64] 1 / row sum (staged form)
   auto epilogue = [&](const Fin& F) {
     {
       const float lsum = reduce_cols<CW, false>(l_part, lane);  // l_part is reset after this
       if (lane < CW) s_red[q4 * 64 + c0 + reduced_col<CW>(lane)] = lsum;
     }
-    if (F.complete && gt < CW && c0 + gt < p.n_rows) {
+    if (!kStage && F.complete && gt < CW && c0 + gt < p.n_rows) {
       const int r = c0 + gt, i = r / G, j = r - i * G;
       s_rowoff[r] = (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
     }
@@ -471,37 +480,89 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     const bool bad = fin_bad;
     const int d = q4 * 32 + lane;  // the O^T lane this thread reads (in each half)
     constexpr int CH = CW < 16 ? CW : 16;  // columns per step
-#pragma unroll
-    for (int c = 0; c < CW; c += CH) {
-      float inv[CH];
-#pragma unroll
-      for (int e = 0; e < CH; ++e) {
-        const int r = c0 + c + e;
+    if constexpr (kStage) {
+      // one thread per row: 1 / L into shared memory, and the piece's log-sum-exp
+      if (gt < CW) {
+        const int r = c0 + gt;
         const float L = s_red[r] + s_red[64 + r] + s_red[128 + r] + s_red[192 + r];
-        inv[e] = (L > 0.f && !bad) ? 1.f / L : 0.f;
-        if (!F.complete && q4 == 0 && lane == 0 && r < p.n_rows) {
-          float lse2 = L > 0.f ? m_get(c + e) + __log2f(L) : -INFINITY;
+        s_inv[r] = (L > 0.f && !bad) ? 1.f / L : 0.f;
+        if (!F.complete && r < p.n_rows) {
+          float m = 0.f;
+          if constexpr (kMaxInSmem) {
+            m = s_mrun[r];
+          } else {
+#pragma unroll
+            for (int e = 0; e < CW; ++e)
+              if (e == gt) m = m_reg[kMaxInSmem ? 0 : e];
+          }
+          float lse2 = L > 0.f ? m + __log2f(L) : -INFINITY;
           if (bad) lse2 = __int_as_float(0x7fc00000);
           __stcg(p.lse + (int64_t)F.slot * p.n_rows + r, lse2);
         }
       }
+      named_sync(bar_group, 128);
+      float* stage = reinterpret_cast<float*>(pbuf);  // [n_rows][D]
 #pragma unroll
-      for (int h = 0; h < C::HALVES; ++h) {
-        float ov[CH];
-        tmem_load_cols<CH>(tmem_o + (uint32_t)(h * N) + lane_off + c0 + c, ov);
+      for (int c = 0; c < CW; c += CH) {
+#pragma unroll
+        for (int hh = 0; hh < C::HALVES; ++hh) {
+          float ov[CH];
+          tmem_load_cols<CH>(tmem_o + (uint32_t)(hh * N) + lane_off + c0 + c, ov);
+#pragma unroll
+          for (int e = 0; e < CH; ++e) {
+            const int r = c0 + c + e;
+            if (r < p.n_rows) stage[r * D + hh * 128 + d] = ov[e] * s_inv[r];
+          }
+        }
+      }
+      fence_proxy_async_smem();  // the staged rows are read by the bulk copies
+      named_sync(kBarSoftmax, kSoftmaxThreads);
+      if (st == 0) {
+        const uint32_t src = smem_u32(stage);
+        if (F.complete) {
+          // rows i*G .. i*G + G - 1 are the G query heads of position i: contiguous in out
+          for (int i = 0; i < R; ++i)
+            bulk_s2g(p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G) * D,
+                     src + (uint32_t)(i * G * D * 4), (uint32_t)(G * D * 4));
+        } else {
+          bulk_s2g(p.opart + (int64_t)F.slot * p.n_rows * D, src, (uint32_t)(p.n_rows * D * 4));
+        }
+        bulk_commit();
+        bulk_wait_read();  // the P buffers are written again after the barrier below
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < CW; c += CH) {
+        float inv[CH];
 #pragma unroll
         for (int e = 0; e < CH; ++e) {
           const int r = c0 + c + e;
-          if (r < p.n_rows) {
-            const int64_t off = F.complete ? s_rowoff[r] : ((int64_t)F.slot * p.n_rows + r) * D;
-            __stcg((F.complete ? p.out : p.opart) + off + h * 128 + d, ov[e] * inv[e]);
+          const float L = s_red[r] + s_red[64 + r] + s_red[128 + r] + s_red[192 + r];
+          inv[e] = (L > 0.f && !bad) ? 1.f / L : 0.f;
+          if (!F.complete && q4 == 0 && lane == 0 && r < p.n_rows) {
+            float lse2 = L > 0.f ? m_get(c + e) + __log2f(L) : -INFINITY;
+            if (bad) lse2 = __int_as_float(0x7fc00000);
+            __stcg(p.lse + (int64_t)F.slot * p.n_rows + r, lse2);
+          }
+        }
+#pragma unroll
+        for (int hh = 0; hh < C::HALVES; ++hh) {
+          float ov[CH];
+          tmem_load_cols<CH>(tmem_o + (uint32_t)(hh * N) + lane_off + c0 + c, ov);
+#pragma unroll
+          for (int e = 0; e < CH; ++e) {
+            const int r = c0 + c + e;
+            if (r < p.n_rows) {
+              const int64_t off = F.complete ? s_rowoff[r] : ((int64_t)F.slot * p.n_rows + r) * D;
+              __stcg((F.complete ? p.out : p.opart) + off + hh * 128 + d, ov[e] * inv[e]);
+            }
           }
         }
       }
     }
     if (bad && st == 0) raise_error(p.dev_err, SPEC_DEVERR_BLOCK_ID);
     if (!F.complete) pend[n_pend++] = F;  // arrival and merge happen when the CTA is done
-    named_sync(kBarSoftmax, kSoftmaxThreads);  // s_red and s_rowoff are reused
+    named_sync(kBarSoftmax, kSoftmaxThreads);  // s_red, s_inv, s_rowoff and the P buffers are reused
   };
 
   // A unit split over several CTAs is merged by the last CTA to arrive on its
@@ -511,6 +572,10 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   auto arrive_and_merge = [&]() {
     named_sync(kBarSoftmax, kSoftmaxThreads);  // every partial store of the CTA is issued
     if (st == 0) {
+      if constexpr (kStage) {
+        bulk_wait_all();             // the staged partials are written
+        fence_proxy_async_global();  // ... before the release below
+      }
       __threadfence();  // release the partials
       int last[2] = {0, 0};
       for (int k = 0; k < n_pend; ++k)
@@ -762,6 +827,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   tc_fence_before();
   named_sync(kBarTail, 32 + kSoftmaxThreads);  // tensor memory may be released
   if (n_pend > 0) arrive_and_merge();
+  if (kStage && st == 0) bulk_wait_all();  // staged rows are written before the CTA exits
 }
 
 }  // namespace tc

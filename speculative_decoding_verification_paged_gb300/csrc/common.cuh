@@ -82,6 +82,19 @@ SPEC_DEVICE void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// Bulk shared -> global copy (no tensor map), tracked by this thread's bulk groups:
+// src/dst 16-byte aligned, bytes % 16 == 0.
+SPEC_DEVICE void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+SPEC_DEVICE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// This thread's committed bulk copies have read their shared-memory source.
+SPEC_DEVICE void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// This thread's committed bulk copies are complete (their writes performed).
+SPEC_DEVICE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+// Order async-proxy global accesses of this thread before its later generic ones.
+SPEC_DEVICE void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;\n" ::: "memory"); }
 // Plain arrival (count 1) on an mbarrier.
 SPEC_DEVICE void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
@@ -94,6 +107,22 @@ SPEC_DEVICE void tma_load_3d(uint32_t dst, const void* tensor_map, int c0, int c
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
       "[%5];\n" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+// L2 policy for data read once: its lines are the first to be evicted, so code,
+// tables and reused data stay in L2 while a stream passes through.
+SPEC_DEVICE uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+// tma_load_3d with an L2 cache policy for the copied lines.
+SPEC_DEVICE void tma_load_3d_hint(uint32_t dst, const void* tensor_map, int c0, int c1, int c2, uint64_t* bar,
+                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%2, %3, %4}], [%5], %6;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tensor_map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 // Order this thread's generic-proxy shared-memory writes before later async-proxy (TMA) writes.
