@@ -131,7 +131,10 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   using C = Cfg<D, MT>;
   constexpr int N = C::N, CW = C::CW;
   static_assert(SQ == 1 || SQ >= S, "a query buffer is reused only after the K stage that covers it");
-  static_assert(2 * S + 2 * SV + 2 + 2 + NP + 1 <= 64, "barriers fit their area");
+  static_assert(2 * S + 2 * SV + 2 + 2 + NP + 2 <= 64, "barriers fit their area");
+  // ring, query buffers and P buffers: contiguous, idle when split units are merged
+  constexpr uint32_t kMergeArea = (uint32_t)((S + SV) * C::TILE_BYTES + SQ * C::Q_BYTES + NP * 2 * C::P_BYTES);
+  static_assert(kMergeArea >= 2 * N * D * 4 + 512 + 16 + N * 4 + 16, "the merge holds its rows and one piece");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;                                // S K tiles, then SV V tiles
@@ -147,6 +150,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   uint64_t* p_full = s_full + 2;  // [2]: P of tile i written (one arrival per softmax warp)
   uint64_t* pv_done = p_full + 2; // [NP]: P.V of the tile that used P buffer j is complete
   uint64_t* fin_bar = pv_done + NP;
+  uint64_t* merge_bar = fin_bar + 1;  // pieces of a split unit landed (merge)
   float* s_red = reinterpret_cast<float*>(full_k + 64);   // [4][64] per-quarter row reductions
   float* s_mrun = s_red + 4 * 64;                         // [64] running row max (64-row tiles)
   int64_t* s_rowoff = reinterpret_cast<int64_t*>(s_mrun + 64);  // [64] output offset of each row
@@ -220,6 +224,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
       }
       for (int j = 0; j < NP; ++j) mbar_init(&pv_done[j], 1);
       mbar_init(fin_bar, 1);
+      mbar_init(merge_bar, 1);
       fence_mbar_init();
     }
     __syncthreads();
@@ -450,6 +455,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   bool cu_fresh = true, from_zero = true, pending = false, fin_bad = false;
   Fin fin;
   Fin pend[2];     // pieces of split units, merged when the CTA is done
+  int merge_phase = 0;
   int n_pend = 0;
   int ctx = 0, prefix_len = 0;
 
@@ -588,77 +594,87 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     for (int k = 0; k < n_pend; ++k) {
       if (!s_misc[8 + k]) continue;
       const Fin& F = pend[k];
-      if (st < p.n_rows) {
-        const int r = st, i = r / G, j = r - i * G;
-        s_rowoff[r] = (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G + j) * D;
+      // out[row] = sum_pieces w_p[row] * partial_p[row], w_p = 2^(lse_p - M) / sum 2^(lse - M).
+      // The K/V ring, query and P buffers are idle now and form one contiguous area:
+      // [out rows][row max, 1/sum][chunk weights][chunk pieces]. Pieces arrive by bulk
+      // copies, a chunk at a time, and the merged rows leave the same way.
+      const int nr = p.n_rows;
+      const uint32_t piece_bytes = (uint32_t)(nr * D * 4);
+      float* ostage = reinterpret_cast<float*>(ring);
+      float* rmax = ostage + nr * D;
+      float* rinv = rmax + 64;
+      float* wchunk = rinv + 64;
+      const int cap = (int)((kMergeArea - piece_bytes - 512 - 16) / (piece_bytes + (uint32_t)nr * 4));
+      uint8_t* pieces = reinterpret_cast<uint8_t*>(ring) + ((kMergeArea - (uint32_t)cap * piece_bytes) & ~15u);
+      if (st == 0) bulk_wait_read();  // the previous merge's rows have left the area
+      if (st < nr) {
+        // one thread per row: running max and sum of 2^lse over the pieces
+        const int r = st;
+        float M = -INFINITY, ws = 0.f;
+        bool nan = false;
+        for (int sg0 = 0; sg0 < F.nseg; sg0 += 4) {
+          float l[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            l[u] = sg0 + u < F.nseg ? __ldcg(p.lse + (int64_t)piece_slot(F.c0 + sg0 + u, F.c0, F.u0, W) * nr + r)
+                                    : -INFINITY;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            nan |= l[u] != l[u];
+            if (!(l[u] > -INFINITY)) continue;
+            const float Mn = fmaxf(M, l[u]);
+            ws = ws * exp2f(M - Mn) + exp2f(l[u] - Mn);
+            M = Mn;
+          }
+        }
+        rmax[r] = M;
+        rinv[r] = (nan || ws == 0.f) ? 0.f : 1.f / ws;  // 0: invalid piece or no key seen
       }
       named_sync(kBarSoftmax, kSoftmaxThreads);
-      // out[row] = sum_pieces 2^(lse - M) * partial / sum_pieces 2^(lse - M), merged
-      // online; a thread takes kB float4 columns at once and loads up to kP pieces
-      // of all of them together, so kP pieces of kB columns cost one L2 round trip
-      constexpr int kB = 4, kP = 4;
-      for (int base = st; base < p.n_rows * (D / 4); base += kB * kSoftmaxThreads) {
-        float M[kB], wsum[kB];
-        float4 acc[kB];
-        bool nan[kB];
-#pragma unroll
-        for (int c = 0; c < kB; ++c) {
-          M[c] = -INFINITY;
-          wsum[c] = 0.f;
-          acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-          nan[c] = false;
+      for (int p0 = 0; p0 < F.nseg; p0 += cap) {
+        const int np_ = min(cap, F.nseg - p0);
+        if (st == 0) {
+          fence_proxy_async_global();  // the acquired pieces are read by the async proxy
+          mbar_arrive_expect_tx(merge_bar, (uint32_t)np_ * piece_bytes);
+          for (int q = 0; q < np_; ++q)
+            bulk_g2s(smem_u32(pieces + q * piece_bytes),
+                     p.opart + (int64_t)piece_slot(F.c0 + p0 + q, F.c0, F.u0, W) * nr * D, piece_bytes, merge_bar);
         }
-        for (int sg0 = 0; sg0 < F.nseg; sg0 += kP) {
-          float l[kP][kB];
-          float4 v[kP][kB];
-#pragma unroll
-          for (int u = 0; u < kP; ++u) {
-            const bool have = sg0 + u < F.nseg;
-            const int64_t slot = have ? piece_slot(F.c0 + sg0 + u, F.c0, F.u0, W) : 0;
-#pragma unroll
-            for (int c = 0; c < kB; ++c) {
-              const int idx = base + c * kSoftmaxThreads;
-              l[u][c] = -INFINITY;
-              v[u][c] = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (have && idx < p.n_rows * (D / 4)) {
-                const int r = idx / (D / 4), d4 = idx - r * (D / 4);
-                l[u][c] = __ldcg(p.lse + slot * p.n_rows + r);
-                v[u][c] = __ldcg(reinterpret_cast<const float4*>(p.opart + (slot * p.n_rows + r) * D) + d4);
-              }
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < kP; ++u) {
-#pragma unroll
-            for (int c = 0; c < kB; ++c) {
-              const float lv = l[u][c];
-              nan[c] |= lv != lv;
-              if (!(lv > -INFINITY)) continue;
-              const float Mn = fmaxf(M[c], lv);
-              const float a = exp2f(M[c] - Mn), wgt = exp2f(lv - Mn);
-              acc[c].x = acc[c].x * a + wgt * v[u][c].x;
-              acc[c].y = acc[c].y * a + wgt * v[u][c].y;
-              acc[c].z = acc[c].z * a + wgt * v[u][c].z;
-              acc[c].w = acc[c].w * a + wgt * v[u][c].w;
-              wsum[c] = wsum[c] * a + wgt;
-              M[c] = Mn;
-            }
-          }
+        for (int t = st; t < np_ * nr; t += kSoftmaxThreads) {
+          const int q = t / nr, r = t - q * nr;
+          const float lv = __ldcg(p.lse + (int64_t)piece_slot(F.c0 + p0 + q, F.c0, F.u0, W) * nr + r);
+          wchunk[t] = (rinv[r] == 0.f || !(lv > -INFINITY)) ? 0.f : exp2f(lv - rmax[r]) * rinv[r];
         }
-#pragma unroll
-        for (int c = 0; c < kB; ++c) {
-          const int idx = base + c * kSoftmaxThreads;
-          if (idx < p.n_rows * (D / 4)) {
-            const int r = idx / (D / 4), d4 = idx - r * (D / 4);
-            const float sc = (nan[c] || wsum[c] == 0.f) ? 0.f : 1.f / wsum[c];  // 0: invalid piece or no key seen
-            const float4 o = sc == 0.f ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                       : make_float4(acc[c].x * sc, acc[c].y * sc, acc[c].z * sc, acc[c].w * sc);
-            __stcg(reinterpret_cast<float4*>(p.out + s_rowoff[r]) + d4, o);
+        named_sync(kBarSoftmax, kSoftmaxThreads);  // chunk weights are visible
+        if (!mbar_wait_bounded(merge_bar, (uint32_t)(merge_phase & 1)) && st == 0)
+          raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
+        ++merge_phase;
+        for (int idx = st; idx < nr * (D / 4); idx += kSoftmaxThreads) {
+          const int r = idx / (D / 4);
+          float4 a = p0 == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<const float4*>(ostage)[idx];
+          for (int q = 0; q < np_; ++q) {
+            const float w = wchunk[q * nr + r];
+            if (w == 0.f) continue;  // an invalid piece, or one that saw no key of the row
+            const float4 v = reinterpret_cast<const float4*>(pieces + q * piece_bytes)[idx];
+            a.x += w * v.x;
+            a.y += w * v.y;
+            a.z += w * v.z;
+            a.w += w * v.w;
           }
+          reinterpret_cast<float4*>(ostage)[idx] = a;
         }
+        named_sync(kBarSoftmax, kSoftmaxThreads);  // the chunk is consumed
       }
-      if (st == 0) p.counters[F.b * Hkv + F.g] = 0;
-      named_sync(kBarSoftmax, kSoftmaxThreads);  // s_rowoff is reused
+      fence_proxy_async_smem();  // the merged rows are read by the bulk copies
+      named_sync(kBarSoftmax, kSoftmaxThreads);
+      if (st == 0) {
+        p.counters[F.b * Hkv + F.g] = 0;
+        // rows i*G .. i*G + G - 1 are the G query heads of position i: contiguous in out
+        for (int i = 0; i < R; ++i)
+          bulk_s2g(p.out + (((int64_t)F.b * R + i) * p.num_q_heads + F.g * G) * D,
+                   smem_u32(ostage) + (uint32_t)(i * G * D * 4), (uint32_t)(G * D * 4));
+        bulk_commit();
+      }
     }
   };
 
@@ -827,7 +843,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   tc_fence_before();
   named_sync(kBarTail, 32 + kSoftmaxThreads);  // tensor memory may be released
   if (n_pend > 0) arrive_and_merge();
-  if (kStage && st == 0) bulk_wait_all();  // staged rows are written before the CTA exits
+  if (st == 0) bulk_wait_all();  // staged rows are written before the CTA exits
 }
 
 }  // namespace tc
