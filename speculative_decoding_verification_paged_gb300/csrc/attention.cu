@@ -141,7 +141,8 @@ struct Settings {
 };
 
 template <typename Kern>
-static int settings_for(LaunchMemo& memo, Kern kern, size_t smem, int threads, bool one_per_sm, Settings* st) {
+static int settings_for(LaunchMemo& memo, Kern kern, size_t smem, int threads, bool one_per_sm, int max_grid,
+                        Settings* st) {
   const int dev = current_device();
   if (dev < 0) return SPEC_ERR_LAUNCH;
   std::lock_guard<std::mutex> lock(memo.mu);
@@ -152,7 +153,7 @@ static int settings_for(LaunchMemo& memo, Kern kern, size_t smem, int threads, b
     if (!one_per_sm && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess)
       return SPEC_ERR_LAUNCH;
     if (per_sm < 1) return SPEC_ERR_UNSUPPORTED;
-    memo.grid[dev] = sms * per_sm > kMaxGrid ? kMaxGrid : sms * per_sm;
+    memo.grid[dev] = sms * per_sm > max_grid ? max_grid : sms * per_sm;
     memo.grid_smem[dev] = smem;
   }
   st->grid = memo.grid[dev];
@@ -175,14 +176,14 @@ static LaunchMemo& memo_tc() {
 template <int D, int MT>
 static int settings_main(int batch, Settings* st) {
   return settings_for(memo_main<D, MT>(), verify_attention_kernel<D, MT>, smem_bytes<D, MT>(batch), kThreads,
-                      false, st);
+                      false, kMaxGrid, st);
 }
 
-// The tcgen05 kernel runs one CTA per SM.
+// The tcgen05 kernel runs one CTA per SM (at most tc::kMaxGrid CTAs).
 template <int D, int MT, int S, int NP, int SV = S, int SQ = S>
 static int settings_tc(int batch, Settings* st) {
   return settings_for(memo_tc<D, MT, S, NP, SV, SQ>(), tc::verify_attention_tc_kernel<D, MT, S, NP, SV, SQ>,
-                      tc::smem_bytes<D, MT, S, NP, SV, SQ>(batch), tc::kThreads, true, st);
+                      tc::smem_bytes<D, MT, S, NP, SV, SQ>(batch), tc::kThreads, true, tc::kMaxGrid, st);
 }
 
 template <int D, int MT>

@@ -33,6 +33,7 @@ constexpr int kRegBudgetThreads = 384;
 constexpr int kBarGroup0 = 2;                // named barriers: one per softmax warpgroup,
 constexpr int kBarSoftmax = 4;               // all softmax warps,
 constexpr int kBarTail = 5;                  // MMA warp + softmax warps
+constexpr int kMaxGrid = 160;                // one CTA per SM, at most; a split unit has at most this many pieces
 constexpr int kTmemCols = 256;               // S^T buffers at columns 0 and N, O^T halves from 2N
 
 template <int D, int MT>
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   static_assert(2 * S + 2 * SV + 2 + 2 + NP + 2 <= 64, "barriers fit their area");
   // ring, query buffers and P buffers: contiguous, idle when split units are merged
   constexpr uint32_t kMergeArea = (uint32_t)((S + SV) * C::TILE_BYTES + SQ * C::Q_BYTES + NP * 2 * C::P_BYTES);
-  static_assert(kMergeArea >= 2 * N * D * 4 + 512 + 16 + N * 4 + 16, "the merge holds its rows and one piece");
+  static_assert(kMergeArea >= 2 * N * D * 4 + 512 + kMaxGrid * N * 4 + 16, "the merge holds its rows, the weights and one piece");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;                                // S K tiles, then SV V tiles
@@ -596,56 +597,60 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
       const Fin& F = pend[k];
       // out[row] = sum_pieces w_p[row] * partial_p[row], w_p = 2^(lse_p - M) / sum 2^(lse - M).
       // The K/V ring, query and P buffers are idle now and form one contiguous area:
-      // [out rows][row max, 1/sum][chunk weights][chunk pieces]. Pieces arrive by bulk
-      // copies, a chunk at a time, and the merged rows leave the same way.
-      const int nr = p.n_rows;
+      // [out rows][row max, 1/sum][lse, then weights, of every piece][a chunk of pieces].
+      // Pieces arrive by bulk copies, a chunk at a time (the first while the weights
+      // are worked out), and the merged rows leave the same way.
+      const int nr = p.n_rows, nseg = F.nseg;
       const uint32_t piece_bytes = (uint32_t)(nr * D * 4);
       float* ostage = reinterpret_cast<float*>(ring);
       float* rmax = ostage + nr * D;
       float* rinv = rmax + 64;
-      float* wchunk = rinv + 64;
-      const int cap = (int)((kMergeArea - piece_bytes - 512 - 16) / (piece_bytes + (uint32_t)nr * 4));
-      uint8_t* pieces = reinterpret_cast<uint8_t*>(ring) + ((kMergeArea - (uint32_t)cap * piece_bytes) & ~15u);
-      if (st == 0) bulk_wait_read();  // the previous merge's rows have left the area
-      if (st < nr) {
-        // one thread per row: running max and sum of 2^lse over the pieces
+      float* wts = rinv + 64;  // [nseg][nr]
+      const uint32_t head = piece_bytes + 512 + (((uint32_t)(nseg * nr * 4) + 15u) & ~15u);
+      const int cap = (int)((kMergeArea - head) / piece_bytes);  // >= 1: nseg <= grid <= kMaxGrid
+      uint8_t* pieces = reinterpret_cast<uint8_t*>(ring) + head;
+      auto load_chunk = [&](int p0) {  // one thread
+        const int np_ = min(cap, nseg - p0);
+        mbar_arrive_expect_tx(merge_bar, (uint32_t)np_ * piece_bytes);
+        for (int q = 0; q < np_; ++q)
+          bulk_g2s(smem_u32(pieces + q * piece_bytes),
+                   p.opart + (int64_t)piece_slot(F.c0 + p0 + q, F.c0, F.u0, W) * nr * D, piece_bytes, merge_bar);
+      };
+      if (st == 0) {
+        bulk_wait_read();            // the previous merge's rows have left the area
+        fence_proxy_async_global();  // the acquired pieces are read by the async proxy
+        load_chunk(0);
+      }
+      for (int t = st; t < nseg * nr; t += kSoftmaxThreads) {
+        const int q = t / nr, r = t - q * nr;
+        wts[t] = __ldcg(p.lse + (int64_t)piece_slot(F.c0 + q, F.c0, F.u0, W) * nr + r);
+      }
+      named_sync(kBarSoftmax, kSoftmaxThreads);
+      if (st < nr) {  // one thread per row: max and sum of 2^lse over the pieces
         const int r = st;
         float M = -INFINITY, ws = 0.f;
         bool nan = false;
-        for (int sg0 = 0; sg0 < F.nseg; sg0 += 4) {
-          float l[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            l[u] = sg0 + u < F.nseg ? __ldcg(p.lse + (int64_t)piece_slot(F.c0 + sg0 + u, F.c0, F.u0, W) * nr + r)
-                                    : -INFINITY;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            nan |= l[u] != l[u];
-            if (!(l[u] > -INFINITY)) continue;
-            const float Mn = fmaxf(M, l[u]);
-            ws = ws * exp2f(M - Mn) + exp2f(l[u] - Mn);
-            M = Mn;
-          }
+        for (int q = 0; q < nseg; ++q) {
+          const float lv = wts[q * nr + r];
+          nan |= lv != lv;
+          if (!(lv > -INFINITY)) continue;
+          const float Mn = fmaxf(M, lv);
+          ws = ws * exp2f(M - Mn) + exp2f(lv - Mn);
+          M = Mn;
         }
         rmax[r] = M;
         rinv[r] = (nan || ws == 0.f) ? 0.f : 1.f / ws;  // 0: invalid piece or no key seen
       }
       named_sync(kBarSoftmax, kSoftmaxThreads);
-      for (int p0 = 0; p0 < F.nseg; p0 += cap) {
-        const int np_ = min(cap, F.nseg - p0);
-        if (st == 0) {
-          fence_proxy_async_global();  // the acquired pieces are read by the async proxy
-          mbar_arrive_expect_tx(merge_bar, (uint32_t)np_ * piece_bytes);
-          for (int q = 0; q < np_; ++q)
-            bulk_g2s(smem_u32(pieces + q * piece_bytes),
-                     p.opart + (int64_t)piece_slot(F.c0 + p0 + q, F.c0, F.u0, W) * nr * D, piece_bytes, merge_bar);
-        }
-        for (int t = st; t < np_ * nr; t += kSoftmaxThreads) {
-          const int q = t / nr, r = t - q * nr;
-          const float lv = __ldcg(p.lse + (int64_t)piece_slot(F.c0 + p0 + q, F.c0, F.u0, W) * nr + r);
-          wchunk[t] = (rinv[r] == 0.f || !(lv > -INFINITY)) ? 0.f : exp2f(lv - rmax[r]) * rinv[r];
-        }
-        named_sync(kBarSoftmax, kSoftmaxThreads);  // chunk weights are visible
+      for (int t = st; t < nseg * nr; t += kSoftmaxThreads) {
+        const int r = t % nr;
+        const float lv = wts[t];
+        wts[t] = (rinv[r] == 0.f || !(lv > -INFINITY)) ? 0.f : exp2f(lv - rmax[r]) * rinv[r];
+      }
+      named_sync(kBarSoftmax, kSoftmaxThreads);  // weights are visible
+      for (int p0 = 0; p0 < nseg; p0 += cap) {
+        const int np_ = min(cap, nseg - p0);
+        if (p0 > 0 && st == 0) load_chunk(p0);
         if (!mbar_wait_bounded(merge_bar, (uint32_t)(merge_phase & 1)) && st == 0)
           raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
         ++merge_phase;
@@ -653,7 +658,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
           const int r = idx / (D / 4);
           float4 a = p0 == 0 ? make_float4(0.f, 0.f, 0.f, 0.f) : reinterpret_cast<const float4*>(ostage)[idx];
           for (int q = 0; q < np_; ++q) {
-            const float w = wchunk[q * nr + r];
+            const float w = wts[(p0 + q) * nr + r];
             if (w == 0.f) continue;  // an invalid piece, or one that saw no key of the row
             const float4 v = reinterpret_cast<const float4*>(pieces + q * piece_bytes)[idx];
             a.x += w * v.x;
