@@ -183,7 +183,7 @@ static int settings_main(int batch, Settings* st) {
 template <int D, int MT, int S, int NP, int SV = S, int SQ = S>
 static int settings_tc(int batch, Settings* st) {
   return settings_for(memo_tc<D, MT, S, NP, SV, SQ>(), tc::verify_attention_tc_kernel<D, MT, S, NP, SV, SQ>,
-                      tc::smem_bytes<D, MT, S, NP, SV, SQ>(batch), tc::kThreads, true, tc::kMaxGrid, st);
+                      tc::smem_bytes<D, MT, S, NP, SV, SQ>(batch), tc::Cfg<D, MT>::kThreads, true, tc::kMaxGrid, st);
 }
 
 template <int D, int MT>
@@ -196,7 +196,8 @@ static int launch_main(const Params& p, const Settings& st, const CUtensorMap& t
 template <int D, int MT, int S, int NP, int SV = S, int SQ = S>
 static int launch_tc(const Params& p, const Settings& st, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, cudaStream_t stream) {
-  tc::verify_attention_tc_kernel<D, MT, S, NP, SV, SQ><<<st.grid, tc::kThreads, st.smem, stream>>>(p, tq, tk, tv);
+  tc::verify_attention_tc_kernel<D, MT, S, NP, SV, SQ><<<st.grid, tc::Cfg<D, MT>::kThreads, st.smem, stream>>>(p, tq, tk,
+                                                                                                     tv);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_LAUNCH;
 }
 

@@ -8,8 +8,9 @@
 // halves of 128 lanes (dims 0-127 and 128-255), each the accumulator of its
 // own M = 128 P.V MMA, at consecutive column blocks. Warp 0 stages K/V/Q with
 // TMA, warp 1 issues the MMAs (one thread; QK of tile i+1 before P.V of tile
-// i), warps 2-9 run the softmax in two warpgroups, each owning half of the
-// rows; a warp reads the 32-lane quarter of tensor memory that its index
+// i), the other warps run the softmax in two warpgroups (16 rows) or four (32
+// or 64 rows), each owning an equal share of the rows; a warp reads the
+// 32-lane quarter of tensor memory that its index
 // selects, i.e. 32 keys of S^T and 32 dims of O^T. P is written to shared
 // memory as a bf16 high part and a bf16 remainder and both are multiplied with
 // V. The running row max may lag by up to 8 (log2 units); a tile that exceeds
@@ -24,22 +25,30 @@ namespace attn {
 namespace tc {
 
 constexpr int TK = 128;                      // keys per tile (MMA M)
-constexpr int kSoftmaxWarps = 8;             // two warpgroups, each owning half the query rows
-constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
-constexpr int kThreads = 64 + kSoftmaxThreads;  // producer warp, MMA warp, softmax warps
-// Register budget: up to three warps share an SM sub-partition (16K registers),
-// so a thread may hold at most 168 registers; declaring 384 threads caps it there.
-constexpr int kRegBudgetThreads = 384;
-constexpr int kBarGroup0 = 2;                // named barriers: one per softmax warpgroup,
-constexpr int kBarSoftmax = 4;               // all softmax warps,
-constexpr int kBarTail = 5;                  // MMA warp + softmax warps
+constexpr int kBarSoftmax = 4;               // named barriers: all softmax warps,
+constexpr int kBarTail = 5;                  // MMA warp + softmax warps,
+constexpr int kBarGroup0 = 6;                // one per softmax warpgroup
 constexpr int kMaxGrid = 160;                // one CTA per SM, at most; a split unit has at most this many pieces
 constexpr int kTmemCols = 256;               // S^T buffers at columns 0 and N, O^T halves from 2N
 
 template <int D, int MT>
 struct Cfg {
   static constexpr int N = 16 * MT;                     // packed query rows (MMA N)
-  static constexpr int CW = N / 2;                      // rows (tensor-memory columns) per warpgroup
+  // Softmax warpgroups: each owns N / NG rows of every tile. Four where they were
+  // measured faster (D = 128 with 64 rows, D = 256 with 32): 16 softmax warps hide
+  // the tensor-memory, exponential and shared-memory latency of a tile better than
+  // 8 holding twice the rows each. Elsewhere the 96-register cap of 18 warps
+  // spills, and two warpgroups stay.
+  static constexpr int NG = (D == 128 && MT == 4) || (D == 256 && MT == 2) ? 4 : 2;
+  static constexpr int CW = N / NG;                     // rows (tensor-memory columns) per warpgroup
+  static constexpr int kSoftmaxWarps = 4 * NG;
+  static constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+  static constexpr int kThreads = 64 + kSoftmaxThreads;  // producer warp, MMA warp, softmax warps
+  // Register budget: registers are split over the four SM sub-partitions (16K each),
+  // and 10 warps put up to three on one (168 registers a thread), 18 warps up to five
+  // (96); declaring 384 or 576 threads caps ptxas there.
+  static constexpr int kRegBudgetThreads = NG == 2 ? 384 : 576;
+  static_assert(CW % 8 == 0, "a softmax thread stores its rows of P 8 at a time");
   static constexpr int SUBS = D / 64;                   // 128-byte-wide column slices
   static constexpr int HALVES = D / 128;                // O^T halves of 128 lanes
   static constexpr int TILE_BYTES = TK * D * 2;         // SUBS [128][64] slices: 32 KB (D = 128), 64 KB
@@ -126,11 +135,12 @@ __device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const float (&v)
 // released separately, so the rings may differ in depth: a K tile is refilled
 // once its QK is done, a V tile once its P.V is done.
 template <int D, int MT, int S, int NP, int SV = S, int SQ = S>
-__global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kernel(
+__global__ void __launch_bounds__(Cfg<D, MT>::kRegBudgetThreads, 1) verify_attention_tc_kernel(
     const Params p, const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v) {
   using C = Cfg<D, MT>;
   constexpr int N = C::N, CW = C::CW;
+  constexpr int kSoftmaxWarps = C::kSoftmaxWarps, kSoftmaxThreads = C::kSoftmaxThreads, kThreads = C::kThreads;
   static_assert(SQ == 1 || SQ >= S, "a query buffer is reused only after the K stage that covers it");
   static_assert(2 * S + 2 * SV + 2 + 2 + NP + 2 <= 64, "barriers fit their area");
   // ring, query buffers and P buffers: contiguous, idle when split units are merged
@@ -170,9 +180,10 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     const int per = (B + kThreads - 1) / kThreads;
     const int b0 = tid * per;
     int mine = 0, nt_min = INT32_MAX, nt_max = 0;  // tile counts of the usable sequences
+    static_assert(kThreads / 32 <= 30, "per-warp scan slots stay below the tile-count slots");
     if (tid == 0) {
-      s_misc[12] = INT32_MAX;
-      s_misc[13] = 0;
+      s_misc[30] = INT32_MAX;
+      s_misc[31] = 0;
     }
     for (int i = 0; i < per; ++i) {
       const int b = b0 + i;
@@ -195,8 +206,8 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
     if (lane == 31) s_misc[warp] = incl;
     __syncthreads();
     if (nt_max > 0) {
-      atomicMin(&s_misc[12], nt_min);
-      atomicMax(&s_misc[13], nt_max);
+      atomicMin(&s_misc[30], nt_min);
+      atomicMax(&s_misc[31], nt_max);
     }
     int run = incl - mine;
     for (int w = 0; w < warp; ++w) run += s_misc[w];
@@ -238,7 +249,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   }
   const int64_t T = (int64_t)s_prefix[B] * Hkv;
   if (T == 0) return;
-  const int unit_tiles = s_misc[12] == s_misc[13] ? s_misc[13] : 0;  // 0: units of several lengths
+  const int unit_tiles = s_misc[30] == s_misc[31] ? s_misc[31] : 0;  // 0: units of several lengths
   const int64_t W = tiles_per_cta(T, unit_tiles, (int)gridDim.x);
   const int64_t f0 = (int64_t)blockIdx.x * W;
   const int64_t f1 = min(T, f0 + W);
@@ -434,7 +445,7 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   }
 
   // =================== softmax / epilogue warps ===================
-  const int sw = warp - 2;             // 0..7
+  const int sw = warp - 2;             // 0 .. kSoftmaxWarps - 1
   const int h = sw >> 2;               // warpgroup: rows [h*CW, h*CW + CW)
   const int c0 = h * CW;
   const int q4 = warp & 3;             // tensor-memory lane quarter of this warp
@@ -443,9 +454,10 @@ __global__ void __launch_bounds__(kRegBudgetThreads, 1) verify_attention_tc_kern
   const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
   const int key_in_tile = q4 * 32 + lane;  // the S^T lane this thread reads
   const int bar_group = kBarGroup0 + h;
-  // Running row max: registers, or shared memory for 64-row tiles (register budget);
+  // Running row max: registers, or shared memory for 16 rows a thread under the
+  // 96-register cap and 32 under the 168-register one (register budget);
   // every thread of a warpgroup holds the same values for its rows.
-  constexpr bool kMaxInSmem = CW >= 32;
+  constexpr bool kMaxInSmem = CW >= (C::NG == 4 ? 16 : 32);
   float l_part[CW], m_reg[kMaxInSmem ? 1 : CW];
 #pragma unroll
   for (int e = 0; e < CW; ++e) l_part[e] = 0.f;
