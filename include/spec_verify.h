@@ -246,7 +246,9 @@ int spec_verify_attention_plan(const spec_attn_desc* d, int32_t k_draft, spec_at
  *  accept_len    [B] int32: m in [0, k]
  *
  * Rows are read only up to the first rejection (early exit), so the bytes read
- * depend on the outcome. Each row is handled by one thread-block cluster; the
+ * depend on the outcome; when the batch's rows are small (B * V * 4 bytes at
+ * most 32 MB), the first float4 batch of each thread's slice of position j + 1
+ * is also loaded while position j is decided. Each row is handled by one thread-block cluster; the
  * call picks the threads per CTA and the CTAs per cluster so that every row of
  * the batch is resident at once where that fits (clusters walk several rows
  * otherwise). The environment variable SPEC_ACCEPT_CONFIG=TxC (T = 128 or 256

@@ -63,6 +63,7 @@ constexpr int kMaxK = 31;
 constexpr int kMaxVocab = 1 << 30;
 constexpr int kNB = 8;  // float4 groups per thread in flight together (statistics, argmax)
 constexpr int kRB = 2;  // float4 groups per thread in flight together (race: logits and draft probabilities)
+constexpr int64_t kPrefetchMaxBytes = 32ll << 20;  // position reads over the batch, at most, to prefetch
 
 struct Params {
   const float* logits;
@@ -75,7 +76,8 @@ struct Params {
   int32_t* dev_err;
   uint32_t seed_lo, seed_hi;
   int batch, k, vocab, slice, csize;
-  int vec;  // 1: rows are 16-byte aligned, use float4 loads
+  int vec;       // 1: rows are 16-byte aligned, use float4 loads
+  int prefetch;  // 1: load position j + 1's first batch while position j is decided
 };
 
 // A partial pushed by one warp for one exchange.
@@ -386,9 +388,11 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
       return kv > 0.f ? win : -1;
     };
 
+    bool prefetched = false;  // v holds position j's first batch already
     for (int j = 0; j <= k; ++j) {
       const float* src = lrow + (int64_t)j * V;
-      if (j > 0) load_batch(src, 0, v);
+      if (j > 0 && !prefetched) load_batch(src, 0, v);
+      prefetched = false;
       if (greedy) {
         // ---- argmax of the slice (lowest index on ties), then of the row. The
         // thread visits its entries in increasing index order; a batch whose
@@ -412,6 +416,10 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
           gb += kStep;
           if (gb >= ngroups) break;
           load_batch(src, gb, v);
+        }
+        if (p.prefetch && j < k) {  // position j + 1's first batch, in flight while j is decided
+          load_batch(src + V, 0, v);
+          prefetched = true;
         }
         warp_best(bv, idx);
         const Part* x = exchange(bv, 0.f, idx);
@@ -451,6 +459,10 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
         gb += kStep;
         if (gb >= ngroups) break;
         load_batch(src, gb, v);
+      }
+      if (p.prefetch && j < k) {  // position j + 1's first batch, in flight while j is decided
+        load_batch(src + V, 0, v);
+        prefetched = true;
       }
       float s = (s0 + s1) + (s2 + s3);
 #pragma unroll
@@ -629,6 +641,12 @@ extern "C" int spec_accept(const float* target_logits, const int32_t* draft_toke
   const bool aligned = (vocab % 4 == 0) && ((reinterpret_cast<uintptr_t>(target_logits) & 15) == 0) &&
                        (draft_probs == nullptr || (reinterpret_cast<uintptr_t>(draft_probs) & 15) == 0);
   p.vec = aligned ? 1 : 0;
+  // Fetching the next position's first batch before a decision saves a rejected
+  // row nothing and an accepting row one load round trip. Where every row's
+  // position reads are small (at most 32 MB per position over the batch) the
+  // extra reads are free and accepting rows gain; on larger batches they
+  // compete with the rows that race after rejecting at position 0.
+  p.prefetch = (int64_t)batch * vocab * 4 <= acc::kPrefetchMaxBytes ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
