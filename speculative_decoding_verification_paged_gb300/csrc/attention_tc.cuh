@@ -8,9 +8,9 @@
 // halves of 128 lanes (dims 0-127 and 128-255), each the accumulator of its
 // own M = 128 P.V MMA, at consecutive column blocks. Warp 0 stages K/V/Q with
 // TMA, warp 1 issues the MMAs (one thread; QK of tile i+1 before P.V of tile
-// i), the other warps run the softmax in two warpgroups (16 rows) or four (32
-// or 64 rows), each owning an equal share of the rows; a warp reads the
-// 32-lane quarter of tensor memory that its index
+// i), the other warps run the softmax in two warpgroups or, for 64 rows at
+// D = 128 and 32 rows at D = 256, four, each owning an equal share of the
+// rows; a warp reads the 32-lane quarter of tensor memory that its index
 // selects, i.e. 32 keys of S^T and 32 dims of O^T. P is written to shared
 // memory as a bf16 high part and a bf16 remainder and both are multiplied with
 // V. The running row max may lag by up to 8 (log2 units); a tile that exceeds
