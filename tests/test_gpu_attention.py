@@ -280,3 +280,23 @@ def test_attention_one_unit_split_over_every_cta(sv, oracle_mod, attn_kernel, Hq
     assert err == 0
     mx, rel = attention_errors(out.cpu().numpy(), oracle_attention_for(oracle_mod, a))
     assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+
+
+@pytest.mark.parametrize("D,k,G", [(128, 7, 8), (256, 3, 8)], ids=["d128_rows64", "d256_rows32"])
+def test_attention_bad_block_inside_a_split_unit(sv, oracle_mod, attn_kernel, D, k, G):
+    """Two long sequences over one kv head, so each unit is cut into dozens of
+    pieces and merged in several chunks; sequence 0 has an out-of-range block id
+    in the middle of its context. Its rows must come out zero (the piece holding
+    the bad block marks itself unusable and the merge drops the unit), the error
+    bit is raised, and sequence 1 still matches the oracle. The shapes are the
+    ones the tcgen05 kernel runs with four softmax warpgroups."""
+    w = wl.Workload(name="bad_split", batch=2, ctx_lens=(60000, 50000), block_size=64, num_q_heads=G,
+                    num_kv_heads=1, head_dim=D, k_draft=k, seed=17 + D)
+    a = wl.make_attention_inputs(w, device=DEV)
+    a["block_table"][0, 400] = a["num_blocks"] + 7
+    out, err = run_attention(sv, a, w)
+    assert err & sv.DEVERR["block_id"]
+    assert torch.all(out[0] == 0)
+    ref = oracle_attention_for(oracle_mod, a, seqs=np.array([1], np.int32))
+    mx, rel = attention_errors(out[[1]].cpu().numpy(), ref)
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
