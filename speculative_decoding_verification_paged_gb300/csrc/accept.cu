@@ -25,8 +25,10 @@
 // resident at once, and the clusters walk the rows (persistent) when the batch
 // is larger than that. Each warp combines its lanes by shuffles and pushes the
 // result straight into an exchange slot of every CTA of the cluster
-// (distributed shared memory), and one cluster barrier per position publishes
-// them: there is no CTA-wide barrier on the path. Every warp of every CTA then
+// (distributed shared memory, an asynchronous store that counts its bytes on the
+// receiving CTA's mbarrier), and each CTA waits on its own mbarrier until every
+// partial of the exchange has landed: there is no CTA-wide or cluster-wide
+// barrier on the path. Every warp of every CTA then
 // combines the same partials in the same order, so all CTAs reach
 // bit-identical decisions. Lane j of every warp holds draft j with its target
 // logit and draft probability, read by shuffle at the decisions.
@@ -90,11 +92,14 @@ struct __align__(16) Part {
 
 struct Shared {
   // Exchange, push model: warp w of CTA r writes its partial into slot
-  // [r * warps + w] of every CTA of the cluster before a cluster barrier, so
-  // everything read after the barrier is local. Two slots alternate: a CTA
-  // writes slot e & 1 of exchange e only after the barrier of exchange e - 1,
-  // which every CTA reaches after reading exchange e - 2 from the same slot.
+  // [r * warps + w] of every CTA of the cluster with an asynchronous store that
+  // counts its 16 bytes on that CTA's mbarrier xbar[e & 1], so everything read
+  // after the wait is local. Two slots alternate: a CTA pushes exchange e only
+  // after its own exchange e - 1 completed, which needs every peer's push of
+  // e - 1, which each peer makes after it has read exchange e - 2 from the same
+  // slot (its next push depends on what it read).
   Part xch[2][kMaxCluster * kMaxWarps];
+  uint64_t xbar[2];  // phase k of xbar[s] completes with exchange 2k + s
 };
 
 // Split cluster barrier used once at start-up: every CTA arrives as soon as it
@@ -147,6 +152,36 @@ constexpr int kRaceResidual = 1;  // w = max(0, p - q)
 constexpr int kRaceOneHot = 2;    // w = max(0, p - [x == d])  (no draft probabilities)
 
 // Registers bound the CTAs resident per SM (1024 threads at 64 registers each).
+// 16-byte asynchronous store into a peer CTA's shared memory that also counts its
+// bytes on the peer's mbarrier (complete_tx); both are shared::cluster addresses.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, int32_t c, int32_t d, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(addr),
+               "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(c), "r"(d), "r"(bar)
+               : "memory");
+}
+// Wait (bounded) for the phase of this CTA's mbarrier with the given parity, with
+// cluster-scope acquire: the data peers stored into this CTA is visible after it.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, long long limit_cycles = 2000000000LL) {
+  auto try_wait = [&]() -> bool {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_wait()) return true;
+  const long long start = clock64();
+  while (!try_wait()) {
+    if (clock64() - start > limit_cycles) return false;
+  }
+  return true;
+}
 template <int T>
 __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
   constexpr int kWarps = T / 32;
@@ -166,6 +201,12 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
   const float4 kZero4 = make_float4(0.f, 0.f, 0.f, 0.f);
   int xs = 0;           // exchanges so far (slot parity)
   bool joined = false;  // the start-up cluster barrier was waited on
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.xbar[0], 1);  // the local arrival sets the exchange's byte count
+    mbar_init(&sh.xbar[1], 1);
+    fence_mbar_init();  // visible to the cluster before any peer can push
+  }
+  __syncthreads();
   cluster_arrive_relaxed();
 
   // Group g of a slice in global memory, checked: one 16-byte load when rows are
@@ -213,12 +254,16 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
   };
   // Push this warp's partial (the same in all its lanes) into every CTA of the
   // cluster, then wait for the cluster's partials; returns the slot to read.
+  // Every CTA of the cluster makes the same exchanges in the same order.
   auto exchange = [&](float f0, float f1, int i0) -> const Part* {
     const int slot = xs & 1;
+    const uint32_t parity = (uint32_t)((xs >> 1) & 1);
     ++xs;
+    if (tid == 0) mbar_arrive_expect_tx(&sh.xbar[slot], (uint32_t)(nparts * (int)sizeof(Part)));
     if (lane < csize)
-      st_cluster_v4(map_to_rank(smem_u32(&sh.xch[slot][rank * kWarps + warp]), (uint32_t)lane), f0, f1, i0, 0);
-    cluster_sync_all();
+      st_async_v4(map_to_rank(smem_u32(&sh.xch[slot][rank * kWarps + warp]), (uint32_t)lane), f0, f1, i0, 0,
+                  map_to_rank(smem_u32(&sh.xbar[slot]), (uint32_t)lane));
+    if (!mbar_wait_cluster_bounded(&sh.xbar[slot], parity) && lane == 0) raise_error(p.dev_err, SPEC_DEVERR_TIMEOUT);
     return sh.xch[slot];
   };
   // (best value, lowest index) over the exchanged partials.
@@ -501,9 +546,9 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
     }
   }
   if (!joined) cluster_wait();
-  // No cluster barrier at the end: every remote access (a push) precedes the
-  // barrier of its exchange, and nothing after it reads or writes another
-  // CTA's memory.
+  // No cluster barrier at the end: every push into this CTA belongs to an
+  // exchange it has waited for, and nothing after the last one reads or writes
+  // another CTA's memory.
 }
 
 // ---------------------------------------------------------------------------
