@@ -310,15 +310,17 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
       continue;
     }
     const bool greedy = md == SPEC_MODE_GREEDY;
-    // Lane j of every warp holds draft j, its target logit and its draft
-    // probability; decisions read them by shuffle. They are first used at
+    // Lane j of every warp holds draft j, its target logit, its draft
+    // probability and the uniform of its test; decisions read them by shuffle. They are first used at
     // position 0's decision, so their loads arrive while the slice streams in.
     // Without draft probabilities the draft distribution is one-hot at the
     // drafted token.
-    float l_d = 0.f, q_d = 1.f;
+    float l_d = 0.f, q_d = 1.f, u_d = 0.f;
     if (lane < k && !greedy) {
       l_d = __ldg(p.logits + ((int64_t)b * R + lane) * V + d_lane);
       if (p.probs) q_d = __ldg(p.probs + ((int64_t)b * k + lane) * V + d_lane);
+      // the uniform of draft j's test, off the chain of decisions
+      u_d = word_to_uniform(philox4x32_10(0u, (uint32_t)lane, (uint32_t)b, 0u, p.seed_lo, p.seed_hi).v[0]);
     }
     const float c2 = (1.0f / T_) * 1.4426950408889634f;  // logit -> log2 units of p
     if (!joined) {
@@ -528,8 +530,7 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
       if (j < k) {
         const float pd = fast_exp2((__shfl_sync(0xffffffffu, l_d, j) - M) * c2) / Z;
         const float qd = __shfl_sync(0xffffffffu, q_d, j);
-        const Philox4 wu = philox4x32_10(0u, (uint32_t)j, (uint32_t)b, 0u, p.seed_lo, p.seed_hi);
-        const float u = word_to_uniform(wu.v[0]);
+        const float u = __shfl_sync(0xffffffffu, u_d, j);
         if (u * qd < pd) continue;
         // ---- rejected at j: race over max(0, p_j - q_j), or over p_j if that is all zero
         if (p.probs)
