@@ -151,17 +151,17 @@ constexpr int kRacePlain = 0;     // w = p (bonus token, or an all-zero residual
 constexpr int kRaceResidual = 1;  // w = max(0, p - q)
 constexpr int kRaceOneHot = 2;    // w = max(0, p - [x == d])  (no draft probabilities)
 
-// Registers bound the CTAs resident per SM (1024 threads at 64 registers each).
 // 16-byte asynchronous store into a peer CTA's shared memory that also counts its
 // bytes on the peer's mbarrier (complete_tx); both are shared::cluster addresses.
 __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, int32_t c, int32_t d, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(addr),
-               "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(c), "r"(d), "r"(bar)
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n"
+               ::"r"(addr), "r"(__float_as_uint(a)), "r"(__float_as_uint(b)), "r"(c), "r"(d), "r"(bar)
                : "memory");
 }
 // Wait (bounded) for the phase of this CTA's mbarrier with the given parity, with
 // cluster-scope acquire: the data peers stored into this CTA is visible after it.
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, long long limit_cycles = 2000000000LL) {
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity,
+                                                          long long limit_cycles = 2000000000LL) {
   auto try_wait = [&]() -> bool {
     uint32_t ok;
     asm volatile(
@@ -182,6 +182,7 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
   }
   return true;
 }
+// Registers bound the CTAs resident per SM (1024 threads at 64 registers each).
 template <int T>
 __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
   constexpr int kWarps = T / 32;
@@ -311,10 +312,10 @@ __global__ void __launch_bounds__(T, 1024 / T) accept_kernel(const Params p) {
     }
     const bool greedy = md == SPEC_MODE_GREEDY;
     // Lane j of every warp holds draft j, its target logit, its draft
-    // probability and the uniform of its test; decisions read them by shuffle. They are first used at
-    // position 0's decision, so their loads arrive while the slice streams in.
-    // Without draft probabilities the draft distribution is one-hot at the
-    // drafted token.
+    // probability and the uniform of its test; decisions read them by shuffle.
+    // They are first used at position 0's decision, so their loads arrive while
+    // the slice streams in. Without draft probabilities the draft distribution
+    // is one-hot at the drafted token.
     float l_d = 0.f, q_d = 1.f, u_d = 0.f;
     if (lane < k && !greedy) {
       l_d = __ldg(p.logits + ((int64_t)b * R + lane) * V + d_lane);
