@@ -248,13 +248,14 @@ int spec_verify_attention_plan(const spec_attn_desc* d, int32_t k_draft, spec_at
  * Rows are read only up to the first rejection (early exit), so the bytes read
  * depend on the outcome; when the batch's rows are small (B * V * 4 bytes at
  * most 32 MB), the first float4 batch of each thread's slice of position j + 1
- * is also loaded while position j is decided. Each row is handled by one thread-block cluster; the
- * call picks the threads per CTA and the CTAs per cluster so that every row of
- * the batch is resident at once where that fits (clusters walk several rows
- * otherwise). The environment variable SPEC_ACCEPT_CONFIG=TxC (T = 128 or 256
- * threads, C = 1, 2, 4, 8 or 16 CTAs per cluster) forces one configuration,
- * for tests and measurements; one the vocabulary cannot use (fewer than 4T
- * logits per CTA with C > 1) makes the call return SPEC_ERR_LAUNCH.
+ * is also loaded while position j is decided. Each row is handled by one
+ * thread-block cluster; the call picks the threads per CTA and the CTAs per
+ * cluster so that every row of the batch is resident at once where that fits
+ * (clusters walk several rows otherwise). The environment variable
+ * SPEC_ACCEPT_CONFIG=TxC (T = 128 or 256 threads, C = 1, 2, 4, 8 or 16 CTAs
+ * per cluster) forces one configuration, for tests and measurements; one the
+ * vocabulary cannot use (fewer than 4T logits per CTA with C > 1) makes the
+ * call return SPEC_ERR_LAUNCH.
  * Device errors: a row with a draft token outside [0, V) (SPEC_DEVERR_TOKEN),
  * a sampling row with temperature not > 0 (SPEC_DEVERR_TEMPERATURE), or a mode
  * other than 0/1 (SPEC_DEVERR_MODE) gets out_tokens all -1 and accept_len -1.

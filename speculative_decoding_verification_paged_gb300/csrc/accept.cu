@@ -13,25 +13,26 @@
 // Design (GB300): one thread-block cluster per batch row, its CTAs splitting
 // the vocabulary into contiguous slices (a multiple of 4 logits each, at most
 // 16 CTAs). Positions are processed in order and the row stops at the first
-// rejection, so logits past it are never read (early exit), and nothing is
-// fetched ahead of a decision. The logits stream through registers: each
-// thread loads eight float4 groups of its slice at a time (128-bit loads, all
-// in flight together) and folds them into one partial (the batch maximum
-// first, then one rescale of the running sum of exponentials and one
-// exponential per logit; or a running argmax). Nothing is staged in shared
-// memory, so a CTA holds only its exchange slots and as many CTAs stay
-// resident as the registers allow: the launch picks the CTA size and cluster
-// size that give the most threads per row while every row of the batch is
-// resident at once, and the clusters walk the rows (persistent) when the batch
-// is larger than that. Each warp combines its lanes by shuffles and pushes the
-// result straight into an exchange slot of every CTA of the cluster
-// (distributed shared memory, an asynchronous store that counts its bytes on the
-// receiving CTA's mbarrier), and each CTA waits on its own mbarrier until every
-// partial of the exchange has landed: there is no CTA-wide or cluster-wide
-// barrier on the path. Every warp of every CTA then
-// combines the same partials in the same order, so all CTAs reach
-// bit-identical decisions. Lane j of every warp holds draft j with its target
-// logit and draft probability, read by shuffle at the decisions.
+// rejection, so logits past it are never read (early exit); only when the
+// batch's positions are small (B V 4 bytes at most 32 MB) is each thread's
+// first batch of position j + 1 loaded while position j is decided. The logits
+// stream through registers: each thread loads eight float4 groups of its slice
+// at a time (128-bit loads, all in flight together) and folds them into one
+// partial (the batch maximum first, then one rescale of the running sum of
+// exponentials and one exponential per logit; or a running argmax). Nothing is
+// staged in shared memory, so a CTA holds only its exchange slots and as many
+// CTAs stay resident as the registers allow: the launch picks the CTA size and
+// cluster size that give the most threads per row while every row of the batch
+// is resident at once, and the clusters walk the rows (persistent) when the
+// batch is larger than that. Each warp combines its lanes by shuffles and
+// pushes the result straight into an exchange slot of every CTA of the cluster
+// (distributed shared memory, an asynchronous store that counts its bytes on
+// the receiving CTA's mbarrier), and each CTA waits on its own mbarrier until
+// every partial of the exchange has landed: there is no CTA-wide or
+// cluster-wide barrier on the path. Every warp of every CTA then combines the
+// same partials in the same order, so all CTAs reach bit-identical decisions.
+// Lane j of every warp holds draft j with its target logit, its draft
+// probability and the uniform of its test, read by shuffle at the decisions.
 //
 // The correction / bonus token is the exponential race over the whole
 // vocabulary: entry x has the key w_x / E_x, E_x = -ln U_x, U_x from word
