@@ -60,6 +60,34 @@ def test_accept_parity_named_workloads(sv, oracle_mod, name, mode):
         assert np.all(tok[b, alen[b] + 1:] == -1) and tok[b, alen[b]] >= 0
 
 
+def test_accept_mixed_rows_equal_single_mode_rows(sv):
+    """Rows are independent on the GPU too. In a serving-shaped mixed batch (per-row modes and
+    temperatures), every row gives bit-identical tokens and accept length to the same row in a
+    batch run wholly in its mode, and a sampling row gives the same as when every row has its
+    temperature. The kernel and its launch configuration are the same in every call, so the
+    comparison needs no tolerance."""
+    w = wl.WORKLOADS["serving128"].replace(batch=96)
+    inp = wl.make_accept_inputs(w, device=DEV, mode="mixed")
+    modes = inp["mode"]
+    m = modes.cpu().numpy()
+    assert 0 < m.sum() < len(m)
+    t_mix, a_mix, e = run_accept(sv, inp, modes)
+    assert e == 0
+    t_g, a_g, e = run_accept(sv, inp, torch.zeros_like(modes))
+    assert e == 0
+    t_s, a_s, e = run_accept(sv, inp, torch.ones_like(modes))
+    assert e == 0
+    for b in range(len(m)):
+        rt, ra = (t_s, a_s) if m[b] else (t_g, a_g)
+        assert np.array_equal(t_mix[b], rt[b]) and a_mix[b] == ra[b], b
+    temps = inp["temperature"]
+    for b in np.nonzero(m)[0][:4]:
+        one_t = dict(inp, temperature=torch.full_like(temps, float(temps[b])))
+        t_u, a_u, e = run_accept(sv, one_t, torch.ones_like(modes))
+        assert e == 0
+        assert np.array_equal(t_mix[b], t_u[b]) and a_mix[b] == a_u[b], b
+
+
 def test_accept_greedy_without_draft_probs(sv, oracle_mod):
     w = wl.WORKLOADS["tiny"].replace(batch=64)
     inp = wl.make_accept_inputs(w, device=DEV, mode="greedy")

@@ -537,6 +537,40 @@ def test_sampling_is_deterministic_per_seed(oracle_mod):
     assert not np.array_equal(a[0], c[0])
 
 
+def test_mixed_rows_equal_single_mode_rows(oracle_mod):
+    """Rows are independent: in a batch that mixes greedy and sampling rows with per-row
+    temperatures (the serving configuration), every row's tokens and accept length equal those
+    of the same row (same index, so the same Philox counters) in a batch run wholly in its mode,
+    and a sampling row's equal those it gets when every row of the batch has its temperature. A
+    mode or temperature read from the wrong row fails the comparison; the last check makes sure
+    the temperature changes outcomes at all, so the comparison has power."""
+    rng = np.random.default_rng(17)
+    B, k, V = 48, 3, 97
+    L = rng.normal(0, 2, (B, k + 1, V)).astype(np.float32)
+    temp = rng.uniform(0.5, 1.2, B).astype(np.float32)
+    Q = _softmax((L[:, :k] + rng.normal(0, 1, (B, k, V))) / temp[:, None, None]).astype(np.float32)
+    q64 = Q.astype(np.float64)
+    q64 /= q64.sum(-1, keepdims=True)
+    d = np.array([[rng.choice(V, p=q64[b, j]) for j in range(k)] for b in range(B)], np.int32)
+    mode = (rng.random(B) < 0.5).astype(np.int32)
+    assert 0 < mode.sum() < B
+    seed = 7
+    tok, alen = oracle_mod.accept(L, d, Q, seed, mode, temp)[:2]
+    tg, ag = oracle_mod.accept(L, d, Q, seed, np.zeros(B, np.int32), temp)[:2]
+    ts, as_ = oracle_mod.accept(L, d, Q, seed, np.ones(B, np.int32), temp)[:2]
+    for b in range(B):
+        rt, ra = (ts, as_) if mode[b] else (tg, ag)
+        assert np.array_equal(tok[b], rt[b]) and alen[b] == ra[b], b
+    assert len(set(alen.tolist())) > 1  # a mix of accept lengths, not a degenerate batch
+    changed = 0
+    for b in np.nonzero(mode)[0][:8]:
+        tu, au = oracle_mod.accept(L, d, Q, seed, np.ones(B, np.int32), np.full(B, temp[b], np.float32))[:2]
+        assert np.array_equal(tok[b], tu[b]) and alen[b] == au[b], b
+        tw, aw = oracle_mod.accept(L, d, Q, seed, np.ones(B, np.int32), np.full(B, 4 * temp[b], np.float32))[:2]
+        changed += int(not np.array_equal(tok[b], tw[b]) or alen[b] != aw[b])
+    assert changed > 0
+
+
 def test_accept_invalid_rows(oracle_mod):
     B, k, V = 3, 2, 5
     L = np.zeros((B, k + 1, V), np.float32)
