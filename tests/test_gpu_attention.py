@@ -240,6 +240,30 @@ def test_attention_is_deterministic_and_reuses_workspace(sv, attn_kernel):
     assert torch.equal(o1, o2)
 
 
+@pytest.mark.parametrize("D,Hq", [(128, 64), (256, 24)])
+def test_attention_split_units_merge_this_calls_pieces(sv, oracle_mod, attn_kernel, D, Hq):
+    """Split units are merged from the pieces of the same call. Two inputs with the same shapes
+    (so the same split plan and the same partial slots in one reused workspace) alternate: the
+    first input's output comes back bit-identical and the second's matches the oracle. A merge
+    that read a piece before its CTA had written it would pick up the other input's piece, which
+    the previous call left in the workspace."""
+    w = wl.Workload(name="split_reuse", batch=4, ctx_lens=(30011, 25000, 41000, 18003), block_size=128,
+                    num_q_heads=Hq, num_kv_heads=8 if D == 128 else 4, head_dim=D, k_draft=7 if D == 128 else 3,
+                    seed=21)
+    a = wl.make_attention_inputs(w, device=DEV)
+    b = wl.make_attention_inputs(w.replace(seed=22), device=DEV)
+    ws = sv.new_attention_workspace(
+        sv.spec_verify_attention_workspace(a["q"], a["k_cache"], a["block_table"], w.k_draft), DEV)
+    o1, e1 = run_attention(sv, a, w, workspace=ws)
+    o2, e2 = run_attention(sv, b, w, workspace=ws)
+    o3, e3 = run_attention(sv, a, w, workspace=ws)
+    assert e1 == e2 == e3 == 0
+    assert torch.equal(o1, o3)
+    assert not torch.equal(o1, o2)
+    mx, rel = attention_errors(o2.cpu().numpy(), oracle_attention_for(oracle_mod, b))
+    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+
+
 def test_attention_bad_block_and_bad_ctx_give_zero_rows(sv, oracle_mod, attn_kernel):
     w = wl.Workload(name="bad", batch=4, ctx_lens=(300, 300, 300, 300), block_size=16, num_q_heads=8,
                     num_kv_heads=2, head_dim=128, k_draft=3, seed=5)
