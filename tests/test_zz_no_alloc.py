@@ -5,10 +5,10 @@ engine's per-step enqueue path, a runtime plugin whose enqueue contract
 forbids allocation, a process that reserved all device memory up front).
 For them the library keeps its attention scratch in a fixed array and offers
 this entry point without a workspace argument. The tests call it through the
-C ABI twice in a row (the second call reuses the array the first left behind)
-and require both results to equal, bit for bit, the workspace form of the same
-call (same kernel, same grid, same split plan), and the oracle within the
-attention tolerance.
+C ABI three times in a row on two alternating inputs of the same shapes (each
+call reuses the array the previous one left behind) and require every result
+to equal, bit for bit, the workspace form of the same call (same kernel, same
+grid, same split plan), and the oracle within the attention tolerance.
 
 This file sorts last so that a run stopping at the first failure has already
 run every other test; it also passes on its own in a fresh process.
@@ -50,29 +50,36 @@ def _ragged(name):
 
 
 @pytest.mark.parametrize("name", ["llama8b_eagle3", "tiny", "hybrid_gdn", "longctx"])
-def test_noalloc_matches_workspace_call_twice(sv, oracle_mod, name):
+def test_noalloc_matches_workspace_calls_alternating_inputs(sv, oracle_mod, name):
+    """Three allocation-free calls, on inputs A, B, A of the same shapes (so the same plan and
+    the same scratch slots): each equals, bit for bit, the workspace form on its own input, so
+    no call reads counters or partials that the previous call left in the scratch."""
     lib = sv.load_library()
     assert lib.spec_verify_attention_noalloc_limit() == 32 << 20
     w = _ragged(name)
-    a = wl.make_attention_inputs(w, device=DEV)
+    inputs = [wl.make_attention_inputs(w, device=DEV), wl.make_attention_inputs(w, device=DEV, seed=w.seed + 1)]
     shape = (w.batch, w.rows, w.num_q_heads, w.head_dim)
-    ref = torch.empty(shape, dtype=torch.float32, device=DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    sv.spec_verify_attention(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["ctx_lens"], w.k_draft, ref,
-                             dev_err=err)
+    refs = []
+    for a in inputs:
+        ref = torch.empty(shape, dtype=torch.float32, device=DEV)
+        sv.spec_verify_attention(a["q"], a["k_cache"], a["v_cache"], a["block_table"], a["ctx_lens"], w.k_draft,
+                                 ref, dev_err=err)
+        refs.append(ref)
     outs = []
-    for _ in range(2):
+    for i in (0, 1, 0):
         out = torch.full(shape, float("nan"), dtype=torch.float32, device=DEV)
-        rc = _call_noalloc(sv, lib, a, w, out, err)
+        rc = _call_noalloc(sv, lib, inputs[i], w, out, err)
         assert rc == 0, sv.status_string(rc)
-        outs.append(out)
+        outs.append((i, out))
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    for out in outs:
-        assert torch.equal(out, ref)
-    want = oracle_attention_for(oracle_mod, a)
-    mx, rel = attention_errors(outs[1].cpu().numpy(), want)
-    assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (mx, rel)
+    assert not torch.equal(refs[0], refs[1])
+    for i, out in outs:
+        assert torch.equal(out, refs[i]), i
+    for i in (0, 1):
+        mx, rel = attention_errors(refs[i].cpu().numpy(), oracle_attention_for(oracle_mod, inputs[i]))
+        assert mx <= ATTN_MAX_ABS and rel <= ATTN_REL_L2, (i, mx, rel)
 
 
 @pytest.mark.parametrize("name", ["llama8b_eagle3", "longctx"])
